@@ -1,0 +1,47 @@
+"""The five decode workloads of the CSA2 path, as sizes and seeds.
+
+Each workload is seeded with 1000 + its index. Query token j of n_q sits at
+absolute position t = N - n_q + j, where N counts the entries in the cache
+after the step's new tokens have been appended.
+"""
+from dataclasses import dataclass, field
+
+
+@dataclass(frozen=True)
+class Workload:
+    index: int
+    name: str
+    mode: str           # "full" | "reuse" | "reindex" | "group"
+    B: int              # sequences
+    N: int              # context entries per sequence (after appending the step's tokens)
+    n_q: int = 1        # query tokens per sequence
+    layers: tuple = field(default=("full",))
+
+    @property
+    def seed(self) -> int:
+        return 1000 + self.index
+
+    @property
+    def queries(self) -> int:
+        return self.B * self.n_q
+
+
+WORKLOADS = {
+    0: Workload(0, "full_b1_n32k", "full", B=1, N=32768),
+    1: Workload(1, "reuse_b64_n64k", "reuse", B=64, N=65536, layers=("reuse",)),
+    2: Workload(2, "reindex_b64_n128k", "reindex", B=64, N=131072, layers=("reindex",)),
+    3: Workload(3, "full_b8_n1m", "full", B=8, N=1048576),
+    4: Workload(4, "group_reindex_3reuse_b32_n256k_q6", "group", B=32, N=262144, n_q=6,
+                layers=("reindex", "reuse", "reuse", "reuse")),
+}
+
+# Method constants (decoder CSA2 at m = 1).
+LATENT_DIM = 512
+IDX_HEADS = 32
+IDX_DIM = 128
+Q_HEADS = 64
+TOPK = 512
+POOL_BLOCKS = 2048
+BLOCK = 8
+WINDOW = 128
+PAGE = 128
