@@ -1,0 +1,493 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the CSA2 hot path on GB300.
+
+One step = one decode step of a Full-mode CSA2 layer over the whole batch:
+MXFP4 append of every sequence's new entry (main KV + indexer key) and FP8
+append of its window entry, MXFP4 quantisation of the indexer query, the
+full causal indexer scan with 8-position block maxima, block top-2048, pool
+rescore + top-512, and sparse attention over 512 FP4 entries + the 128-entry
+FP8 window (64 heads x 512, bf16 output).
+
+Default workload: 8 sequences x 1,048,576 context entries, 1 query token
+each (Full mode at 1M context). Other workloads: --workload 0..4.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle on
+the same workload instead (a bounded sample, scaled to queries/s).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode queries/s per CSA2 mode at context N; % of HBM roofline (1xGB300)"
+
+# ncu DRAM traffic of the dominant kernel, per launch, with the hash of the
+# sources it was measured on (reported as null once those sources change).
+NCU_TRAFFIC = {}
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "sparse_attention_fp4_mxfp4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows if len(r) >= 9 for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- algorithmic bytes (reads the method must do) --------------------------------------
+
+def scan_bytes(wl) -> int:
+    """Full scan: 72 B per causal position per sequence (all n_q tokens share
+    the read) + the FP4 indexer query and head weights of each token."""
+    return wl.B * (72 * wl.N + wl.n_q * (32 * 72 + 32 * 4))
+
+
+def attn_bytes_per_query() -> int:
+    # 512 FP4 entries x 288 B + 128 FP8 window entries x 512 B + q (64 x 512 bf16) + top-k.
+    return 512 * 288 + 128 * 512 + 64 * 512 * 2 + 512 * 4
+
+
+def step_bytes(wl) -> int:
+    q = wl.B * wl.n_q
+    if wl.mode == "full":
+        return scan_bytes(wl) + q * attn_bytes_per_query()
+    if wl.mode == "reuse":
+        return q * attn_bytes_per_query()
+    if wl.mode == "reindex":
+        return q * (2048 * 576 + 32 * 72 + 32 * 4 + 2048 * 4 + attn_bytes_per_query())
+    raise ValueError(wl.mode)
+
+
+# ---- our arm ------------------------------------------------------------------------------------
+
+def run_ours(args, wl, rank, world, local):
+    import sparse_attention_fp4_mxfp4_gb300 as csa2
+    from tests import harness as H
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    t_setup = time.time()
+    S = H.build(wl, dev)
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup
+    B, n_q, N = wl.B, wl.n_q, wl.N
+    Q = B * n_q
+    stream = torch.cuda.current_stream()
+    c = S.cache
+    L = S.layers[0]
+    out = torch.empty(B, n_q, 64, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, n_q, 64, dtype=torch.float32, device=dev)
+    ws = torch.empty(csa2.csa2_workspace_bytes(csa2.OP_DECODE_LAYER, B, n_q, N), dtype=torch.uint8, device=dev)
+    pool = torch.empty(B, n_q, 2048, dtype=torch.int32, device=dev)
+    topk = S.topk if wl.mode == "reuse" else torch.empty(B, n_q, 512, dtype=torch.int32, device=dev)
+    max_blocks = (N + 7) // 8
+    bm = ws[: Q * max_blocks * 4].view(torch.float32).view(B, n_q, max_blocks)
+    rws = ws[((Q * max_blocks * 4 + 255) // 256) * 256:]
+    ev = {}
+
+    def mark(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        ev.setdefault(name, []).append(e)
+
+    launches_per_step = 0
+
+    def step(timed_marks):
+        nonlocal launches_per_step
+        n = 0
+        H.append_step(S)
+        n += 1 + len(S.layers)
+        if wl.mode in ("full", "reindex"):
+            csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
+            n += 1
+        if wl.mode == "full":
+            if timed_marks:
+                mark("scan0")
+            csa2.csa2_indexer_scan(L.q_codes, L.q_scales, L.w, S.seq_len, N, c.block_table, c.n_pages,
+                                   c.idx_pages, bm)
+            if timed_marks:
+                mark("scan1")
+            csa2.csa2_block_topk(bm, S.seq_len, pool)
+            n += 2
+        if wl.mode in ("full", "reindex"):
+            p = pool if wl.mode == "full" else L.pool
+            if timed_marks:
+                mark("rescore0")
+            csa2.csa2_indexer_reindex(L.q_codes, L.q_scales, L.w, S.seq_len, c.block_table, c.n_pages,
+                                      c.idx_pages, p, topk, rws)
+            if timed_marks:
+                mark("rescore1")
+            n += 2
+        if timed_marks:
+            mark("attn0")
+        csa2.csa2_sparse_attn(L.q, topk, S.seq_len, c.block_table, c.n_pages, c.main_pages, c.rings,
+                              L.ring_idx, out, lse, ws)
+        if timed_marks:
+            mark("attn1")
+        n += 2
+        launches_per_step = n
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    st = csa2.csa2_check_device_status()
+    if st != csa2.OK:
+        raise RuntimeError("device status after warm-up: " + csa2.device_status_message())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, world, dev)
+    stage_ms = {}
+    for name in ("scan", "rescore", "attn"):
+        if name + "0" in ev:
+            tt = [a.elapsed_time(b) for a, b in zip(ev[name + "0"], ev[name + "1"])]
+            stage_ms[name] = sum(tt) / len(tt)
+    st = csa2.csa2_check_device_status()
+    if st != csa2.OK:
+        raise RuntimeError("device status after timing: " + csa2.device_status_message())
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, S, out, lse, ws, pool, topk, dev)
+
+    peak, peak_kind = measured_peaks()
+    if wl.mode == "full":
+        dom, dom_bytes = "indexer_scan", scan_bytes(wl)
+    elif wl.mode == "reindex":
+        dom, dom_bytes = "indexer_rescore", Q * (2048 * 576 + 32 * 72 + 32 * 4 + 2048 * 4)
+    else:
+        dom, dom_bytes = "sparse_attn", Q * attn_bytes_per_query()
+    dom_ms = stage_ms.get({"indexer_scan": "scan", "indexer_rescore": "rescore", "sparse_attn": "attn"}[dom])
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else None
+    traffic = None
+    rec = NCU_TRAFFIC.get((dom, wl.index))
+    if rec and rec["hash"] == source_hash(rec["files"]):
+        traffic = rec["bytes_per_launch"]
+    total_q = sum_over_ranks(float(Q), world, dev)
+    value = total_q / (ms_max * 1e-3)
+    sb = step_bytes(wl)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "queries/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp4(e2m1)+e4m3 storage, f16 tensor-core operands, fp32 accumulate/softmax, bf16 out",
+        "data": "synthetic (seeded generator; RMSNormed post-RoPE latents, N(0,1) indexer keys/queries)",
+        "config": {"workload": wl.name, "mode": wl.mode, "batch": B, "context": N, "query_tokens": n_q,
+                   "queries_per_step": Q, "l2": "inputs larger than L2 (the scanned indexer plane and the "
+                   "gathered KV exceed the 126 MB L2)" if wl.mode != "reuse" else "store larger than L2; "
+                   "gathers are random", "parallelism": f"replicas x{world} (independent sequences)",
+                   "setup_s": round(setup_s, 1)},
+        "hbm_fraction_step": (sb / (ms_max * 1e-3) / 1e9) / peak,
+        "stage_ms": stage_ms,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom_bytes, "peak_source": peak_kind},
+        "clocks": clk,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    return line
+
+
+def run_e2e(args, wl, S, out, lse, ws, pool, topk, dev):
+    """Same step through the public C-ABI with host inputs: every step copies
+    its new entries and queries from pinned host memory and reads the output
+    back."""
+    import sparse_attention_fp4_mxfp4_gb300 as csa2
+    c = S.cache
+    L = S.layers[0]
+    host = {
+        "latent": S.step_latent.cpu().pin_memory(), "key": S.step_idx_key.cpu().pin_memory(),
+        "swa": S.step_swa[0].cpu().pin_memory(), "q": L.q.cpu().pin_memory(),
+    }
+    if L.q_idx is not None:
+        host["q_idx"] = L.q_idx.cpu().pin_memory()
+        host["w"] = L.w.cpu().pin_memory()
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    mode = {"full": csa2.MODE_FULL, "reindex": csa2.MODE_REINDEX, "reuse": csa2.MODE_REUSE}[wl.mode]
+    a = csa2.layer_args(mode, B=wl.B, n_q=wl.n_q, max_ctx=wl.N, seq_len=S.seq_len, block_table=c.block_table,
+                        n_pages=c.n_pages, main_pages=c.main_pages, idx_pages=c.idx_pages, rings=c.rings,
+                        ring_idx=L.ring_idx, q=dev_in["q"], out=out, ws=ws, lse=lse,
+                        q_idx_codes=L.q_codes, q_idx_scales=L.q_scales, w=dev_in.get("w"),
+                        pool=pool if wl.mode == "full" else L.pool, topk=topk)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+
+    def step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        csa2.csa2_append_kv(dev_in["latent"], dev_in["key"], S.step_seq, S.step_pos, c.block_table,
+                            c.main_pages, c.idx_pages)
+        csa2.csa2_append_swa(dev_in["swa"], S.step_ring_idx[0], S.step_pos, c.rings)
+        if "q_idx" in dev_in:
+            csa2.csa2_quant_mxfp4(dev_in["q_idx"], L.q_codes, L.q_scales)
+        csa2.csa2_decode_layer(a)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 500))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": wl.B * wl.n_q / (ms * 1e-3), "unit": "queries/s", "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---- the CPU oracle (baseline and reference arm) ------------------------------------------------
+
+def oracle_query(wl, b=0, j=0, n_scan=None):
+    """One query of the workload through the CPU oracle. Returns (seconds,
+    scaled seconds for the whole query, description). n_scan limits the scan
+    sample (positions 0..n_scan-1); its time is scaled to the full context."""
+    import oracle
+    import synth
+    from tests.harness import n_blocks
+    seed, N, n_q = wl.seed, wl.N, wl.n_q
+    t = N - n_q + j
+    li = 0
+    q = synth.normal(seed, synth.Q + li, b, N - n_q + j, 1, 64 * 512).reshape(64, 512)
+    desc = ""
+    if wl.mode in ("full", "reindex"):
+        qi = synth.normal(seed, synth.IDXQ + li, b, t, 1, 32 * 128).reshape(32, 128)
+        w = synth.uniform(seed, synth.W + li, b, t, 1, 32)[0]
+    if wl.mode == "full":
+        n = t + 1 if n_scan is None else min(t + 1, n_scan)
+        keys = synth.normal(seed, synth.IDXKEY, b, 0, n, 128)
+        t0 = time.perf_counter()
+        r = oracle.full_indexer(qi, w, keys, n - 1, want_scores=False)
+        t_idx = time.perf_counter() - t0
+        scale = (t + 1) / n
+        sel = r["topk"]
+        desc = f"Full-mode query (sequence {b}): oracle scan of {n} of {t + 1} positions" + (
+            f", scan time scaled x{scale:.1f}" if scale > 1 else "")
+    elif wl.mode == "reindex":
+        keys = synth.normal(seed, synth.IDXKEY, b, 0, t + 1, 128)
+        pool = synth.sample_sorted(seed, synth.POOL + li, b, t, n_blocks(t), 2048)
+        t0 = time.perf_counter()
+        r = oracle.reindex(qi, w, keys, t, pool)
+        t_idx = time.perf_counter() - t0
+        scale = 1.0
+        sel = r["topk"]
+        desc = f"Reindex-mode query (sequence {b})"
+    else:
+        sel = synth.sample_sorted(seed, synth.TOPK, b, t, t + 1, 512)
+        t_idx, scale = 0.0, 1.0
+        desc = f"Reuse-mode query (sequence {b})"
+    sel = np.asarray(sel)
+    sel = sel[sel >= 0].astype(np.int64)
+    main = synth.latent_rows(seed, np.full(sel.size, b), sel)
+    win = oracle.window_positions(t, N, 128)
+    wrows = synth.latent_rows(seed, np.full(win.size, b), win, tensor=synth.SWA + li)
+    t0 = time.perf_counter()
+    oracle.sparse_attention(q, main, wrows, 1.0 / math.sqrt(512))
+    t_att = time.perf_counter() - t0
+    return t_idx + t_att, t_idx * scale + t_att, desc + ", then oracle sparse attention over 512 + window keys"
+
+
+def cpu_baseline(wl, budget_s=20.0):
+    import oracle
+    wall, scaled, desc = oracle_query(wl, n_scan=None if wl.mode != "full" or wl.N <= 262144 else 262144)
+    return {"value": 1.0 / scaled, "unit": "queries/s", "cores": oracle.THREADS, "kind": "oracle",
+            "sample": desc, "wall_s": round(wall, 2)}
+
+
+def run_reference(args, wl, rank, world):
+    """--impl reference: the CPU oracle as it stands on this host's cores."""
+    import oracle
+    if rank != 0:
+        return None
+    n_total = args.steps + args.warmup
+    # Bound the whole run to about two minutes: the scan sample per step shrinks with the step count.
+    n_scan = None
+    if wl.mode == "full":
+        probe_n = min(wl.N, 65536)
+        t0 = time.perf_counter()
+        oracle_query(wl, n_scan=probe_n)
+        per_pos = (time.perf_counter() - t0) / probe_n
+        n_scan = int(max(4096, min(wl.N, 100.0 / max(1, n_total) / max(per_pos, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_query(wl, n_scan=n_scan)
+    scaled = []
+    desc = ""
+    for _ in range(args.steps):
+        _, s, desc = oracle_query(wl, n_scan=n_scan)
+        scaled.append(s)
+    sec = sum(scaled) / len(scaled)
+    v = 1.0 / sec
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded generator)",
+        "config": {"workload": wl.name, "mode": wl.mode, "batch": wl.B, "context": wl.N, "query_tokens": wl.n_q},
+        "cpu_baseline": {"value": v, "unit": "queries/s", "cores": oracle.THREADS, "kind": "oracle",
+                         "sample": desc + " (one query per step)"},
+        "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from synth.workloads import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, wl, rank, world)
+    else:
+        line = run_ours(args, wl, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

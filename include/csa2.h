@@ -1,0 +1,261 @@
+/*
+ * csa2.h -- C ABI of libcsa2.so, the sm_103a (GB300) decode hot path of
+ * DeepSeek-V4.1-Flash's CSA2 sparse attention.
+ *
+ * Sources (public pages the method is taken from):
+ *   [RN] "DeepSeek V4.1: model architecture and system design, a close reading"
+ *        (blog.keqichen.top): section 1 (configuration: indexer 32 heads x 128,
+ *        top-k 512, query 64 heads x 512, 2048 blocks x 8 positions = 16384
+ *        candidates, window 128), section 2.2 (CSA2 modes Full / Reindex /
+ *        Reuse and the hierarchical sparse indexer), section 2.3 (FP4 main KV:
+ *        E2M1 with one E4M3 scale per 16 channels, no global scale, quantised
+ *        after RoPE; sliding-window KV kept in FP8).
+ *   [AB] "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression"
+ *        (abstract notes): section 3.3 (what each mode reuses), section 3.4
+ *        (block selection by the maximum score of a block's positions, pool
+ *        shared by later Reindex layers), section 3.6 (FP4 main KV, dequantised
+ *        before attention).
+ *   [SY] "DeepSeek-V4 model structure (7): structure decides the system": the
+ *        paged KV cache in 128-token blocks and the per-sequence sliding-window
+ *        state; attention over the top-k entries plus 128 window entries with
+ *        K = V single-head MQA on a 512-dim latent.
+ *
+ * Conventions
+ *   - Every function returns a csa2 status (int); CSA2_OK is 0. Functions
+ *     validate their host-side arguments first and never abort or exit.
+ *     csa2_last_error() gives a thread-local text for the last failure.
+ *   - All tensor pointers are DEVICE pointers unless a comment says host.
+ *     The caller allocates and frees every buffer; the library allocates no
+ *     memory and keeps no per-call state. Device pointers that the kernels
+ *     read or write with vector accesses must be 16-byte aligned
+ *     (CSA2_ERR_INVALID_ARG otherwise).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Every call is asynchronous on that stream. Index checks done on
+ *     the device (page ids, positions, ring slots) do not fail the call: the
+ *     offending access is skipped and a device status word is set, which
+ *     csa2_check_device_status() reads after the stream's work is done. Every
+ *     wait inside a kernel is bounded (about 2 s) and records
+ *     CSA2_ERR_DEVICE_TIMEOUT instead of hanging.
+ *   - bf16 tensors are passed as void* and hold IEEE bfloat16 bit patterns.
+ *
+ * Data layout in HBM (decoder CSA2 at m = 1: one entry per token)
+ *   - Main KV page (CSA2_PLANE_MAIN): 128 entries x 288 bytes. Entry e of a
+ *     page starts at e * 288: 256 bytes of E2M1 codes (channel 2i in the low
+ *     nibble of byte i, channel 2i+1 in the high nibble), then 32 E4M3 scale
+ *     bytes (scale j covers channels 16j..16j+15).
+ *   - Indexer-key page (CSA2_PLANE_INDEX): 16 groups of 8 entries, 576 bytes
+ *     per group (9216 bytes per page). Group g covers entries 8g..8g+7:
+ *     bytes [0, 512) hold codes ordered [chunk c = 0..3][row r = 0..7][16
+ *     bytes = channels 32c..32c+31 of entry 8g+r]; bytes [512, 576) hold the
+ *     8 scale bytes of each row, row-major.
+ *   - Block table: int32 [B, max_pages]; entry (b, i) is the physical page of
+ *     positions 128i..128i+127 of sequence b (-1 = unmapped). Main and
+ *     indexer planes share the table: physical page P is main_pages + P*36864
+ *     and idx_pages + P*9216. n_pages = number of physical pages of each pool.
+ *   - Sliding-window ring: [n_rings, 128, 512] E4M3 bytes, no scale; position
+ *     p of a sequence lives in slot p % 128 of its ring.
+ *   - Query token j of n_q of sequence b sits at position
+ *     t = seq_len[b] - n_q + j (seq_len counts the entries already appended,
+ *     including this step's tokens). Its sliding window is the positions
+ *     max(0, t - 127, seq_len[b] - 128) .. t still resident in the ring.
+ */
+#ifndef CSA2_H_
+#define CSA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status ---------------------------------------------------------------- */
+#define CSA2_OK 0
+#define CSA2_ERR_INVALID_ARG 1     /* null/misaligned pointer, bad size or count */
+#define CSA2_ERR_UNSUPPORTED 2     /* a shape the library does not implement */
+#define CSA2_ERR_WORKSPACE 3       /* workspace missing or too small */
+#define CSA2_ERR_CUDA 4            /* a CUDA runtime call or launch failed */
+#define CSA2_ERR_DEVICE_TIMEOUT 5  /* a bounded wait inside a kernel gave up */
+#define CSA2_ERR_DEVICE_BOUNDS 6   /* a device-side index check failed */
+
+/* ---- fixed geometry of the decoder CSA2 layer ([RN] 1, [AB] 3.1) ----------- */
+#define CSA2_LATENT_DIM 512    /* main KV latent channels (K = V) */
+#define CSA2_Q_HEADS 64        /* attention query heads */
+#define CSA2_IDX_HEADS 32      /* indexer heads */
+#define CSA2_IDX_DIM 128       /* indexer head dim */
+#define CSA2_TOPK 512          /* selected positions per query */
+#define CSA2_POOL_BLOCKS 2048  /* candidate blocks per query */
+#define CSA2_BLOCK 8           /* positions per candidate block */
+#define CSA2_WINDOW 128        /* sliding-window entries */
+#define CSA2_PAGE_TOKENS 128   /* entries per page */
+#define CSA2_MAIN_ENTRY_BYTES 288
+#define CSA2_IDX_ENTRY_BYTES 72
+#define CSA2_MAX_NQ 8          /* query tokens per sequence in one call */
+
+#define CSA2_PLANE_MAIN 0
+#define CSA2_PLANE_INDEX 1
+
+#define CSA2_OUT_F32 0
+#define CSA2_OUT_BF16 1
+
+#define CSA2_MODE_FULL 0
+#define CSA2_MODE_REINDEX 1
+#define CSA2_MODE_REUSE 2
+
+#define CSA2_OP_INDEXER_FULL 1
+#define CSA2_OP_INDEXER_REINDEX 2
+#define CSA2_OP_SPARSE_ATTN 3
+#define CSA2_OP_DECODE_LAYER 4
+
+const char* csa2_status_string(int status);
+/* Thread-local detail text of the last failing call on this thread. */
+const char* csa2_last_error(void);
+int csa2_version(void);
+
+/* ---- size queries (host only, no GPU needed) ------------------------------- */
+/* Bytes of one page of a plane: 36864 (main) or 9216 (indexer). */
+int csa2_page_bytes(int plane, size_t* bytes);
+/* Bytes of one sliding-window ring: 128 * 512 = 65536. */
+int csa2_ring_bytes(size_t* bytes);
+/* Workspace bytes that an op needs for B sequences, n_q tokens each and a
+ * context of at most max_ctx entries. */
+int csa2_workspace_bytes(int op, int B, int n_q, int64_t max_ctx, size_t* bytes);
+
+/* ---- append: MXFP4 main KV + indexer keys, FP8 window ([RN] 2.3, [AB] 3.6) -- */
+/* Quantises T new entries and stores each into slot pos % 128 of page
+ * block_table[seq_idx[i], pos / 128] of both planes.
+ *   latent:  bf16 [T, 512], post-RoPE main-KV entries
+ *   idx_key: bf16 [T, 128], indexer keys
+ *   seq_idx: int32 [T] in [0, B); pos: int64 [T]; block_table: int32 [B, max_pages]
+ * Per 16-channel block: scale = E4M3(amax / 6) (fp32 IEEE division, round to
+ * nearest even, saturating at 448); code = nearest E2M1 value of |v| / scale,
+ * ties to the even code. Entries with an unmapped or out-of-range page are
+ * skipped and set CSA2_ERR_DEVICE_BOUNDS. */
+int csa2_append_kv(const void* latent, const void* idx_key, const int32_t* seq_idx,
+                   const int64_t* pos, int T, const int32_t* block_table, int B, int max_pages,
+                   int64_t n_pages, uint8_t* main_pages, uint8_t* idx_pages, void* stream);
+
+/* E4M3 (round to nearest even, saturating, no scale) of T new window entries
+ * x: bf16 [T, 512] into slot pos % 128 of ring ring_idx[i] of rings
+ * [n_rings, 128, 512]. */
+int csa2_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, int T,
+                    int64_t n_rings, uint8_t* rings, void* stream);
+
+/* ---- codec utilities -------------------------------------------------------- */
+/* MXFP4 quantisation of n bf16 values (n % 16 == 0): codes [n/2], scales
+ * [n/16]. Used for the indexer query (32 heads x 128 per token) and tests. */
+int csa2_quant_mxfp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales, void* stream);
+/* Dequantisation to fp32 (exact). */
+int csa2_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t n, float* out,
+                       void* stream);
+/* fp32 -> E4M3 (round to nearest even, saturating to +-448). */
+int csa2_quant_fp8(const float* x, int64_t n, uint8_t* out, void* stream);
+
+/* ---- hierarchical sparse indexer ([RN] 2.2, [AB] 3.4) ----------------------- */
+/* Full-mode scan: for every causal position p <= t of every query token,
+ * s(p) = sum_h w_h * max(0, qhat_h . khat_p) (fp32 accumulation of exact FP4
+ * products on the tensor cores), then the maximum over each block of 8 causal
+ * positions.
+ *   q_codes: [B, n_q, 32, 64] bytes, q_scales: [B, n_q, 32, 8] (MXFP4 of the
+ *   indexer query, as written by csa2_quant_mxfp4 on a [B, n_q, 32, 128]
+ *   tensor); w: fp32 [B, n_q, 32]; seq_len: int64 [B].
+ *   block_max: fp32 [B, n_q, max_blocks], max_blocks >= ceil(max_ctx / 8);
+ *   entries at or past ceil((t + 1) / 8) are left untouched.
+ * max_ctx is a host-side upper bound of seq_len (sizes the grid). */
+int csa2_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                      const int64_t* seq_len, int B, int n_q, int64_t max_ctx,
+                      const int32_t* block_table, int max_pages, int64_t n_pages,
+                      const uint8_t* idx_pages, float* block_max, int64_t max_blocks,
+                      void* stream);
+
+/* Top 2048 blocks of each query token by block maximum (higher first, then
+ * lower block id); all causal blocks when there are at most 2048.
+ *   pool: int32 [B, n_q, 2048], block ids ascending, -1 padded. */
+int csa2_block_topk(const float* block_max, const int64_t* seq_len, int B, int n_q,
+                    int64_t max_blocks, int32_t* pool, void* stream);
+
+/* Reindex: scores only the positions 8b..8b+7 (<= t) of each pool block b
+ * with this layer's indexer query and takes the top 512 (higher score first,
+ * then lower position).
+ *   pool: int32 [B, n_q, 2048] (-1 entries ignored); topk: int32 [B, n_q,
+ *   512], positions ascending, -1 padded.
+ *   ws: workspace of csa2_workspace_bytes(CSA2_OP_INDEXER_REINDEX, ...). */
+int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                         const int64_t* seq_len, int B, int n_q, const int32_t* block_table,
+                         int max_pages, int64_t n_pages, const uint8_t* idx_pages,
+                         const int32_t* pool, int32_t* topk, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Full-mode indexer = scan + block top-2048 + rescore of the pool + top-512.
+ * The final top-512 over the pool equals the top-512 over all causal
+ * positions up to ties. ws: csa2_workspace_bytes(CSA2_OP_INDEXER_FULL, ...). */
+int csa2_indexer_full(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                      const int64_t* seq_len, int B, int n_q, int64_t max_ctx,
+                      const int32_t* block_table, int max_pages, int64_t n_pages,
+                      const uint8_t* idx_pages, int32_t* pool, int32_t* topk, void* ws,
+                      size_t ws_bytes, void* stream);
+
+/* ---- sparse attention (Reuse mode; [RN] 2.2, [AB] 3.3 / 3.6, [SY]) ---------- */
+/* o_h = softmax(scale * q_h K^T) V with K = V = the dequantised keys: the main
+ * entries at the query's top-k positions (-1 skipped) followed by its FP8
+ * window entries, duplicates kept. 64 heads x 512 dims, fp32 softmax.
+ *   q: bf16 [B, n_q, 64, 512]; topk: int32 [B, n_q, 512]; ring_idx: int32 [B]
+ *   out: [B, n_q, 64, 512] fp32 (out_dtype CSA2_OUT_F32) or bf16
+ *   (CSA2_OUT_BF16); lse: fp32 [B, n_q, 64] natural-log sum of exp of the
+ *   scaled logits (may be NULL).
+ *   ws: csa2_workspace_bytes(CSA2_OP_SPARSE_ATTN, ...). */
+int csa2_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len, int B, int n_q,
+                     const int32_t* block_table, int max_pages, int64_t n_pages,
+                     const uint8_t* main_pages, const uint8_t* rings, const int32_t* ring_idx,
+                     int64_t n_rings, float softmax_scale, int out_dtype, void* out, float* lse,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* ---- mode dispatcher ([RN] 2.2, [AB] 3.3) ----------------------------------- */
+typedef struct csa2_layer_args {
+  int mode;                 /* CSA2_MODE_FULL / _REINDEX / _REUSE */
+  int B, n_q;
+  int64_t max_ctx;          /* host-side upper bound of seq_len */
+  const int64_t* seq_len;   /* [B] */
+  const int32_t* block_table;
+  int max_pages;
+  int64_t n_pages;
+  const uint8_t* main_pages;
+  const uint8_t* idx_pages;
+  const uint8_t* rings;     /* this layer's rings [n_rings, 128, 512] */
+  const int32_t* ring_idx;  /* [B] */
+  int64_t n_rings;
+  const uint8_t* q_idx_codes;  /* FULL / REINDEX: this layer's indexer query */
+  const uint8_t* q_idx_scales;
+  const float* w;
+  const void* q;            /* bf16 [B, n_q, 64, 512], this layer's query */
+  int32_t* pool;            /* FULL: written. REINDEX: read; NULL = the group's latest pool */
+  int32_t* topk;            /* FULL / REINDEX: written. REUSE: read; NULL = latest top-k */
+  float softmax_scale;
+  int out_dtype;
+  void* out;
+  float* lse;               /* may be NULL */
+  void* ws;
+  size_t ws_bytes;          /* csa2_workspace_bytes(CSA2_OP_DECODE_LAYER, ...) */
+} csa2_layer_args;
+
+/* One layer: FULL = indexer_full then sparse_attn; REINDEX = indexer_reindex
+ * (on the given or latest pool) then sparse_attn; REUSE = sparse_attn on the
+ * given or latest top-k. */
+int csa2_decode_layer(const csa2_layer_args* layer, void* stream);
+
+/* Layers in order on one stream. A REINDEX layer with pool == NULL uses the
+ * latest FULL layer's pool of the group; a REUSE layer with topk == NULL uses
+ * the latest top-k written by an earlier layer of the group. Layers may share
+ * one workspace: they run one after another on the stream. */
+int csa2_decode_group(const csa2_layer_args* layers, int n_layers, void* stream);
+
+/* ---- device status ---------------------------------------------------------- */
+/* Waits for the stream, then reads (and clears) the device status words:
+ * *status = CSA2_OK, CSA2_ERR_DEVICE_TIMEOUT or CSA2_ERR_DEVICE_BOUNDS. */
+int csa2_check_device_status(void* stream, int* status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H_ */

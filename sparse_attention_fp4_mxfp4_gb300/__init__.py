@@ -1,0 +1,289 @@
+"""Python binding of libcsa2.so, the GB300 (sm_103a) CSA2 decode hot path.
+
+Argument marshalling only: every step runs in the CUDA library. Functions
+carry the C ABI's names (include/csa2.h documents arguments, layouts and
+errors) and take torch tensors; device pointers, sizes and the current CUDA
+stream are passed through. A failing call raises Csa2Error with the library's
+message. There is no CPU fallback: importing this package fails loudly when
+the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcsa2.so")
+
+# Constants of include/csa2.h.
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE_BOUNDS = range(7)
+LATENT_DIM, Q_HEADS, IDX_HEADS, IDX_DIM = 512, 64, 32, 128
+TOPK, POOL_BLOCKS, BLOCK, WINDOW, PAGE_TOKENS = 512, 2048, 8, 128, 128
+MAIN_ENTRY_BYTES, IDX_ENTRY_BYTES, MAX_NQ = 288, 72, 8
+PLANE_MAIN, PLANE_INDEX = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
+MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
+OP_INDEXER_FULL, OP_INDEXER_REINDEX, OP_SPARSE_ATTN, OP_DECODE_LAYER = 1, 2, 3, 4
+
+# Exported entry points of include/csa2.h.
+EXPORTS = (
+    "csa2_status_string", "csa2_last_error", "csa2_version", "csa2_page_bytes", "csa2_ring_bytes",
+    "csa2_workspace_bytes", "csa2_append_kv", "csa2_append_swa", "csa2_quant_mxfp4",
+    "csa2_dequant_mxfp4", "csa2_quant_fp8", "csa2_indexer_scan", "csa2_block_topk",
+    "csa2_indexer_reindex", "csa2_indexer_full", "csa2_sparse_attn", "csa2_decode_layer",
+    "csa2_decode_group", "csa2_check_device_status",
+)
+
+
+class Csa2Error(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"csa2 status {status}: {msg}")
+        self.status = status
+
+
+class LayerArgs(ctypes.Structure):
+    """csa2_layer_args of include/csa2.h."""
+    _fields_ = [
+        ("mode", ctypes.c_int), ("B", ctypes.c_int), ("n_q", ctypes.c_int),
+        ("max_ctx", ctypes.c_int64), ("seq_len", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+        ("max_pages", ctypes.c_int), ("n_pages", ctypes.c_int64), ("main_pages", ctypes.c_void_p),
+        ("idx_pages", ctypes.c_void_p), ("rings", ctypes.c_void_p), ("ring_idx", ctypes.c_void_p),
+        ("n_rings", ctypes.c_int64), ("q_idx_codes", ctypes.c_void_p), ("q_idx_scales", ctypes.c_void_p),
+        ("w", ctypes.c_void_p), ("q", ctypes.c_void_p), ("pool", ctypes.c_void_p), ("topk", ctypes.c_void_p),
+        ("softmax_scale", ctypes.c_float), ("out_dtype", ctypes.c_int), ("out", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p), ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(LIB_PATH)
+    p, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    psz = ctypes.POINTER(ctypes.c_size_t)
+    sig = {
+        "csa2_status_string": ([i32], ctypes.c_char_p),
+        "csa2_last_error": ([], ctypes.c_char_p),
+        "csa2_version": ([], i32),
+        "csa2_page_bytes": ([i32, psz], i32),
+        "csa2_ring_bytes": ([psz], i32),
+        "csa2_workspace_bytes": ([i32, i32, i32, i64, psz], i32),
+        "csa2_append_kv": ([p, p, p, p, i32, p, i32, i32, i64, p, p, p], i32),
+        "csa2_append_swa": ([p, p, p, i32, i64, p, p], i32),
+        "csa2_quant_mxfp4": ([p, i64, p, p, p], i32),
+        "csa2_dequant_mxfp4": ([p, p, i64, p, p], i32),
+        "csa2_quant_fp8": ([p, i64, p, p], i32),
+        "csa2_indexer_scan": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, i64, p], i32),
+        "csa2_block_topk": ([p, p, i32, i32, i64, p, p], i32),
+        "csa2_indexer_reindex": ([p, p, p, p, i32, i32, p, i32, i64, p, p, p, p, sz, p], i32),
+        "csa2_indexer_full": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, p, p, sz, p], i32),
+        "csa2_sparse_attn": ([p, p, p, i32, i32, p, i32, i64, p, p, p, i64, f32, i32, p, p, p, sz, p], i32),
+        "csa2_decode_layer": ([ctypes.POINTER(LayerArgs), p], i32),
+        "csa2_decode_group": ([ctypes.POINTER(LayerArgs), i32, p], i32),
+        "csa2_check_device_status": ([p, ctypes.POINTER(ctypes.c_int)], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes, fn.restype = args, res
+    return L
+
+
+lib = _load()
+
+
+def _check(status: int):
+    if status != OK:
+        raise Csa2Error(status, lib.csa2_last_error().decode())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim=None):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: {t.dim()} dims, expected {ndim}")
+
+
+# ---- size queries -------------------------------------------------------------
+
+def csa2_page_bytes(plane: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib.csa2_page_bytes(plane, ctypes.byref(n)))
+    return n.value
+
+
+def csa2_ring_bytes() -> int:
+    n = ctypes.c_size_t()
+    _check(lib.csa2_ring_bytes(ctypes.byref(n)))
+    return n.value
+
+
+def csa2_workspace_bytes(op: int, B: int, n_q: int, max_ctx: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib.csa2_workspace_bytes(op, B, n_q, max_ctx, ctypes.byref(n)))
+    return n.value
+
+
+# ---- append -------------------------------------------------------------------
+
+def csa2_append_kv(latent, idx_key, seq_idx, pos, block_table, main_pages, idx_pages, stream=None):
+    """latent bf16 [T,512], idx_key bf16 [T,128], seq_idx int32 [T], pos int64 [T],
+    block_table int32 [B,max_pages], main_pages uint8 [P,36864], idx_pages uint8 [P,9216]."""
+    _need(latent, "latent", torch.bfloat16, 2)
+    _need(idx_key, "idx_key", torch.bfloat16, 2)
+    _need(seq_idx, "seq_idx", torch.int32, 1)
+    _need(pos, "pos", torch.int64, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    T = latent.shape[0]
+    if latent.shape[1] != LATENT_DIM or idx_key.shape != (T, IDX_DIM) or seq_idx.numel() != T or pos.numel() != T:
+        raise ValueError("append_kv: inconsistent shapes")
+    _check(lib.csa2_append_kv(_ptr(latent), _ptr(idx_key), _ptr(seq_idx), _ptr(pos), T, _ptr(block_table),
+                              block_table.shape[0], block_table.shape[1], main_pages.shape[0],
+                              _ptr(main_pages), _ptr(idx_pages), _stream(stream)))
+
+
+def csa2_append_swa(x, ring_idx, pos, rings, stream=None):
+    """x bf16 [T,512], ring_idx int32 [T], pos int64 [T], rings uint8 [R,128,512]."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(ring_idx, "ring_idx", torch.int32, 1)
+    _need(pos, "pos", torch.int64, 1)
+    T = x.shape[0]
+    _check(lib.csa2_append_swa(_ptr(x), _ptr(ring_idx), _ptr(pos), T, rings.shape[0], _ptr(rings),
+                               _stream(stream)))
+
+
+# ---- codecs -------------------------------------------------------------------
+
+def csa2_quant_mxfp4(x, codes=None, scales=None, stream=None):
+    """bf16 [..., n] (n % 16 == 0) -> (codes uint8 [..., n/2], scales uint8 [..., n/16])."""
+    _need(x, "x", torch.bfloat16)
+    n = x.numel()
+    if codes is None:
+        codes = torch.empty(*x.shape[:-1], x.shape[-1] // 2, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(*x.shape[:-1], x.shape[-1] // 16, dtype=torch.uint8, device=x.device)
+    _check(lib.csa2_quant_mxfp4(_ptr(x), n, _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes, scales
+
+
+def csa2_dequant_mxfp4(codes, scales, out=None, stream=None):
+    n = codes.numel() * 2
+    if out is None:
+        out = torch.empty(*codes.shape[:-1], codes.shape[-1] * 2, dtype=torch.float32, device=codes.device)
+    _check(lib.csa2_dequant_mxfp4(_ptr(codes), _ptr(scales), n, _ptr(out), _stream(stream)))
+    return out
+
+
+def csa2_quant_fp8(x, out=None, stream=None):
+    _need(x, "x", torch.float32)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib.csa2_quant_fp8(_ptr(x), x.numel(), _ptr(out), _stream(stream)))
+    return out
+
+
+# ---- indexer ------------------------------------------------------------------
+
+def csa2_indexer_scan(q_codes, q_scales, w, seq_len, max_ctx, block_table, n_pages, idx_pages,
+                      block_max, stream=None):
+    """q_codes uint8 [B,n_q,32,64], q_scales uint8 [B,n_q,32,8], w fp32 [B,n_q,32],
+    seq_len int64 [B] -> block_max fp32 [B,n_q,max_blocks]."""
+    B, n_q = w.shape[0], w.shape[1]
+    _check(lib.csa2_indexer_scan(_ptr(q_codes), _ptr(q_scales), _ptr(w), _ptr(seq_len), B, n_q, max_ctx,
+                                 _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx_pages),
+                                 _ptr(block_max), block_max.shape[-1], _stream(stream)))
+
+
+def csa2_block_topk(block_max, seq_len, pool, stream=None):
+    B, n_q = block_max.shape[0], block_max.shape[1]
+    _check(lib.csa2_block_topk(_ptr(block_max), _ptr(seq_len), B, n_q, block_max.shape[-1], _ptr(pool),
+                               _stream(stream)))
+
+
+def csa2_indexer_reindex(q_codes, q_scales, w, seq_len, block_table, n_pages, idx_pages, pool, topk, ws,
+                         stream=None):
+    B, n_q = w.shape[0], w.shape[1]
+    _check(lib.csa2_indexer_reindex(_ptr(q_codes), _ptr(q_scales), _ptr(w), _ptr(seq_len), B, n_q,
+                                    _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx_pages),
+                                    _ptr(pool), _ptr(topk), _ptr(ws), ws.numel() * ws.element_size(),
+                                    _stream(stream)))
+
+
+def csa2_indexer_full(q_codes, q_scales, w, seq_len, max_ctx, block_table, n_pages, idx_pages, pool, topk,
+                      ws, stream=None):
+    B, n_q = w.shape[0], w.shape[1]
+    _check(lib.csa2_indexer_full(_ptr(q_codes), _ptr(q_scales), _ptr(w), _ptr(seq_len), B, n_q, max_ctx,
+                                 _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx_pages),
+                                 _ptr(pool), _ptr(topk), _ptr(ws), ws.numel() * ws.element_size(),
+                                 _stream(stream)))
+
+
+# ---- attention ----------------------------------------------------------------
+
+def csa2_sparse_attn(q, topk, seq_len, block_table, n_pages, main_pages, rings, ring_idx, out, lse, ws,
+                     softmax_scale=1.0 / math.sqrt(LATENT_DIM), stream=None):
+    """q bf16 [B,n_q,64,512], topk int32 [B,n_q,512] -> out [B,n_q,64,512] (fp32 or bf16), lse fp32 [B,n_q,64]."""
+    _need(q, "q", torch.bfloat16, 4)
+    B, n_q = q.shape[0], q.shape[1]
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(lib.csa2_sparse_attn(_ptr(q), _ptr(topk), _ptr(seq_len), B, n_q, _ptr(block_table),
+                                block_table.shape[1], n_pages, _ptr(main_pages), _ptr(rings), _ptr(ring_idx),
+                                rings.shape[0], softmax_scale, out_dtype, _ptr(out), _ptr(lse), _ptr(ws),
+                                ws.numel() * ws.element_size(), _stream(stream)))
+
+
+# ---- dispatcher ---------------------------------------------------------------
+
+def layer_args(mode, *, B, n_q, max_ctx, seq_len, block_table, n_pages, main_pages, idx_pages, rings,
+               ring_idx, q, out, ws, q_idx_codes=None, q_idx_scales=None, w=None, pool=None, topk=None,
+               lse=None, softmax_scale=1.0 / math.sqrt(LATENT_DIM)) -> LayerArgs:
+    a = LayerArgs()
+    a.mode, a.B, a.n_q, a.max_ctx = mode, B, n_q, max_ctx
+    a.seq_len, a.block_table, a.max_pages, a.n_pages = _ptr(seq_len), _ptr(block_table), block_table.shape[1], n_pages
+    a.main_pages, a.idx_pages = _ptr(main_pages), _ptr(idx_pages)
+    a.rings, a.ring_idx, a.n_rings = _ptr(rings), _ptr(ring_idx), rings.shape[0]
+    a.q_idx_codes, a.q_idx_scales, a.w, a.q = _ptr(q_idx_codes), _ptr(q_idx_scales), _ptr(w), _ptr(q)
+    a.pool, a.topk = _ptr(pool), _ptr(topk)
+    a.softmax_scale = softmax_scale
+    a.out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    a.out, a.lse = _ptr(out), _ptr(lse)
+    a.ws, a.ws_bytes = _ptr(ws), ws.numel() * ws.element_size()
+    return a
+
+
+def csa2_decode_layer(args: LayerArgs, stream=None):
+    _check(lib.csa2_decode_layer(ctypes.byref(args), _stream(stream)))
+
+
+def csa2_decode_group(layers, stream=None):
+    arr = (LayerArgs * len(layers))(*layers)
+    _check(lib.csa2_decode_group(arr, len(layers), _stream(stream)))
+
+
+def csa2_check_device_status(stream=None) -> int:
+    """Waits for the stream and returns (and clears) the device status code."""
+    st = ctypes.c_int(0)
+    _check(lib.csa2_check_device_status(_stream(stream), ctypes.byref(st)))
+    return st.value
+
+
+def device_status_message() -> str:
+    return lib.csa2_last_error().decode()

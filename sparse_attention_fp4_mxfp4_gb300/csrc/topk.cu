@@ -1,0 +1,208 @@
+// Top-k selections of the hierarchical sparse indexer ("DeepSeek V4.1: model
+// architecture and system design, a close reading" section 2.2;
+// "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" section
+// 3.4): the 2048 best 8-position blocks by block maximum form the candidate
+// pool; the 512 best pool positions form the top-k.
+//
+// One CTA of 1024 threads per query token. Exact radix select on the
+// order-preserving integer image of the fp32 scores (digits of 11, 11 and 10
+// bits), then an ordered compaction: everything above the threshold, plus the
+// lowest-index elements equal to it until k are taken. The output is in
+// ascending index order and padded with -1. Invalid elements (masked slots,
+// -inf, NaN) are never selected.
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kThreads = 1024;
+
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  if (!(f > -INFINITY)) return 0u;  // -inf and NaN: invalid
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Block-wide exclusive prefix sum over 1024 threads; returns the total in *total.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;  // inclusive
+  }
+  __syncthreads();
+  const uint32_t base = warp > 0 ? warp_sums[warp - 1] : 0u;
+  const uint32_t tot = warp_sums[31];
+  __syncthreads();
+  *total = tot;
+  return base + x - v;
+}
+
+// Row of n keys, pick k. `map` turns an element index into the output value.
+// mode 0: block top-k (value = block id); mode 1: pool top-k (value = position
+// pool[i / 8] * 8 + i % 8).
+template <int kMode>
+__global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __restrict__ keys,
+                                                              int64_t row_stride,
+                                                              const int64_t* __restrict__ seq_len,
+                                                              int n_q, int k,
+                                                              const int32_t* __restrict__ pool,
+                                                              int32_t* __restrict__ out) {
+  __shared__ uint32_t hist[2048];
+  __shared__ uint32_t warp_sums[32];
+  __shared__ uint32_t s_sel[2];
+
+  const int q = blockIdx.x;
+  const int b = q / n_q, j = q % n_q;
+  const int tid = threadIdx.x;
+  const float* row = keys + static_cast<int64_t>(q) * row_stride;
+  int32_t* orow = out + static_cast<int64_t>(q) * k;
+  int64_t n;
+  if (kMode == 0) {
+    const int64_t t = seq_len[b] - n_q + j;
+    n = t >= 0 ? (t + 8) / 8 : 0;
+    if (n > row_stride) {
+      if (tid == 0) report(CSA2_ERR_DEVICE_BOUNDS, 301);
+      n = row_stride;
+    }
+  } else {
+    n = row_stride;
+  }
+  const int32_t* prow = pool + static_cast<int64_t>(q) * 2048;
+
+  // Radix passes. prefix/mask describe the bits fixed so far; `remaining`
+  // counts how many elements still have to be taken among those matching.
+  uint32_t prefix = 0, mask = 0, remaining = static_cast<uint32_t>(k);
+  uint32_t valid = 0;
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+  bool all_valid = false;
+  for (int pass = 0; pass < 3; ++pass) {
+    const int sh = shifts[pass];
+    const uint32_t nb = 1u << widths[pass];
+    for (uint32_t i = tid; i < 2048; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    for (int64_t i = tid; i < n; i += kThreads) {
+      const uint32_t u = ordered_key(row[i]);
+      if (u != 0u && (u & mask) == prefix) atomicAdd(&hist[(u >> sh) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    // Counts from the top: thread t owns bins [2t, 2t+1] in descending order.
+    const uint32_t hi_bin = nb - 1 - 2 * tid, lo_bin = hi_bin - 1;
+    uint32_t c_hi = 0, c_lo = 0;
+    if (2 * static_cast<uint32_t>(tid) < nb) {
+      c_hi = hist[hi_bin];
+      c_lo = hist[lo_bin];
+    }
+    uint32_t total;
+    const uint32_t before = block_excl_scan(c_hi + c_lo, warp_sums, &total);
+    if (pass == 0) {
+      valid = total;
+      if (valid <= static_cast<uint32_t>(k)) {
+        all_valid = true;
+        break;
+      }
+    }
+    if (2 * static_cast<uint32_t>(tid) < nb) {
+      if (before < remaining && before + c_hi >= remaining) {
+        s_sel[0] = hi_bin;
+        s_sel[1] = before;
+      } else if (before + c_hi < remaining && before + c_hi + c_lo >= remaining) {
+        s_sel[0] = lo_bin;
+        s_sel[1] = before + c_hi;
+      }
+    }
+    __syncthreads();
+    const uint32_t bin = s_sel[0];
+    remaining -= s_sel[1];
+    prefix |= bin << sh;
+    mask |= (nb - 1) << sh;
+    __syncthreads();
+  }
+
+  // Threshold T: take u > T, and the first `need_eq` elements with u == T.
+  const uint32_t T = all_valid ? 0u : prefix;
+  const uint32_t need_eq = all_valid ? 0u : remaining;
+  const int64_t seg = (n + kThreads - 1) / kThreads;
+  const int64_t lo = static_cast<int64_t>(tid) * seg, hi = lo + seg < n ? lo + seg : n;
+  uint32_t gt = 0, eq = 0;
+  for (int64_t i = lo; i < hi; ++i) {
+    const uint32_t u = ordered_key(row[i]);
+    if (u > T) ++gt;
+    else if (u == T && u != 0u) ++eq;
+  }
+  uint32_t tot_eq;
+  const uint32_t eq_base = block_excl_scan(eq, warp_sums, &tot_eq);
+  const uint32_t take_eq = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
+  uint32_t tot_sel;
+  uint32_t o = block_excl_scan(gt + take_eq, warp_sums, &tot_sel);
+  uint32_t taken_eq = 0;
+  for (int64_t i = lo; i < hi; ++i) {
+    const uint32_t u = ordered_key(row[i]);
+    bool sel = u > T;
+    if (!sel && u == T && u != 0u && taken_eq < take_eq) {
+      sel = true;
+      ++taken_eq;
+    }
+    if (sel) {
+      int32_t v;
+      if (kMode == 0) {
+        v = static_cast<int32_t>(i);
+      } else {
+        v = prow[i >> 3] * 8 + static_cast<int32_t>(i & 7);
+      }
+      if (o < static_cast<uint32_t>(k)) orow[o] = v;  // never past the row, whatever the counts say
+      ++o;
+    }
+  }
+  for (int i = static_cast<int>(tot_sel) + tid; i < k; i += kThreads) orow[i] = -1;
+}
+
+}  // namespace
+
+cudaError_t status_topk(cudaStream_t stream, int* code, int* where, bool clear) {
+  int h[2] = {0, 0};
+  cudaError_t e = cudaMemcpyFromSymbolAsync(h, g_status, sizeof(h), 0, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess && clear) {
+    const int z[2] = {0, 0};
+    e = cudaMemcpyToSymbolAsync(g_status, z, sizeof(z), 0, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  }
+  *code = h[0];
+  *where = h[1];
+  return e;
+}
+
+cudaError_t launch_block_topk(const float* block_max, const int64_t* seq_len, int B, int n_q,
+                              int64_t max_blocks, int32_t* pool, cudaStream_t stream) {
+  const int Q = B * n_q;
+  if (Q == 0) return cudaSuccess;
+  radix_topk_kernel<0><<<Q, kThreads, 0, stream>>>(block_max, max_blocks, seq_len, n_q, 2048,
+                                                   nullptr, pool);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pool_topk(const float* scores, const int64_t* seq_len, int B, int n_q,
+                             const int32_t* pool, int32_t* topk, cudaStream_t stream) {
+  const int Q = B * n_q;
+  if (Q == 0) return cudaSuccess;
+  radix_topk_kernel<1><<<Q, kThreads, 0, stream>>>(scores, 16384, seq_len, n_q, 512, pool, topk);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,267 @@
+"""Workload construction and oracle references shared by the GPU tests and the
+benchmark.
+
+Inputs come from the seeded generator (synth), are copied to the device and
+written into the paged store through the library's own append call; the CPU
+oracle receives the very same generator arrays. Nothing here computes any of
+the method's arithmetic itself: it wires inputs to the library and to the
+oracle, and compares their outputs.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import synth
+from synth.workloads import WORKLOADS, Workload
+
+TAU = 1.0 / math.sqrt(512)
+TOL_ATTN_F32 = 2e-3    # max over channels |o - r| / max |r|, per (query, head)
+TOL_ATTN_BF16 = 4e-3   # bf16 output rounding alone contributes up to 2^-9
+TOPK_TIE_RTOL = 1e-5   # selections may differ only among scores this close to the k-th
+
+
+def u16_to_bf16(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def bf16_to_u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@dataclass
+class Layer:
+    kind: str
+    q: torch.Tensor            # bf16 [B, n_q, 64, 512]
+    q_u16: np.ndarray
+    q_idx: torch.Tensor | None = None   # bf16 [B, n_q, 32, 128]
+    q_idx_u16: np.ndarray | None = None
+    w: torch.Tensor | None = None       # fp32 [B, n_q, 32]
+    w_np: np.ndarray | None = None
+    q_codes: torch.Tensor | None = None
+    q_scales: torch.Tensor | None = None
+    pool: torch.Tensor | None = None    # int32 [B, n_q, 2048]
+    ring_idx: torch.Tensor | None = None
+
+
+@dataclass
+class Setup:
+    wl: Workload
+    N: int
+    cache: object
+    seq_len: torch.Tensor
+    layers: list = field(default_factory=list)
+    topk: torch.Tensor | None = None       # int32 [B, n_q, 512]
+    step_latent: torch.Tensor | None = None
+    step_idx_key: torch.Tensor | None = None
+    step_seq: torch.Tensor | None = None
+    step_pos: torch.Tensor | None = None
+    step_swa: list = field(default_factory=list)     # per layer bf16 [B*n_q, 512]
+    step_ring_idx: list = field(default_factory=list)
+
+    @property
+    def B(self):
+        return self.wl.B
+
+    @property
+    def n_q(self):
+        return self.wl.n_q
+
+    def t(self, j: int) -> int:
+        return self.N - self.n_q + j
+
+
+def n_blocks(t: int) -> int:
+    return (t + 8) // 8
+
+
+def build(wl: Workload, device="cuda", *, N=None, B=None, n_q=None, shuffle_seed=None, prefill_step=False,
+          chunk=65536):
+    """Materialise a workload on the device.
+
+    Positions 0 .. N-n_q-1 of every sequence are appended at set-up; the step's
+    n_q tokens (positions N-n_q .. N-1) are prepared in step_* tensors and are
+    appended by append_step() (or here too when prefill_step is set).
+    """
+    import sparse_attention_fp4_mxfp4_gb300 as csa2
+    from sparse_attention_fp4_mxfp4_gb300.cache import PagedCache
+
+    if N is not None or B is not None or n_q is not None:
+        wl = Workload(wl.index, wl.name, wl.mode, B=B or wl.B, N=N or wl.N, n_q=n_q or wl.n_q, layers=wl.layers)
+    N, Bq, nq, seed = wl.N, wl.B, wl.n_q, wl.seed
+    n_layers = len(wl.layers)
+    cache = PagedCache(Bq, N, n_rings=Bq * n_layers, device=device, shuffle_seed=shuffle_seed)
+    S = Setup(wl=wl, N=N, cache=cache, seq_len=torch.full((Bq,), N, dtype=torch.int64, device=device))
+    pre = N - nq
+    for b in range(Bq):
+        for p0 in range(0, pre, chunk):
+            n = min(chunk, pre - p0)
+            lat = u16_to_bf16(synth.latent(seed, b, p0, n), device)
+            key = u16_to_bf16(synth.normal(seed, synth.IDXKEY, b, p0, n, 128), device)
+            seq = torch.full((n,), b, dtype=torch.int32, device=device)
+            pos = torch.arange(p0, p0 + n, dtype=torch.int64, device=device)
+            csa2.csa2_append_kv(lat, key, seq, pos, cache.block_table, cache.main_pages, cache.idx_pages)
+    # Window entries of the positions already in the cache, one ring per (layer, sequence).
+    lo = max(0, N - 128)
+    for li in range(n_layers):
+        for b in range(Bq):
+            if pre > lo:
+                x = u16_to_bf16(synth.latent(seed, b, lo, pre - lo, tensor=synth.SWA + li), device)
+                ridx = torch.full((pre - lo,), li * Bq + b, dtype=torch.int32, device=device)
+                pos = torch.arange(lo, pre, dtype=torch.int64, device=device)
+                csa2.csa2_append_swa(x, ridx, pos, cache.rings)
+    # The step's new tokens.
+    lat = np.concatenate([synth.latent(seed, b, pre, nq) for b in range(Bq)])
+    key = np.concatenate([synth.normal(seed, synth.IDXKEY, b, pre, nq, 128) for b in range(Bq)])
+    S.step_latent = u16_to_bf16(lat, device)
+    S.step_idx_key = u16_to_bf16(key, device)
+    S.step_seq = torch.arange(Bq, dtype=torch.int32, device=device).repeat_interleave(nq)
+    S.step_pos = torch.arange(pre, N, dtype=torch.int64, device=device).repeat(Bq)
+    for li in range(n_layers):
+        x = np.concatenate([synth.latent(seed, b, pre, nq, tensor=synth.SWA + li) for b in range(Bq)])
+        S.step_swa.append(u16_to_bf16(x, device))
+        S.step_ring_idx.append((li * Bq + torch.arange(Bq, dtype=torch.int32, device=device)).repeat_interleave(nq))
+    # Per-layer queries.
+    for li, kind in enumerate(wl.layers):
+        qn = np.stack([synth.normal(seed, synth.Q + li, b, pre, nq, 64 * 512) for b in range(Bq)])
+        qn = qn.reshape(Bq, nq, 64, 512)
+        L = Layer(kind=kind, q=u16_to_bf16(qn, device), q_u16=qn,
+                  ring_idx=(li * Bq + torch.arange(Bq, dtype=torch.int32, device=device)))
+        if kind in ("full", "reindex"):
+            qi = np.stack([synth.normal(seed, synth.IDXQ + li, b, pre, nq, 32 * 128) for b in range(Bq)])
+            L.q_idx_u16 = qi.reshape(Bq, nq, 32, 128)
+            L.q_idx = u16_to_bf16(L.q_idx_u16, device)
+            L.w_np = np.stack([synth.uniform(seed, synth.W + li, b, pre, nq, 32) for b in range(Bq)])
+            L.w = torch.from_numpy(L.w_np).to(device)
+            L.q_codes = torch.empty(Bq, nq, 32, 64, dtype=torch.uint8, device=device)
+            L.q_scales = torch.empty(Bq, nq, 32, 8, dtype=torch.uint8, device=device)
+        if kind == "reindex":
+            pools = np.full((Bq, nq, 2048), -1, np.int32)
+            for b in range(Bq):
+                for j in range(nq):
+                    t = N - nq + j
+                    s = synth.sample_sorted(seed, synth.POOL + li, b, t, n_blocks(t), 2048)
+                    pools[b, j, : s.size] = s
+            L.pool = torch.from_numpy(pools).to(device)
+        S.layers.append(L)
+    if wl.layers[0] == "reuse":
+        tk = np.full((Bq, nq, 512), -1, np.int32)
+        for b in range(Bq):
+            for j in range(nq):
+                t = N - nq + j
+                s = synth.sample_sorted(seed, synth.TOPK, b, t, t + 1, 512)
+                tk[b, j, : s.size] = s
+        S.topk = torch.from_numpy(tk).to(device)
+    else:
+        S.topk = torch.full((Bq, nq, 512), -1, dtype=torch.int32, device=device)
+    if prefill_step:
+        append_step(S)
+    return S
+
+
+def append_step(S: Setup):
+    """A1 + A2 of one decode step: the n_q new entries of every sequence."""
+    import sparse_attention_fp4_mxfp4_gb300 as csa2
+    c = S.cache
+    csa2.csa2_append_kv(S.step_latent, S.step_idx_key, S.step_seq, S.step_pos, c.block_table, c.main_pages,
+                        c.idx_pages)
+    for li in range(len(S.layers)):
+        csa2.csa2_append_swa(S.step_swa[li], S.step_ring_idx[li], S.step_pos, c.rings)
+
+
+# ---- oracle references ------------------------------------------------------------
+
+def oracle_keys(S: Setup, b: int, t: int) -> np.ndarray:
+    return synth.normal(S.wl.seed, synth.IDXKEY, b, 0, t + 1, 128)
+
+
+def oracle_full(S: Setup, b: int, j: int, li: int = 0, keys=None):
+    import oracle
+    L = S.layers[li]
+    t = S.t(j)
+    keys = oracle_keys(S, b, t) if keys is None else keys
+    return oracle.full_indexer(L.q_idx_u16[b, j], L.w_np[b, j], keys, t)
+
+
+def oracle_reindex(S: Setup, b: int, j: int, li: int, pool_row, keys=None):
+    import oracle
+    L = S.layers[li]
+    t = S.t(j)
+    keys = oracle_keys(S, b, t) if keys is None else keys
+    return oracle.reindex(L.q_idx_u16[b, j], L.w_np[b, j], keys, t, np.asarray(pool_row, np.int32))
+
+
+def oracle_attention(S: Setup, b: int, j: int, li: int, topk_row):
+    import oracle
+    seed = S.wl.seed
+    t = S.t(j)
+    sel = np.asarray(topk_row)
+    sel = sel[sel >= 0].astype(np.int64)
+    main = synth.latent_rows(seed, np.full(sel.size, b), sel)
+    win = oracle.window_positions(t, S.N, 128)
+    wrows = synth.latent_rows(seed, np.full(win.size, b), win, tensor=synth.SWA + li)
+    return oracle.sparse_attention(S.layers[li].q_u16[b, j], main, wrows, TAU)
+
+
+# ---- comparisons -------------------------------------------------------------------
+
+def check_selection(got, want, score_of, k, what=""):
+    """Selections equal except for elements whose oracle score lies within
+    TOPK_TIE_RTOL (relative) of the oracle's k-th score."""
+    got = np.asarray(got)
+    want = np.asarray(want)
+    g = set(got[got >= 0].tolist())
+    w = set(want[want >= 0].tolist())
+    assert len(g) == (got >= 0).sum(), f"{what}: duplicate selections"
+    assert len(g) == len(w), f"{what}: {len(g)} selected, oracle {len(w)}"
+    if g == w:
+        return 0
+    wl = sorted(w, key=lambda i: -score_of(i))
+    kth = score_of(wl[min(k, len(wl)) - 1])
+    tol = TOPK_TIE_RTOL * max(abs(kth), 1e-30)
+    for i in g ^ w:
+        assert abs(score_of(i) - kth) <= tol, (
+            f"{what}: element {i} (score {score_of(i)!r}) differs from the oracle's selection "
+            f"and is not tied with the k-th score {kth!r}")
+    return len(g ^ w)
+
+
+def check_attention(out, ref, tol):
+    """Per (head) row: max_c |o - r| / max_c |r| <= tol."""
+    out = np.asarray(out, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(out - ref).max(-1) / np.maximum(np.abs(ref).max(-1), 1e-30)
+    assert (err <= tol).all(), f"attention max-relative error {err.max():.3e} > {tol} (head {int(err.argmax())})"
+    return float(err.max())
+
+
+# ---- page unpacking (test-side view of the documented layout) ---------------------------
+
+def unpack_main(cache, b: int, positions) -> tuple[np.ndarray, np.ndarray]:
+    """codes uint8 [n, 256] and scales uint8 [n, 32] of the main entries at positions."""
+    bt = cache.block_table.cpu().numpy()
+    pages = cache.main_pages
+    out_c, out_s = [], []
+    pos = np.asarray(positions, np.int64)
+    rows = torch.from_numpy(bt[b, pos // 128].astype(np.int64)).to(pages.device)
+    slots = torch.from_numpy(pos % 128).to(pages.device)
+    ent = pages.view(pages.shape[0], 128, 288)[rows, slots].cpu().numpy()
+    return ent[:, :256], ent[:, 256:]
+
+
+def unpack_idx(cache, b: int, positions) -> tuple[np.ndarray, np.ndarray]:
+    """codes uint8 [n, 64] (channel order) and scales uint8 [n, 8] of indexer keys."""
+    bt = cache.block_table.cpu().numpy()
+    pages = cache.idx_pages
+    pos = np.asarray(positions, np.int64)
+    pg = pages.view(pages.shape[0], 16, 576)
+    rows = torch.from_numpy(bt[b, pos // 128].astype(np.int64)).to(pages.device)
+    grp = torch.from_numpy((pos % 128) // 8).to(pages.device)
+    g = pg[rows, grp].cpu().numpy()  # [n, 576]
+    r = pos % 8
+    codes = g[:, :512].reshape(-1, 4, 8, 16)[np.arange(pos.size), :, r, :].reshape(-1, 64)
+    scales = g[:, 512:].reshape(-1, 8, 8)[np.arange(pos.size), r, :]
+    return codes, scales

@@ -1,0 +1,74 @@
+"""The C-ABI library loads and exports every entry point that include/csa2.h
+declares; host-only calls (sizes, status strings, argument validation) work
+without a GPU. No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa2.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_csa2_build", os.path.join(ROOT, "sparse_attention_fp4_mxfp4_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return ctypes.CDLL(mod.build())
+
+
+def declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(csa2_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for must in ("csa2_append_kv", "csa2_append_swa", "csa2_indexer_full", "csa2_indexer_reindex",
+                 "csa2_indexer_scan", "csa2_block_topk", "csa2_sparse_attn", "csa2_decode_layer",
+                 "csa2_decode_group", "csa2_check_device_status", "csa2_workspace_bytes"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_symbol():
+    import sparse_attention_fp4_mxfp4_gb300 as m
+    assert sorted(m.EXPORTS) == declared()
+
+
+def test_size_queries(lib):
+    n = ctypes.c_size_t()
+    assert lib.csa2_page_bytes(0, ctypes.byref(n)) == 0 and n.value == 36864
+    assert lib.csa2_page_bytes(1, ctypes.byref(n)) == 0 and n.value == 9216
+    assert lib.csa2_page_bytes(7, ctypes.byref(n)) == 1
+    assert lib.csa2_ring_bytes(ctypes.byref(n)) == 0 and n.value == 65536
+    lib.csa2_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    assert lib.csa2_workspace_bytes(3, 64, 1, 65536, ctypes.byref(n)) == 0
+    assert n.value == 64 * 5 * 64 * 512 * 4 + 64 * 5 * 64 * 8
+    assert lib.csa2_workspace_bytes(2, 64, 1, 131072, ctypes.byref(n)) == 0 and n.value == 64 * 16384 * 4
+    assert lib.csa2_workspace_bytes(3, 1, 9, 100, ctypes.byref(n)) == 2  # n_q > 8 unsupported
+    assert lib.csa2_workspace_bytes(3, 1, 0, 100, ctypes.byref(n)) == 1
+
+
+def test_status_strings_and_null_checks(lib):
+    lib.csa2_status_string.restype = ctypes.c_char_p
+    lib.csa2_last_error.restype = ctypes.c_char_p
+    assert lib.csa2_status_string(0) == b"ok"
+    assert lib.csa2_status_string(5).startswith(b"a bounded device wait")
+    p = ctypes.c_void_p
+    lib.csa2_append_kv.argtypes = [p, p, p, p, ctypes.c_int, p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, p, p, p]
+    assert lib.csa2_append_kv(None, None, None, None, 4, None, 1, 1, 1, None, None, None) == 1
+    assert b"latent" in lib.csa2_last_error()
+    assert lib.csa2_append_kv(None, None, None, None, 0, None, 1, 1, 1, None, None, None) == 0  # nothing to do
+    lib.csa2_quant_mxfp4.argtypes = [p, ctypes.c_int64, p, p, p]
+    assert lib.csa2_quant_mxfp4(p(16), 17, p(16), p(16), None) == 1
+    assert lib.csa2_decode_group(None, 1, None) == 1
