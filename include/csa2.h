@@ -186,6 +186,27 @@ int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const 
                          const int32_t* pool, int32_t* topk, void* ws, size_t ws_bytes,
                          void* stream);
 
+/* Same computation and outputs as csa2_indexer_reindex, for callers that cannot
+ * allocate device memory (inside CUDA-graph capture, under a host framework
+ * that owns every allocation, or on a decode path where allocating could
+ * synchronise or fail): the per-slot scores live in a fixed 4 MiB device
+ * array inside the library instead of a caller workspace. The pages have no
+ * counterpart of this entry point; it only changes where scratch lives.
+ *   - At most 64 query tokens per call (B * n_q <= 64); larger calls return
+ *     CSA2_ERR_UNSUPPORTED and allocate nothing.
+ *   - Every GPU that loads the library holds the array until the process
+ *     exits. The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race and must be serialised by the caller. No
+ *     content has to start at zero: each call writes every slot it reads.
+ *   - No cudaMalloc / cudaFree or allocating library routine is called. */
+int csa2_indexer_reindex_noalloc(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                                 const int64_t* seq_len, int B, int n_q,
+                                 const int32_t* block_table, int max_pages, int64_t n_pages,
+                                 const uint8_t* idx_pages, const int32_t* pool, int32_t* topk,
+                                 void* stream);
+
 /* Full-mode indexer = scan + block top-2048 + rescore of the pool + top-512.
  * The final top-512 over the pool equals the top-512 over all causal
  * positions up to ties. ws: csa2_workspace_bytes(CSA2_OP_INDEXER_FULL, ...). */

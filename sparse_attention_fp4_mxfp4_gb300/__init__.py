@@ -33,7 +33,7 @@ EXPORTS = (
     "csa2_status_string", "csa2_last_error", "csa2_version", "csa2_page_bytes", "csa2_ring_bytes",
     "csa2_workspace_bytes", "csa2_append_kv", "csa2_append_swa", "csa2_quant_mxfp4",
     "csa2_dequant_mxfp4", "csa2_quant_fp8", "csa2_indexer_scan", "csa2_block_topk",
-    "csa2_indexer_reindex", "csa2_indexer_full", "csa2_sparse_attn", "csa2_decode_layer",
+    "csa2_indexer_reindex", "csa2_indexer_reindex_noalloc", "csa2_indexer_full", "csa2_sparse_attn", "csa2_decode_layer",
     "csa2_decode_group", "csa2_check_device_status",
 )
 
@@ -79,6 +79,7 @@ def _load():
         "csa2_indexer_scan": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, i64, p], i32),
         "csa2_block_topk": ([p, p, i32, i32, i64, p, p], i32),
         "csa2_indexer_reindex": ([p, p, p, p, i32, i32, p, i32, i64, p, p, p, p, sz, p], i32),
+        "csa2_indexer_reindex_noalloc": ([p, p, p, p, i32, i32, p, i32, i64, p, p, p, p], i32),
         "csa2_indexer_full": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, p, p, sz, p], i32),
         "csa2_sparse_attn": ([p, p, p, i32, i32, p, i32, i64, p, p, p, i64, f32, i32, p, p, p, sz, p], i32),
         "csa2_decode_layer": ([ctypes.POINTER(LayerArgs), p], i32),
@@ -225,6 +226,16 @@ def csa2_indexer_reindex(q_codes, q_scales, w, seq_len, block_table, n_pages, id
                                     _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx_pages),
                                     _ptr(pool), _ptr(topk), _ptr(ws), ws.numel() * ws.element_size(),
                                     _stream(stream)))
+
+
+def csa2_indexer_reindex_noalloc(q_codes, q_scales, w, seq_len, block_table, n_pages, idx_pages, pool, topk,
+                                 stream=None):
+    """csa2_indexer_reindex without a workspace (scores kept in the library's
+    fixed device array; at most 64 query tokens per call)."""
+    B, n_q = w.shape[0], w.shape[1]
+    _check(lib.csa2_indexer_reindex_noalloc(_ptr(q_codes), _ptr(q_scales), _ptr(w), _ptr(seq_len), B, n_q,
+                                            _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx_pages),
+                                            _ptr(pool), _ptr(topk), _stream(stream)))
 
 
 def csa2_indexer_full(q_codes, q_scales, w, seq_len, max_ctx, block_table, n_pages, idx_pages, pool, topk,

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcsa2.so")
-SOURCES = ["append.cu", "indexer.cu", "topk.cu", "attn.cu", "capi.cu"]
+SOURCES = ["append.cu", "indexer.cu", "topk.cu", "attn.cu", "capi.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -65,6 +65,10 @@ int check_pages(const int32_t* block_table, int max_pages, int64_t n_pages) {
 
 }  // namespace
 
+namespace csa2 {
+int record_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace csa2
+
 extern "C" {
 
 const char* csa2_status_string(int status) {

@@ -8,6 +8,9 @@
 
 namespace csa2 {
 
+// Sets the thread-local text returned by csa2_last_error(); returns `code`.
+int record_error(int code, const char* msg);
+
 // Each kernel translation unit keeps its own device status word; these read
 // (and optionally clear) it. Synchronous with respect to `stream`.
 cudaError_t status_append(cudaStream_t stream, int* code, int* where, bool clear);
