@@ -150,14 +150,17 @@ def attn_bytes_per_query() -> int:
 
 
 def step_bytes(wl) -> int:
+    """Reads the method must do per step, summed over the workload's layers."""
     q = wl.B * wl.n_q
-    if wl.mode == "full":
-        return scan_bytes(wl) + q * attn_bytes_per_query()
-    if wl.mode == "reuse":
-        return q * attn_bytes_per_query()
-    if wl.mode == "reindex":
-        return q * (2048 * 576 + 32 * 72 + 32 * 4 + 2048 * 4 + attn_bytes_per_query())
-    raise ValueError(wl.mode)
+    total = 0
+    for kind in wl.layers:
+        if kind == "full":
+            total += scan_bytes(wl) + q * attn_bytes_per_query()
+        elif kind == "reindex":
+            total += q * (2048 * 576 + 32 * 72 + 32 * 4 + 2048 * 4 + attn_bytes_per_query())
+        else:
+            total += q * attn_bytes_per_query()
+    return total
 
 
 # ---- our arm ------------------------------------------------------------------------------------
@@ -173,21 +176,12 @@ def run_ours(args, wl, rank, world, local):
         dist.init_process_group("nccl", device_id=dev)
     t_setup = time.time()
     S = H.build(wl, dev)
+    R = H.Runner(S)
     torch.cuda.synchronize()
     setup_s = time.time() - t_setup
     B, n_q, N = wl.B, wl.n_q, wl.N
     Q = B * n_q
     stream = torch.cuda.current_stream()
-    c = S.cache
-    L = S.layers[0]
-    out = torch.empty(B, n_q, 64, 512, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(B, n_q, 64, dtype=torch.float32, device=dev)
-    ws = torch.empty(csa2.csa2_workspace_bytes(csa2.OP_DECODE_LAYER, B, n_q, N), dtype=torch.uint8, device=dev)
-    pool = torch.empty(B, n_q, 2048, dtype=torch.int32, device=dev)
-    topk = S.topk if wl.mode == "reuse" else torch.empty(B, n_q, 512, dtype=torch.int32, device=dev)
-    max_blocks = (N + 7) // 8
-    bm = ws[: Q * max_blocks * 4].view(torch.float32).view(B, n_q, max_blocks)
-    rws = ws[((Q * max_blocks * 4 + 255) // 256) * 256:]
     ev = {}
 
     def mark(name):
@@ -195,45 +189,8 @@ def run_ours(args, wl, rank, world, local):
         e.record(stream)
         ev.setdefault(name, []).append(e)
 
-    launches_per_step = 0
-
-    def step(timed_marks):
-        nonlocal launches_per_step
-        n = 0
-        H.append_step(S)
-        n += 1 + len(S.layers)
-        if wl.mode in ("full", "reindex"):
-            csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
-            n += 1
-        if wl.mode == "full":
-            if timed_marks:
-                mark("scan0")
-            csa2.csa2_indexer_scan(L.q_codes, L.q_scales, L.w, S.seq_len, N, c.block_table, c.n_pages,
-                                   c.idx_pages, bm)
-            if timed_marks:
-                mark("scan1")
-            csa2.csa2_block_topk(bm, S.seq_len, pool)
-            n += 2
-        if wl.mode in ("full", "reindex"):
-            p = pool if wl.mode == "full" else L.pool
-            if timed_marks:
-                mark("rescore0")
-            csa2.csa2_indexer_reindex(L.q_codes, L.q_scales, L.w, S.seq_len, c.block_table, c.n_pages,
-                                      c.idx_pages, p, topk, rws)
-            if timed_marks:
-                mark("rescore1")
-            n += 2
-        if timed_marks:
-            mark("attn0")
-        csa2.csa2_sparse_attn(L.q, topk, S.seq_len, c.block_table, c.n_pages, c.main_pages, c.rings,
-                              L.ring_idx, out, lse, ws)
-        if timed_marks:
-            mark("attn1")
-        n += 2
-        launches_per_step = n
-
     for _ in range(args.warmup):
-        step(False)
+        R.step()
     torch.cuda.synchronize()
     st = csa2.csa2_check_device_status()
     if st != csa2.OK:
@@ -247,7 +204,7 @@ def run_ours(args, wl, rank, world, local):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step(True)
+        R.step(mark)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -255,28 +212,30 @@ def run_ours(args, wl, rank, world, local):
     ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(ms, world, dev)
     stage_ms = {}
-    for name in ("scan", "rescore", "attn"):
+    for name in ("scan", "blocktopk", "rescore", "attn"):
         if name + "0" in ev:
             tt = [a.elapsed_time(b) for a, b in zip(ev[name + "0"], ev[name + "1"])]
-            stage_ms[name] = sum(tt) / len(tt)
+            stage_ms[name] = sum(tt) / args.steps  # per step (all layers)
     st = csa2.csa2_check_device_status()
     if st != csa2.OK:
         raise RuntimeError("device status after timing: " + csa2.device_status_message())
 
-    # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, wl, S, out, lse, ws, pool, topk, dev)
+        e2e = run_e2e(args, wl, S, R, dev)
 
     peak, peak_kind = measured_peaks()
-    if wl.mode == "full":
-        dom, dom_bytes = "indexer_scan", scan_bytes(wl)
-    elif wl.mode == "reindex":
-        dom, dom_bytes = "indexer_rescore", Q * (2048 * 576 + 32 * 72 + 32 * 4 + 2048 * 4)
+    kinds = [L.kind for L in S.layers]
+    if "full" in kinds:
+        dom, dom_bytes, dom_stage, per_step = "indexer_scan", scan_bytes(wl), "scan", 1
+    elif "reindex" in kinds:
+        dom, dom_bytes, dom_stage, per_step = ("indexer_rescore", Q * (2048 * 576 + 32 * 72 + 32 * 4 + 2048 * 4),
+                                               "rescore", kinds.count("reindex"))
     else:
-        dom, dom_bytes = "sparse_attn", Q * attn_bytes_per_query()
-    dom_ms = stage_ms.get({"indexer_scan": "scan", "indexer_rescore": "rescore", "sparse_attn": "attn"}[dom])
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else None
+        dom, dom_bytes, dom_stage, per_step = "sparse_attn", Q * attn_bytes_per_query(), "attn", len(kinds)
+    dom_ms = stage_ms.get(dom_stage)
+    launch_ms = dom_ms / per_step if dom_ms else None
+    achieved = dom_bytes / (launch_ms * 1e-3) / 1e9 if launch_ms else None
     traffic = None
     rec = NCU_TRAFFIC.get((dom, wl.index))
     if rec and rec["hash"] == source_hash(rec["files"]):
@@ -297,18 +256,18 @@ def run_ours(args, wl, rank, world, local):
         "vs_baseline": None,
         "dtype": "fp4(e2m1)+e4m3 storage, f16 tensor-core operands, fp32 accumulate/softmax, bf16 out",
         "data": "synthetic (seeded generator; RMSNormed post-RoPE latents, N(0,1) indexer keys/queries)",
-        "config": {"workload": wl.name, "mode": wl.mode, "batch": B, "context": N, "query_tokens": n_q,
-                   "queries_per_step": Q, "l2": "inputs larger than L2 (the scanned indexer plane and the "
-                   "gathered KV exceed the 126 MB L2)" if wl.mode != "reuse" else "store larger than L2; "
-                   "gathers are random", "parallelism": f"replicas x{world} (independent sequences)",
-                   "setup_s": round(setup_s, 1)},
+        "config": {"workload": wl.name, "mode": wl.mode, "layers": list(kinds), "batch": B, "context": N,
+                   "query_tokens": n_q, "queries_per_step": Q,
+                   "l2": "inputs larger than L2 (store of %.1f GB; the step reads %.0f MB)" % (
+                       S.cache.nbytes() / 1e9, step_bytes(wl) / 1e6),
+                   "parallelism": f"replicas x{world} (independent sequences)", "setup_s": round(setup_s, 1)},
         "hbm_fraction_step": (sb / (ms_max * 1e-3) / 1e9) / peak,
         "stage_ms": stage_ms,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": (achieved / peak) if achieved else None, "traffic": traffic,
                      "algorithmic_bytes_per_launch": dom_bytes, "peak_source": peak_kind},
         "clocks": clk,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": R.launches * args.steps,
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -316,43 +275,49 @@ def run_ours(args, wl, rank, world, local):
     return line
 
 
-def run_e2e(args, wl, S, out, lse, ws, pool, topk, dev):
+def run_e2e(args, wl, S, R, dev):
     """Same step through the public C-ABI with host inputs: every step copies
-    its new entries and queries from pinned host memory and reads the output
-    back."""
+    its new entries and every layer's queries from pinned host memory, runs
+    the layers with csa2_decode_group and reads every layer's output back."""
     import sparse_attention_fp4_mxfp4_gb300 as csa2
     c = S.cache
-    L = S.layers[0]
-    host = {
-        "latent": S.step_latent.cpu().pin_memory(), "key": S.step_idx_key.cpu().pin_memory(),
-        "swa": S.step_swa[0].cpu().pin_memory(), "q": L.q.cpu().pin_memory(),
-    }
-    if L.q_idx is not None:
-        host["q_idx"] = L.q_idx.cpu().pin_memory()
-        host["w"] = L.w.cpu().pin_memory()
+    host = {"latent": S.step_latent, "key": S.step_idx_key}
+    for li, L in enumerate(S.layers):
+        host[f"swa{li}"] = S.step_swa[li]
+        host[f"q{li}"] = L.q
+        if L.q_idx is not None:
+            host[f"qi{li}"] = L.q_idx
+            host[f"w{li}"] = L.w
+    host = {k: v.cpu().pin_memory() for k, v in host.items()}
     dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    mode = {"full": csa2.MODE_FULL, "reindex": csa2.MODE_REINDEX, "reuse": csa2.MODE_REUSE}[wl.mode]
-    a = csa2.layer_args(mode, B=wl.B, n_q=wl.n_q, max_ctx=wl.N, seq_len=S.seq_len, block_table=c.block_table,
-                        n_pages=c.n_pages, main_pages=c.main_pages, idx_pages=c.idx_pages, rings=c.rings,
-                        ring_idx=L.ring_idx, q=dev_in["q"], out=out, ws=ws, lse=lse,
-                        q_idx_codes=L.q_codes, q_idx_scales=L.q_scales, w=dev_in.get("w"),
-                        pool=pool if wl.mode == "full" else L.pool, topk=topk)
+    outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in R.out]
+    lses_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in R.lse]
+    mode = {"full": csa2.MODE_FULL, "reindex": csa2.MODE_REINDEX, "reuse": csa2.MODE_REUSE}
+    args_list = []
+    for li, L in enumerate(S.layers):
+        args_list.append(csa2.layer_args(
+            mode[L.kind], B=wl.B, n_q=wl.n_q, max_ctx=wl.N, seq_len=S.seq_len, block_table=c.block_table,
+            n_pages=c.n_pages, main_pages=c.main_pages, idx_pages=c.idx_pages, rings=c.rings,
+            ring_idx=L.ring_idx, q=dev_in[f"q{li}"], out=R.out[li], ws=R.ws, lse=R.lse[li],
+            q_idx_codes=L.q_codes, q_idx_scales=L.q_scales, w=dev_in.get(f"w{li}"),
+            pool=R.pool if L.kind == "full" else L.pool if L.kind == "reindex" else None,
+            topk=R.topk if L.kind != "reuse" or li == 0 else None))
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    d2h = sum(o.numel() * o.element_size() for o in outs_h) + sum(x.numel() * 4 for x in lses_h)
 
     def step():
         for k, v in host.items():
             dev_in[k].copy_(v, non_blocking=True)
         csa2.csa2_append_kv(dev_in["latent"], dev_in["key"], S.step_seq, S.step_pos, c.block_table,
                             c.main_pages, c.idx_pages)
-        csa2.csa2_append_swa(dev_in["swa"], S.step_ring_idx[0], S.step_pos, c.rings)
-        if "q_idx" in dev_in:
-            csa2.csa2_quant_mxfp4(dev_in["q_idx"], L.q_codes, L.q_scales)
-        csa2.csa2_decode_layer(a)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        for li, L in enumerate(S.layers):
+            csa2.csa2_append_swa(dev_in[f"swa{li}"], S.step_ring_idx[li], S.step_pos, c.rings)
+            if L.q_idx is not None:
+                csa2.csa2_quant_mxfp4(dev_in[f"qi{li}"], L.q_codes, L.q_scales)
+        csa2.csa2_decode_group(args_list)
+        for li in range(len(S.layers)):
+            outs_h[li].copy_(R.out[li], non_blocking=True)
+            lses_h[li].copy_(R.lse[li], non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -472,11 +437,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--B", type=int, default=None, help="override the batch (profiling captures only)")
+    ap.add_argument("--N", type=int, default=None, help="override the context (profiling captures only)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     from synth.workloads import WORKLOADS
     wl = WORKLOADS[args.workload]
+    if args.B or args.N:
+        from synth.workloads import Workload
+        wl = Workload(wl.index, wl.name + f"_B{args.B or wl.B}_N{args.N or wl.N}", wl.mode, B=args.B or wl.B,
+                      N=args.N or wl.N, n_q=wl.n_q, layers=wl.layers)
     rank, world, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, wl, rank, world)

@@ -172,6 +172,67 @@ def append_step(S: Setup):
         csa2.csa2_append_swa(S.step_swa[li], S.step_ring_idx[li], S.step_pos, c.rings)
 
 
+class Runner:
+    """One decode step of a materialised workload, as bench.py times it: the
+    step's appends (A1, A2), then every layer in order. A FULL layer quantises
+    its indexer query, scans, selects the pool and the top-512; a REINDEX
+    layer quantises its query and rescores its pool; every layer then runs
+    sparse attention with the latest top-k, its own query and its own ring."""
+
+    def __init__(self, S: Setup, out_dtype=torch.bfloat16):
+        import sparse_attention_fp4_mxfp4_gb300 as csa2
+        self.csa2 = csa2
+        self.S = S
+        dev = S.seq_len.device
+        B, n_q, N = S.B, S.n_q, S.N
+        Q = B * n_q
+        self.max_blocks = (N + 7) // 8
+        self.ws = torch.empty(csa2.csa2_workspace_bytes(csa2.OP_DECODE_LAYER, B, n_q, N), dtype=torch.uint8,
+                              device=dev)
+        bm_bytes = Q * self.max_blocks * 4
+        self.bm = self.ws[:bm_bytes].view(torch.float32).view(B, n_q, self.max_blocks)
+        self.rws = self.ws[((bm_bytes + 255) // 256) * 256:]
+        self.pool = torch.empty(B, n_q, 2048, dtype=torch.int32, device=dev)
+        self.topk = S.topk if S.layers[0].kind == "reuse" else torch.empty(B, n_q, 512, dtype=torch.int32,
+                                                                            device=dev)
+        self.out = [torch.empty(B, n_q, 64, 512, dtype=out_dtype, device=dev) for _ in S.layers]
+        self.lse = [torch.empty(B, n_q, 64, dtype=torch.float32, device=dev) for _ in S.layers]
+        self.launches = 0
+
+    def step(self, mark=None):
+        csa2, S, c = self.csa2, self.S, self.S.cache
+        mark = mark or (lambda name: None)
+        n = 0
+        append_step(S)
+        n += 1 + len(S.layers)
+        for li, L in enumerate(S.layers):
+            if L.kind in ("full", "reindex"):
+                csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
+                n += 1
+            if L.kind == "full":
+                mark("scan0")
+                csa2.csa2_indexer_scan(L.q_codes, L.q_scales, L.w, S.seq_len, S.N, c.block_table, c.n_pages,
+                                       c.idx_pages, self.bm)
+                mark("scan1")
+                mark("blocktopk0")
+                csa2.csa2_block_topk(self.bm, S.seq_len, self.pool)
+                mark("blocktopk1")
+                n += 2
+            if L.kind in ("full", "reindex"):
+                pool = self.pool if L.kind == "full" else L.pool
+                mark("rescore0")
+                csa2.csa2_indexer_reindex(L.q_codes, L.q_scales, L.w, S.seq_len, c.block_table, c.n_pages,
+                                          c.idx_pages, pool, self.topk, self.rws)
+                mark("rescore1")
+                n += 2
+            mark("attn0")
+            csa2.csa2_sparse_attn(L.q, self.topk, S.seq_len, c.block_table, c.n_pages, c.main_pages, c.rings,
+                                  L.ring_idx, self.out[li], self.lse[li], self.ws)
+            mark("attn1")
+            n += 2
+        self.launches = n
+
+
 # ---- oracle references ------------------------------------------------------------
 
 def oracle_keys(S: Setup, b: int, t: int) -> np.ndarray:

@@ -1,0 +1,120 @@
+"""Parity at the five workloads' full sizes, in the launch sequence bench.py
+times (tests.harness.Runner), on outputs the oracle can compute one by one:
+
+  0  Full, 1 x 32K:          the query's pool, top-512 and attention
+  1  Reuse, 64 x 64K:        attention of 8 sampled queries; page bytes of 2 sequences
+  2  Reindex, 64 x 128K:     top-512 and attention of 6 sampled queries
+  3  Full, 8 x 1M:           pool and top-512 of every sequence, attention of 2
+  4  Reindex + 3 Reuse, 32 x 256K, 6 tokens: top-512 of 4 sampled (sequence,
+     token) pairs and the attention of all four layers for them
+
+Selections: equal up to ties within 1e-5 relative of the oracle's k-th score.
+Attention: within 4e-3 max-relative per head row (bf16 output, as timed).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth.workloads import WORKLOADS
+from tests import harness as H
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+import sparse_attention_fp4_mxfp4_gb300 as csa2  # noqa: E402
+
+DEV = "cuda"
+
+
+def _run(index):
+    S = H.build(WORKLOADS[index], DEV)
+    R = H.Runner(S)
+    R.step()
+    torch.cuda.synchronize()
+    assert csa2.csa2_check_device_status() == csa2.OK, csa2.device_status_message()
+    return S, R
+
+
+def _samples(S, n, seed):
+    rng = np.random.default_rng(seed)
+    pairs = {(int(rng.integers(S.B)), int(rng.integers(S.n_q))) for _ in range(4 * n)}
+    return sorted(pairs)[:n]
+
+
+def _check_attn(S, R, b, j, li, topk_row):
+    ro, rl = H.oracle_attention(S, b, j, li, topk_row)
+    H.check_attention(R.out[li][b, j].float().cpu().numpy(), ro, H.TOL_ATTN_BF16)
+    np.testing.assert_allclose(R.lse[li][b, j].cpu().numpy(), rl, rtol=1e-4, atol=1e-4)
+
+
+def _check_full(S, R, b, j):
+    ref = H.oracle_full(S, b, j)
+    pool = R.pool[b, j].cpu().numpy()
+    tk = R.topk[b, j].cpu().numpy()
+    H.check_selection(pool, ref["pool"], lambda i: ref["blockmax"][i], 2048, f"pool {b},{j}")
+    H.check_selection(tk, ref["topk"], lambda i: ref["scores"][i], 512, f"topk {b},{j}")
+    return tk
+
+
+def test_workload0_full_b1_n32k():
+    S, R = _run(0)
+    tk = _check_full(S, R, 0, 0)
+    _check_attn(S, R, 0, 0, 0, tk)
+    del S, R
+    torch.cuda.empty_cache()
+
+
+def test_workload1_reuse_b64_n64k():
+    S, R = _run(1)
+    tk = R.topk.cpu().numpy()
+    for b, j in _samples(S, 8, 1):
+        _check_attn(S, R, b, j, 0, tk[b, j])
+    for b in (0, S.B - 1):
+        pos = np.concatenate([np.arange(0, 300), np.arange(S.N - 300, S.N)])
+        mc, ms = H.unpack_main(S.cache, b, pos)
+        rows = synth.latent_rows(S.wl.seed, np.full(pos.size, b), pos)
+        rc, rs = oracle.mxfp4_quant(synth.bf16_to_f32(rows))
+        assert np.array_equal(mc, rc) and np.array_equal(ms, rs)
+    del S, R
+    torch.cuda.empty_cache()
+
+
+def test_workload2_reindex_b64_n128k():
+    S, R = _run(2)
+    tk = R.topk.cpu().numpy()
+    pools = S.layers[0].pool.cpu().numpy()
+    for b, j in _samples(S, 6, 2):
+        ref = H.oracle_reindex(S, b, j, 0, pools[b, j])
+        ps = ref["pos_scores"]
+        slot = {int(pools[b, j][i // 8]) * 8 + i % 8: ps[i] for i in range(ps.size) if pools[b, j][i // 8] >= 0}
+        H.check_selection(tk[b, j], ref["topk"], lambda p: slot[p], 512, f"reindex {b},{j}")
+        _check_attn(S, R, b, j, 0, tk[b, j])
+    del S, R
+    torch.cuda.empty_cache()
+
+
+def test_workload3_full_b8_n1m():
+    S, R = _run(3)
+    for b in range(S.B):
+        tk = _check_full(S, R, b, 0)
+        if b in (0, S.B - 1):
+            _check_attn(S, R, b, 0, 0, tk)
+    del S, R
+    torch.cuda.empty_cache()
+
+
+def test_workload4_group_b32_n256k_q6():
+    S, R = _run(4)
+    tk = R.topk.cpu().numpy()
+    pools = S.layers[0].pool.cpu().numpy()
+    for b, j in _samples(S, 4, 4):
+        keys = H.oracle_keys(S, b, S.t(j))
+        ref = H.oracle_reindex(S, b, j, 0, pools[b, j], keys=keys)
+        ps = ref["pos_scores"]
+        slot = {int(pools[b, j][i // 8]) * 8 + i % 8: ps[i] for i in range(ps.size) if pools[b, j][i // 8] >= 0}
+        H.check_selection(tk[b, j], ref["topk"], lambda p: slot[p], 512, f"group reindex {b},{j}")
+        for li in range(4):
+            _check_attn(S, R, b, j, li, tk[b, j])
+    del S, R
+    torch.cuda.empty_cache()
