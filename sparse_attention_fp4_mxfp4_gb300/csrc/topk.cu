@@ -4,12 +4,14 @@
 // 3.4): the 2048 best 8-position blocks by block maximum form the candidate
 // pool; the 512 best pool positions form the top-k.
 //
-// One CTA of 1024 threads per query token. Exact radix select on the
+// Exact radix select on the
 // order-preserving integer image of the fp32 scores (digits of 11, 11 and 10
 // bits), then an ordered compaction: everything above the threshold, plus the
 // lowest-index elements equal to it until k are taken. The output is in
 // ascending index order and padded with -1. Invalid elements (masked slots,
-// -inf, NaN) are never selected.
+// -inf, NaN) are never selected. The cluster kernel below keeps the row in
+// shared memory; the single-CTA global-memory kernel serves rows too long for
+// a 16-CTA cluster.
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -172,6 +174,209 @@ __global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __res
   for (int i = static_cast<int>(tot_sel) + tid; i < k; i += kThreads) orow[i] = -1;
 }
 
+// ---- cluster version: the row lives in shared memory ------------------------
+//
+// A cluster of C CTAs (C <= 16) selects from one row; CTA r keeps elements
+// [r * chunk, (r + 1) * chunk) of the row in its shared memory as ordered keys,
+// so the row is read from global memory once. Each radix pass builds a local
+// histogram; every CTA then sums all C histograms through distributed shared
+// memory and derives the same threshold digit. The ordered compaction uses
+// the per-CTA counts exchanged the same way. Control flow is uniform across
+// the cluster: every CTA executes every cluster barrier.
+constexpr int kChunk = 16384;  // elements per CTA
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t dsmem_ld(const uint32_t* local, uint32_t rank) {
+  uint32_t ra, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads) cluster_topk_kernel(const float* __restrict__ keys,
+                                                                int64_t row_stride,
+                                                                const int64_t* __restrict__ seq_len,
+                                                                int n_q, int k, int C,
+                                                                const int32_t* __restrict__ pool,
+                                                                int32_t* __restrict__ out) {
+  extern __shared__ uint32_t sm[];
+  uint32_t* key = sm;                    // [kChunk] ordered keys of this CTA's slice
+  uint32_t* hist = sm + kChunk;          // [2048] local histogram
+  uint32_t* tot = hist + 2048;           // [2048] cluster-wide histogram
+  uint32_t* warp_sums = tot + 2048;      // [32]
+  uint32_t* xchg = warp_sums + 32;       // [4]: gt, eq of this CTA
+  uint32_t* s_sel = xchg + 4;            // [2]
+
+  const uint32_t r = cluster_rank();
+  const int q = blockIdx.y;
+  const int b = q / n_q, j = q % n_q;
+  const int tid = threadIdx.x;
+  int64_t n;
+  if (kMode == 0) {
+    const int64_t t = seq_len[b] - n_q + j;
+    n = t >= 0 ? (t + 8) / 8 : 0;
+    if (n > row_stride || n > static_cast<int64_t>(C) * kChunk) {
+      if (tid == 0 && r == 0) report(CSA2_ERR_DEVICE_BOUNDS, 311);
+      n = min(row_stride, static_cast<int64_t>(C) * kChunk);
+    }
+  } else {
+    n = row_stride;
+  }
+  const int64_t chunk = (n + C - 1) / C;
+  const int64_t lo = static_cast<int64_t>(r) * chunk;
+  const int64_t hi = min(n, lo + chunk);
+  const int m = hi > lo ? static_cast<int>(hi - lo) : 0;
+  const float* row = keys + static_cast<int64_t>(q) * row_stride + lo;
+  for (int i = tid; i < m; i += kThreads) key[i] = ordered_key(row[i]);
+  __syncthreads();
+
+  uint32_t prefix = 0, mask = 0, remaining = static_cast<uint32_t>(k);
+  bool all_valid = false;
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int sh = shifts[pass];
+    const uint32_t nb = 1u << widths[pass];
+    for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < m; i += kThreads) {
+      const uint32_t u = key[i];
+      if (u != 0u && (u & mask) == prefix) atomicAdd(&hist[(u >> sh) & (nb - 1)], 1u);
+    }
+    cluster_sync_all();  // every local histogram is complete
+    for (int i = tid; i < 2048; i += kThreads) {
+      uint32_t s = 0;
+      for (int c = 0; c < C; ++c) s += dsmem_ld(&hist[i], c);
+      tot[i] = s;
+    }
+    cluster_sync_all();  // nobody reads a remote histogram any more
+    const uint32_t hi_bin = nb - 1 - 2 * tid, lo_bin = hi_bin - 1;
+    uint32_t c_hi = 0, c_lo = 0;
+    if (2 * static_cast<uint32_t>(tid) < nb) {
+      c_hi = tot[hi_bin];
+      c_lo = tot[lo_bin];
+    }
+    uint32_t total;
+    const uint32_t before = block_excl_scan(c_hi + c_lo, warp_sums, &total);
+    if (pass == 0 && total <= static_cast<uint32_t>(k)) {
+      all_valid = true;
+      break;
+    }
+    if (2 * static_cast<uint32_t>(tid) < nb) {
+      if (before < remaining && before + c_hi >= remaining) {
+        s_sel[0] = hi_bin;
+        s_sel[1] = before;
+      } else if (before + c_hi < remaining && before + c_hi + c_lo >= remaining) {
+        s_sel[0] = lo_bin;
+        s_sel[1] = before + c_hi;
+      }
+    }
+    __syncthreads();
+    remaining -= s_sel[1];
+    prefix |= s_sel[0] << sh;
+    mask |= (nb - 1) << sh;
+    __syncthreads();
+  }
+  const uint32_t T = all_valid ? 0u : prefix;
+  const uint32_t need_eq = all_valid ? 0u : remaining;
+
+  // Per-thread contiguous segments of this CTA's slice keep index order.
+  const int seg = (m + kThreads - 1) / kThreads;
+  const int s0 = tid * seg, s1 = min(m, s0 + seg);
+  uint32_t gt = 0, eq = 0;
+  for (int i = s0; i < s1; ++i) {
+    const uint32_t u = key[i];
+    if (u > T) ++gt;
+    else if (u == T && u != 0u) ++eq;
+  }
+  uint32_t cta_eq, cta_gt;
+  const uint32_t eq_base_local = block_excl_scan(eq, warp_sums, &cta_eq);
+  block_excl_scan(gt, warp_sums, &cta_gt);
+  if (tid == 0) {
+    xchg[0] = cta_gt;
+    xchg[1] = cta_eq;
+  }
+  cluster_sync_all();
+  // Ties go to the lowest indices: CTA slices are in index order.
+  uint32_t eq_before = 0, sel_before = 0, total_sel = 0, eq_cta_before = 0;
+  for (uint32_t c = 0; c < static_cast<uint32_t>(C); ++c) {
+    const uint32_t g = dsmem_ld(&xchg[0], c), e = dsmem_ld(&xchg[1], c);
+    const uint32_t take = need_eq > eq_before ? min(e, need_eq - eq_before) : 0u;
+    if (c < r) {
+      sel_before += g + take;
+      eq_cta_before += e;
+    }
+    total_sel += g + take;
+    eq_before += e;
+  }
+  const uint32_t eq_base = eq_cta_before + eq_base_local;
+  const uint32_t take_eq = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
+  uint32_t cta_sel;
+  uint32_t o = sel_before + block_excl_scan(gt + take_eq, warp_sums, &cta_sel);
+  int32_t* orow = out + static_cast<int64_t>(q) * k;
+  const int32_t* prow = pool + static_cast<int64_t>(q) * 2048;
+  uint32_t taken_eq = 0;
+  for (int i = s0; i < s1; ++i) {
+    const uint32_t u = key[i];
+    bool sel = u > T;
+    if (!sel && u == T && u != 0u && taken_eq < take_eq) {
+      sel = true;
+      ++taken_eq;
+    }
+    if (sel) {
+      const int64_t gi = lo + i;
+      const int32_t v = kMode == 0 ? static_cast<int32_t>(gi) : prow[gi >> 3] * 8 + static_cast<int32_t>(gi & 7);
+      if (o < static_cast<uint32_t>(k)) orow[o] = v;  // never past the row, whatever the counts say
+      ++o;
+    }
+  }
+  if (r == 0)
+    for (int i = static_cast<int>(min(total_sel, static_cast<uint32_t>(k))) + tid; i < k; i += kThreads) orow[i] = -1;
+  cluster_sync_all();  // keep this CTA's shared memory alive until every remote read is done
+}
+
+constexpr size_t kClusterSmem = (kChunk + 2048 + 2048 + 32 + 4 + 4) * sizeof(uint32_t);
+
+template <int kMode>
+cudaError_t launch_cluster_topk(const float* keys, int64_t row_stride, const int64_t* seq_len, int Q,
+                                int n_q, int k, int C, const int32_t* pool, int32_t* out,
+                                cudaStream_t stream) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(cluster_topk_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kClusterSmem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(cluster_topk_kernel<kMode>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, Q, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kClusterSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, cluster_topk_kernel<kMode>, keys, row_stride, seq_len, n_q, k, C, pool, out);
+}
+
 }  // namespace
 
 cudaError_t status_topk(cudaStream_t stream, int* code, int* where, bool clear) {
@@ -192,6 +397,13 @@ cudaError_t launch_block_topk(const float* block_max, const int64_t* seq_len, in
                               int64_t max_blocks, int32_t* pool, cudaStream_t stream) {
   const int Q = B * n_q;
   if (Q == 0) return cudaSuccess;
+  const int64_t C = (max_blocks + kChunk - 1) / kChunk;
+  if (C <= 16) {
+    const cudaError_t e = launch_cluster_topk<0>(block_max, max_blocks, seq_len, Q, n_q, 2048,
+                                                 static_cast<int>(C < 1 ? 1 : C), nullptr, pool, stream);
+    if (e == cudaSuccess || C <= 8) return e;
+    cudaGetLastError();  // a 16-CTA cluster may not fit this GPU: use the global-memory select
+  }
   radix_topk_kernel<0><<<Q, kThreads, 0, stream>>>(block_max, max_blocks, seq_len, n_q, 2048,
                                                    nullptr, pool);
   return cudaGetLastError();
@@ -201,8 +413,7 @@ cudaError_t launch_pool_topk(const float* scores, const int64_t* seq_len, int B,
                              const int32_t* pool, int32_t* topk, cudaStream_t stream) {
   const int Q = B * n_q;
   if (Q == 0) return cudaSuccess;
-  radix_topk_kernel<1><<<Q, kThreads, 0, stream>>>(scores, 16384, seq_len, n_q, 512, pool, topk);
-  return cudaGetLastError();
+  return launch_cluster_topk<1>(scores, 16384, seq_len, Q, n_q, 512, 1, pool, topk, stream);
 }
 
 }  // namespace csa2
