@@ -3,30 +3,35 @@
 // "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" section
 // 3.4): s(p) = sum_h w_h * max(0, qhat_h . khat_p) over 32 heads x 128 dims.
 //
+// The keys stay in their stored MXFP4 form: the tensor cores multiply packed
+// E2M1 codes with one E4M3 scale per 16 channels (tcgen05.mma
+// kind::mxf4nvf4, scale_vec::4X), which is exactly the storage format, so
+// nothing is dequantised. The indexer page layout (16 groups of 8 entries:
+// [chunk][row][16 B] codes, then 8 scale bytes per row) is itself a K-major
+// operand of 8-row x 16-byte core matrices: K-adjacent core matrices are 128 B
+// apart, 8-row groups 576 B apart.
+//
 // One kernel serves both uses:
-//   * Full scan: a tile is one 128-entry page of the indexer plane; the
-//     epilogue reduces scores to the maximum over 8-position blocks. All n_q
-//     query tokens of a sequence share the tile: N = 32 * n_q MMA columns.
+//   * Full scan: a tile is one 128-entry page; the epilogue reduces scores to
+//     the maximum over 8-position blocks. All n_q query tokens of a sequence
+//     share the tile: N = 32 * n_q MMA columns.
 //   * Pool rescore (Reindex, and the end of Full): a tile is 16 pool blocks of
 //     8 positions, gathered block by block; the epilogue writes every score.
 //
 // Per CTA: warp 4 streams tiles into a ring of shared-memory stages with bulk
-// copies; warps 0-3 dequantise a stage to an f16 128 x 128 operand (exact:
-// E2M1 x E4M3 fits f16) in the 128-byte-swizzled K-major layout and run the
-// epilogue of the previous tile; warp 5 issues tcgen05.mma (M = 128
-// positions, N = 32 * n_q, K = 128) into a double-buffered TMEM accumulator.
+// copies; warps 0-3 move each row's 8 scale bytes into TMEM and run the
+// epilogue of the previous tile; warp 5 issues the two K = 64 MMAs of a tile
+// (M = 128 positions) straight from the stage.
 #include <algorithm>
 
-#include "formats.cuh"
 #include "kernels.h"
 #include "sm103.cuh"
 
 namespace csa2 {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kTileBytes = 16 * 576;     // one indexer page / 16 pool blocks
-constexpr int kABytes = 128 * 128 * 2;   // f16 operand tile
 constexpr int kThreads = 192;
 constexpr int kIdxPageBytes = 16 * 576;
 
@@ -49,58 +54,47 @@ struct ScanParams {
   int tiles_per_cta;
 };
 
-__host__ __device__ constexpr uint32_t tmem_cols_for(int n_cols) {
-  uint32_t c = 32;
-  while (c < static_cast<uint32_t>(2 * n_cols)) c <<= 1;
-  return c;
+// TMEM columns: accumulators (two buffers when N <= 128), then, 32-aligned,
+// two buffers of 8 scale columns for A (4 per K step) and 16 scale columns for
+// B (8 per K step, n_q of them used).
+struct TmemPlan {
+  uint32_t nacc, sfa, sfb, ncols;
+};
+
+__host__ __device__ constexpr TmemPlan tmem_plan(int n_q) {
+  const uint32_t n = 32u * n_q;
+  const uint32_t nacc = n <= 128 ? 2u : 1u;
+  const uint32_t sf = (nacc * n + 31u) & ~31u;
+  uint32_t cols = 32;
+  while (cols < sf + 32u) cols <<= 1;
+  return TmemPlan{nacc, sf, sf + 16u, cols};
 }
 
 __host__ __device__ constexpr int smem_bytes_for(int n_q) {
-  return 1024 /*align*/ + 2 * kABytes + 32 * n_q * 256 /*q operand*/ + kStages * kTileBytes +
-         2048 /*barriers, flags, head weights*/;
-}
-
-// Dequantises one staged tile (16 groups of 8 entries in the indexer-page
-// layout) into the swizzled f16 operand; thread t handles row t.
-__device__ __forceinline__ void dequant_tile(const uint8_t* stage, uint8_t* a, int t) {
-  const uint8_t* grp = stage + (t >> 3) * 576;
-  const int row = t & 7;
-  const uint2 sc = *reinterpret_cast<const uint2*>(grp + 512 + row * 8);
-  const uint64_t sc8 = (static_cast<uint64_t>(sc.y) << 32) | sc.x;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint4 codes = *reinterpret_cast<const uint4*>(grp + c * 128 + row * 16);
-    uint4 out[4];
-    dequant32_f16(codes, static_cast<uint16_t>((sc8 >> (16 * c)) & 0xFFFFu), out);
-    uint8_t* kb = a + (c >> 1) * 16384;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      *reinterpret_cast<uint4*>(kb + sw128_offset(t, (c & 1) * 4 + j)) = out[j];
-  }
+  return 1024 /*align*/ + kStages * kTileBytes + 32 * n_q * 64 /*q operand*/ + 2048 /*barriers, w*/;
 }
 
 template <bool kPool>
-__global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const ScanParams P) {
+__global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int n_q = kPool ? 1 : P.n_q;
   const int n_cols = 32 * n_q;
-  uint8_t* abuf = smem;                                  // 2 x 32 KB
-  uint8_t* qbuf = smem + 2 * kABytes;                    // n_cols x 256 B
-  uint8_t* stages = qbuf + n_cols * 256;                 // kStages x 9216 B
-  uint8_t* misc = stages + kStages * kTileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);    // 16 barriers
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 128);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 132);
-  uint32_t* stage_mask = reinterpret_cast<uint32_t*>(misc + 136);  // kStages words
+  const TmemPlan plan = tmem_plan(n_q);
+  uint8_t* stages = smem;                                   // kStages x 9216 B
+  uint8_t* qbuf = stages + kStages * kTileBytes;            // n_cols x 64 B, core-matrix order
+  uint8_t* misc = qbuf + n_cols * 64;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);       // 20 barriers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 196);
+  uint32_t* stage_mask = reinterpret_cast<uint32_t*>(misc + 200);  // kStages words
   float* wsm = reinterpret_cast<float*>(misc + 256);                 // n_cols floats
 
-  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[4]);
-  const uint32_t afull0 = smem_u32(&bars[8]), aempty0 = smem_u32(&bars[10]);
-  const uint32_t dfull0 = smem_u32(&bars[12]), dempty0 = smem_u32(&bars[14]);
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[kStages]);
+  const uint32_t sfull0 = smem_u32(&bars[2 * kStages]);
+  const uint32_t dfull0 = smem_u32(&bars[2 * kStages + 2]), dempty0 = smem_u32(&bars[2 * kStages + 4]);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Work of this CTA.
   int b, jq = 0;  // sequence, query token (pool mode)
   int64_t first_tile, n_tiles, tile_stride;
   if (kPool) {
@@ -127,33 +121,27 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const ScanParams P
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, 128);
+      mbar_init(empty0 + 8 * i, 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(afull0 + 8 * i, 128);
-      mbar_init(aempty0 + 8 * i, 1);
+      mbar_init(sfull0 + 8 * i, 128);
       mbar_init(dfull0 + 8 * i, 1);
       mbar_init(dempty0 + 8 * i, 128);
     }
     *abort_flag = 0;
     mbar_init_fence();
   }
-  const uint32_t ncols = tmem_cols_for(n_cols);
-  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), ncols);
+  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), plan.ncols);
 
-  // Query operand: qhat of the CTA's query tokens, f16 [n_cols rows x 128].
+  // Query operand: packed E2M1 codes of the CTA's query tokens, rows
+  // n = token * 32 + head, in core-matrix order [n / 8][chunk][n % 8][16 B].
   if (tid < 128) {
     for (int task = tid; task < n_cols * 4; task += 128) {
       const int n = task >> 2, c = task & 3;
       const int jj = kPool ? jq : n >> 5, h = n & 31;
       const int64_t qrow = (static_cast<int64_t>(b) * P.n_q + jj) * 32 + h;
       const uint4 codes = *reinterpret_cast<const uint4*>(P.q_codes + qrow * 64 + c * 16);
-      const uint16_t s2 = *reinterpret_cast<const uint16_t*>(P.q_scales + qrow * 8 + 2 * c);
-      uint4 out[4];
-      dequant32_f16(codes, s2, out);
-      uint8_t* kb = qbuf + (c >> 1) * (n_cols * 128);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(kb + sw128_offset(n, (c & 1) * 4 + j)) = out[j];
+      *reinterpret_cast<uint4*>(qbuf + ((n >> 3) * 4 + c) * 128 + (n & 7) * 16) = codes;
     }
     for (int i = tid; i < n_cols; i += 128) {
       const int jj = kPool ? jq : i >> 5;
@@ -165,6 +153,28 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const ScanParams P
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // Query scales: column n of B has its scales in lane n % 32 of column
+  // sfb + 8 * step + n / 32, replicated in all four 32-lane quarters (each
+  // quarter of the M = 128 datapath reads B's scales from its own lanes), so
+  // warps 0-3 each write their quarter. Every scale-factor address handed to
+  // the MMA is 4-column aligned.
+  if (warp < 4) {
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    for (int jj = 0; jj < n_q; ++jj) {
+      const int jt = kPool ? jq : jj;
+      const int64_t qrow = (static_cast<int64_t>(b) * P.n_q + jt) * 32 + lane;
+      const uint8_t* sp = P.q_scales + qrow * 8;  // only 2-byte alignment is promised
+      const uint32_t lo = sp[0] | (sp[1] << 8) | (sp[2] << 16) | (static_cast<uint32_t>(sp[3]) << 24);
+      const uint32_t hi = sp[4] | (sp[5] << 8) | (sp[6] << 16) | (static_cast<uint32_t>(sp[7]) << 24);
+      tmem_st1(tmem + lane_base + plan.sfb + jj, lo);
+      tmem_st1(tmem + lane_base + plan.sfb + 8 + jj, hi);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp == 4) {
     // ---- producer ----
@@ -227,52 +237,64 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const ScanParams P
   } else if (warp == 5) {
     // ---- MMA issuer ----
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(128, n_cols, false, false);
+      const uint32_t idesc = idesc_mxf4nvf4(128, n_cols);
+      const uint32_t qb = smem_u32(qbuf);
       int64_t issued = 0;
       for (int64_t i = 0; i < n_tiles; ++i) {
+        const int s = static_cast<int>(i % kStages);
         const int a = static_cast<int>(i & 1);
-        const int64_t ua = i >> 1;
-        if (!mbar_wait(afull0 + 8 * a, ua & 1, 211, abort_flag)) { *abort_flag = 1; break; }
-        if (ua > 0 && !mbar_wait(dempty0 + 8 * a, (ua - 1) & 1, 212, abort_flag)) { *abort_flag = 1; break; }
+        const int acc = static_cast<int>(i % plan.nacc);
+        const int64_t ub = i / plan.nacc;
+        if (!mbar_wait(full0 + 8 * s, (i / kStages) & 1, 210, abort_flag)) { *abort_flag = 1; break; }
+        if (!mbar_wait(sfull0 + 8 * a, (i >> 1) & 1, 211, abort_flag)) { *abort_flag = 1; break; }
+        if (ub > 0 && !mbar_wait(dempty0 + 8 * acc, (ub - 1) & 1, 212, abort_flag)) { *abort_flag = 1; break; }
         if (*abort_flag) break;
         tc_fence_after();
-        const uint32_t a_base = smem_u32(abuf + a * kABytes);
-        const uint32_t b_base = smem_u32(qbuf);
+        const uint32_t st = smem_u32(stages + s * kTileBytes);
+        const uint32_t sfa = tmem + plan.sfa + 8 * a;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = sdesc(a_base + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = sdesc(b_base + (k >> 2) * (n_cols * 128) + (k & 3) * 32, 16, 1024, kSwizzle128B);
-          umma_f16(tmem + a * n_cols, ad, bd, idesc, k > 0 ? 1u : 0u);
+        for (int k = 0; k < 2; ++k) {
+          const uint64_t ad = sdesc(st + k * 256, 128, 576, 0);
+          const uint64_t bd = sdesc(qb + k * 256, 128, 512, 0);
+          umma_mxf4nvf4(tmem + acc * n_cols, ad, bd, idesc, sfa + 4 * k, tmem + plan.sfb + k * 8,
+                        k > 0 ? 1u : 0u);
         }
-        umma_commit(aempty0 + 8 * a);
-        umma_commit(dfull0 + 8 * a);
+        umma_commit(empty0 + 8 * s);
+        umma_commit(dfull0 + 8 * acc);
         issued = i + 1;
       }
       // Before TMEM is released, the last MMAs must have finished (they have on
       // the normal path: the epilogue waited for them).
-      if (issued > 0) mbar_wait(dfull0 + 8 * ((issued - 1) & 1), ((issued - 1) >> 1) & 1, 213);
+      if (issued > 0)
+        mbar_wait(dfull0 + 8 * ((issued - 1) % plan.nacc), ((issued - 1) / plan.nacc) & 1, 213);
     }
   } else {
-    // ---- dequant + epilogue (warps 0-3, thread t <-> row t) ----
-    uint32_t valid_rows[2] = {0, 0};  // bit set per 8-row group of the tile in flight
+    // ---- scales to TMEM + epilogue (warps 0-3, thread t <-> row t) ----
+    uint32_t valid_rows[2] = {0, 0};  // per 8-row group, tiles i and i-1
     auto epilogue = [&](int64_t i) -> bool {
-      const int a = static_cast<int>(i & 1);
-      const int64_t ua = i >> 1;
-      if (!mbar_wait(dfull0 + 8 * a, ua & 1, 221, abort_flag)) return false;
+      const int acc = static_cast<int>(i % plan.nacc);
+      if (!mbar_wait(dfull0 + 8 * acc, (i / plan.nacc) & 1, 221, abort_flag)) return false;
       tc_fence_after();
       const int64_t tile = first_tile + i * tile_stride;
-      const bool row_ok = (valid_rows[a] >> (tid >> 3)) & 1u;
+      const bool row_ok = (valid_rows[i & 1] >> (tid >> 3)) & 1u;
       for (int jj = 0; jj < n_q; ++jj) {
         uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + a * n_cols + jj * 32, r);
+        tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * n_cols + jj * 32, r);
         tmem_wait_ld();
         if (jj == n_q - 1) {
           tc_fence_before();
-          mbar_arrive(dempty0 + 8 * a);
+          mbar_arrive(dempty0 + 8 * acc);
         }
-        float s = 0.f;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        const float* wj = wsm + jj * 32;
 #pragma unroll
-        for (int h = 0; h < 32; ++h) s = fmaf(wsm[jj * 32 + h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+        for (int h = 0; h < 32; h += 4) {
+          s0 = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.f), s0);
+          s1 = fmaf(wj[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
+          s2 = fmaf(wj[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
+          s3 = fmaf(wj[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
+        }
+        const float s = (s0 + s1) + (s2 + s3);
         if (!kPool) {
           const int64_t t_q = seq_n - P.n_q + jj;
           const int64_t p = tile * 128 + tid;
@@ -293,19 +315,21 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const ScanParams P
       return true;
     };
     bool ok = true;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     for (int64_t i = 0; i < n_tiles && ok; ++i) {
       const int s = static_cast<int>(i % kStages);
-      const int64_t u = i / kStages;
       const int a = static_cast<int>(i & 1);
-      const int64_t ua = i >> 1;
-      if (!mbar_wait(full0 + 8 * s, u & 1, 231, abort_flag)) { ok = false; break; }
-      if (ua > 0 && !mbar_wait(aempty0 + 8 * a, (ua - 1) & 1, 232, abort_flag)) { ok = false; break; }
-      const uint32_t mask = stage_mask[s];
-      valid_rows[a] = mask;
-      if ((mask >> (tid >> 3)) & 1u) dequant_tile(stages + s * kTileBytes, abuf + a * kABytes, tid);
-      fence_proxy_async();
-      mbar_arrive(empty0 + 8 * s);
-      mbar_arrive(afull0 + 8 * a);
+      if (!mbar_wait(full0 + 8 * s, (i / kStages) & 1, 231, abort_flag)) { ok = false; break; }
+      valid_rows[a] = stage_mask[s];
+      // Row t's 8 scale bytes: blocks 0-3 feed the first K = 64 step, 4-7 the second.
+      const uint8_t* grp = stages + s * kTileBytes + (tid >> 3) * 576;
+      const uint2 sc = *reinterpret_cast<const uint2*>(grp + 512 + (tid & 7) * 8);
+      const uint32_t sfa = tmem + lane_base + plan.sfa + 8 * a;
+      tmem_st1(sfa + warp, sc.x);
+      tmem_st1(sfa + 4 + warp, sc.y);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(sfull0 + 8 * a);
       if (i > 0) ok = epilogue(i - 1);
     }
     if (ok && n_tiles > 0) ok = epilogue(n_tiles - 1);
@@ -316,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const ScanParams P
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, ncols);
+    tmem_dealloc(tmem, plan.ncols);
   }
 }
 
@@ -347,6 +371,13 @@ int num_sms() {
     sms[dev] = v > 0 ? v : 148;
   }
   return sms[dev];
+}
+
+// Resident CTAs per SM, bounded by shared memory and TMEM columns.
+int ctas_per_sm(int n_q) {
+  const int by_smem = (228 * 1024) / (smem_bytes_for(n_q) + 1024);
+  const int by_tmem = 512 / static_cast<int>(tmem_plan(n_q).ncols);
+  return std::max(1, std::min(by_smem, by_tmem));
 }
 
 }  // namespace
@@ -385,7 +416,7 @@ cudaError_t launch_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales,
   p.block_max = block_max;
   p.max_blocks = max_blocks;
   const int64_t pages = (max_ctx + 127) / 128;
-  const int64_t target = 2LL * num_sms();
+  const int64_t target = static_cast<int64_t>(ctas_per_sm(n_q)) * num_sms();
   const int64_t per_seq = std::max<int64_t>(1, std::min<int64_t>(pages, (target + B - 1) / B));
   return launch<false>(p, dim3(static_cast<unsigned>(per_seq), B), n_q, stream);
 }
@@ -410,7 +441,7 @@ cudaError_t launch_pool_scores(const uint8_t* q_codes, const uint8_t* q_scales, 
   p.idx_pages = idx_pages;
   p.pool = pool;
   p.scores = scores;
-  const int64_t target = 2LL * num_sms();
+  const int64_t target = static_cast<int64_t>(ctas_per_sm(1)) * num_sms();
   int splits = static_cast<int>(std::min<int64_t>(128, std::max<int64_t>(1, (target + Q - 1) / Q)));
   const int per = (128 + splits - 1) / splits;
   splits = (128 + per - 1) / per;

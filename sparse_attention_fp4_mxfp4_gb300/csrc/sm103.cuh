@@ -162,6 +162,40 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Instruction descriptor of kind::mxf4nvf4 (E2M1 A and B, one UE4M3 scale per
+// 16 elements, f32 accumulator): [7,10) A format (1 = E2M1), [10,13) B format,
+// bits 15/16 = 0 (both K-major), [17,23) N >> 3, bit 23 = 0 (UE4M3 scales),
+// [24,29) M >> 4, scale-factor ids 0. K = 64 per instruction.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= (A x SFA)[smem] * (B x SFB)[smem]^T with 16-element block scales
+// read from TMEM. Scale layout in TMEM (M = 128): the 4 scales of row r for this
+// K = 64 step are the 4 bytes (block j in byte j) of lane r, column
+// sfa + r / 32; those of B column n are in lane 32 * q + n % 32, column
+// sfb + n / 32, for every lane quarter q (each quarter reads its own copy).
+__device__ __forceinline__ void umma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Registers -> TMEM: one 32-bit column for the warp's 32 lanes.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Arrives once on the mbarrier when every MMA issued so far by this thread has
 // completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
