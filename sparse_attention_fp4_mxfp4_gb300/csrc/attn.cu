@@ -80,6 +80,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const AttnParam
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 512);
 
+  // Issue this thread's 16 Q loads first: they do not depend on anything and
+  // overlap with the key-slot lookups below.
+  const uint4* qg = reinterpret_cast<const uint4*>(P.q + static_cast<int64_t>(q) * 64 * 512);
+  uint4 qv[16];
+#pragma unroll
+  for (int it = 0; it < 16; ++it) qv[it] = qg[tid + it * kThreads];
+
   // ---- key slots of this split ----
   if (tid < 128) {
     int64_t off = -1;
@@ -112,65 +119,76 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const AttnParam
     key_off[tid] = off;
   }
 
-  // ---- Q (bf16 -> f16) into the swizzled B operand ----
-  {
-    const uint4* qg = reinterpret_cast<const uint4*>(P.q + static_cast<int64_t>(q) * 64 * 512);
-    for (int i = tid; i < 64 * 64; i += kThreads) {
-      const int h = i >> 6, c = i & 63;
-      const uint4 u = qg[i];
-      float f[8];
-      bf16x8_to_f32(u, f);
-      uint32_t o[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        __half2 hv = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
-        o[k] = *reinterpret_cast<uint32_t*>(&hv);
-      }
-      *reinterpret_cast<uint4*>(Qs + (c >> 3) * 8192 + sw128_offset(h, c & 7)) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
-  __syncthreads();
+  __syncthreads();  // key slots are known
 
   // ---- gather + dequantise keys into the swizzled A operand ----
+  // All of a thread's key loads are issued before any is used. A missing key
+  // becomes zero codes with a zero scale, which dequantises to zeros.
   if (split < 4) {
-    for (int i = tid; i < 128 * 16; i += kThreads) {
+    uint4 cv[8];
+    uint32_t sv[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int i = tid + it * kThreads;
       const int r = i >> 4, c = i & 15;  // key row, 32-channel chunk
       const int64_t off = key_off[r];
-      uint4 out[4];
+      cv[it] = make_uint4(0, 0, 0, 0);
+      sv[it] = 0;
       if (off >= 0) {
         const uint8_t* e = P.main_pages + off;
-        const uint4 codes = *reinterpret_cast<const uint4*>(e + c * 16);
-        const uint16_t s2 = *reinterpret_cast<const uint16_t*>(e + 256 + 2 * c);
-        dequant32_f16(codes, s2, out);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) out[k] = make_uint4(0, 0, 0, 0);
+        cv[it] = *reinterpret_cast<const uint4*>(e + c * 16);
+        sv[it] = *reinterpret_cast<const uint16_t*>(e + 256 + 2 * c);
       }
+    }
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int i = tid + it * kThreads;
+      const int r = i >> 4, c = i & 15;
+      uint4 out[4];
+      dequant32_f16(cv[it], static_cast<uint16_t>(sv[it]), out);
       uint8_t* kb = Kt + (c >> 1) * 16384;
 #pragma unroll
       for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(kb + sw128_offset(r, (c & 1) * 4 + k)) = out[k];
     }
   } else {
-    for (int i = tid; i < 128 * 32; i += kThreads) {
+    uint4 rv[16];
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {
+      const int i = tid + it * kThreads;
       const int r = i >> 5, c = i & 31;  // key row, 16-channel chunk
       const int64_t off = key_off[r];
-      uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
-      if (off >= 0) {
-        const uint4 v = *reinterpret_cast<const uint4*>(P.rings + off + c * 16);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t h[8];
+      rv[it] = off >= 0 ? *reinterpret_cast<const uint4*>(P.rings + off + c * 16) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          h[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xFFFFu));
-          h[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
-        }
-        o0 = make_uint4(h[0], h[1], h[2], h[3]);
-        o1 = make_uint4(h[4], h[5], h[6], h[7]);
+    for (int it = 0; it < 16; ++it) {
+      const int i = tid + it * kThreads;
+      const int r = i >> 5, c = i & 31;
+      const uint32_t w[4] = {rv[it].x, rv[it].y, rv[it].z, rv[it].w};
+      uint32_t h[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        h[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xFFFFu));
+        h[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
       }
       uint8_t* kb = Kt + (c >> 2) * 16384;
-      *reinterpret_cast<uint4*>(kb + sw128_offset(r, (c & 3) * 2)) = o0;
-      *reinterpret_cast<uint4*>(kb + sw128_offset(r, (c & 3) * 2 + 1)) = o1;
+      *reinterpret_cast<uint4*>(kb + sw128_offset(r, (c & 3) * 2)) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(kb + sw128_offset(r, (c & 3) * 2 + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
     }
+  }
+  // ---- Q (bf16 -> f16) into the swizzled B operand ----
+#pragma unroll
+  for (int it = 0; it < 16; ++it) {
+    const int i = tid + it * kThreads;
+    const int h = i >> 6, c = i & 63;
+    float f[8];
+    bf16x8_to_f32(qv[it], f);
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __half2 hv = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
+      o[k] = *reinterpret_cast<uint32_t*>(&hv);
+    }
+    *reinterpret_cast<uint4*>(Qs + (c >> 3) * 8192 + sw128_offset(h, c & 7)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
   fence_proxy_async();
   tc_fence_before();

@@ -177,61 +177,61 @@ __global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P
   tc_fence_after();
 
   if (warp == 4) {
-    // ---- producer ----
-    if (lane == 0) {
-      for (int64_t i = 0; i < n_tiles; ++i) {
-        const int s = static_cast<int>(i % kStages);
-        const int64_t u = i / kStages;
-        if (u > 0 && !mbar_wait(empty0 + 8 * s, (u - 1) & 1, 201, abort_flag)) { *abort_flag = 1; break; }
-        if (*abort_flag) break;
-        const int64_t tile = first_tile + i * tile_stride;
-        const uint32_t dst = smem_u32(stages + s * kTileBytes);
-        if (!kPool) {
-          const int32_t page = (tile < P.max_pages)
-                                   ? P.block_table[static_cast<int64_t>(b) * P.max_pages + tile]
-                                   : -1;
+    // ---- producer (whole warp: lookups in parallel, one bulk copy per lane) ----
+    const int64_t t_q = seq_n - P.n_q + jq;
+    int32_t next_pages = -1;  // scan: page id of tile (i & ~31) + lane
+    for (int64_t i = 0; i < n_tiles; ++i) {
+      const int s = static_cast<int>(i % kStages);
+      const int64_t u = i / kStages;
+      int go = 1;
+      if (lane == 0) {
+        if (u > 0 && !mbar_wait(empty0 + 8 * s, (u - 1) & 1, 201, abort_flag)) *abort_flag = 1;
+        go = *abort_flag ? 0 : 1;
+      }
+      if (!__shfl_sync(0xffffffffu, go, 0)) break;
+      const int64_t tile = first_tile + i * tile_stride;
+      const uint32_t dst = smem_u32(stages + s * kTileBytes);
+      if (!kPool) {
+        if ((i & 31) == 0) {  // page ids of the next 32 tiles, one per lane
+          const int64_t tl = first_tile + (i + lane) * tile_stride;
+          next_pages = (i + lane < n_tiles && tl < P.max_pages)
+                           ? P.block_table[static_cast<int64_t>(b) * P.max_pages + tl] : -1;
+        }
+        const int32_t page = __shfl_sync(0xffffffffu, next_pages, static_cast<int>(i & 31));
+        if (lane == 0) {
           if (page < 0 || page >= P.n_pages) {
             report(CSA2_ERR_DEVICE_BOUNDS, 202);
             stage_mask[s] = 0;
             mbar_arrive(full0 + 8 * s);
-            continue;
-          }
-          stage_mask[s] = 0xFFFFu;
-          mbar_arrive_expect_tx(full0 + 8 * s, kTileBytes);
-          bulk_g2s(dst, P.idx_pages + static_cast<int64_t>(page) * kIdxPageBytes, kTileBytes, full0 + 8 * s);
-        } else {
-          const int64_t t_q = seq_n - P.n_q + jq;
-          const int32_t* prow = P.pool + (static_cast<int64_t>(b) * P.n_q + jq) * 2048 + tile * 16;
-          uint32_t mask = 0, nvalid = 0;
-          int32_t pages[16];
-          for (int g = 0; g < 16; ++g) {
-            const int32_t blk = prow[g];
-            pages[g] = -1;
-            if (blk < 0 || static_cast<int64_t>(blk) * 8 > t_q) continue;
-            const int64_t lp = static_cast<int64_t>(blk) >> 4;
-            const int32_t page = lp < P.max_pages ? P.block_table[static_cast<int64_t>(b) * P.max_pages + lp] : -1;
-            if (page < 0 || page >= P.n_pages) {
-              report(CSA2_ERR_DEVICE_BOUNDS, 203);
-              continue;
-            }
-            pages[g] = page;
-            mask |= 1u << g;
-            ++nvalid;
-          }
-          stage_mask[s] = mask;
-          if (nvalid == 0) {
-            mbar_arrive(full0 + 8 * s);
-            continue;
-          }
-          mbar_arrive_expect_tx(full0 + 8 * s, nvalid * 576);
-          for (int g = 0; g < 16; ++g) {
-            if (pages[g] < 0) continue;
-            const int32_t blk = prow[g];
-            bulk_g2s(dst + g * 576,
-                     P.idx_pages + static_cast<int64_t>(pages[g]) * kIdxPageBytes + (blk & 15) * 576,
-                     576, full0 + 8 * s);
+          } else {
+            stage_mask[s] = 0xFFFFu;
+            mbar_arrive_expect_tx(full0 + 8 * s, kTileBytes);
+            bulk_g2s(dst, P.idx_pages + static_cast<int64_t>(page) * kIdxPageBytes, kTileBytes, full0 + 8 * s);
           }
         }
+      } else {
+        // Lane g < 16 resolves pool slot g of this tile.
+        int32_t blk = -1, page = -1;
+        bool valid = false;
+        if (lane < 16) {
+          blk = P.pool[(static_cast<int64_t>(b) * P.n_q + jq) * 2048 + tile * 16 + lane];
+          if (blk >= 0 && static_cast<int64_t>(blk) * 8 <= t_q) {
+            const int64_t lp = static_cast<int64_t>(blk) >> 4;
+            page = lp < P.max_pages ? P.block_table[static_cast<int64_t>(b) * P.max_pages + lp] : -1;
+            if (page < 0 || page >= P.n_pages) report(CSA2_ERR_DEVICE_BOUNDS, 203);
+            else valid = true;
+          }
+        }
+        const uint32_t mask = __ballot_sync(0xffffffffu, valid) & 0xFFFFu;
+        if (lane == 0) {
+          stage_mask[s] = mask;
+          if (mask == 0) mbar_arrive(full0 + 8 * s);
+          else mbar_arrive_expect_tx(full0 + 8 * s, __popc(mask) * 576u);
+        }
+        __syncwarp();
+        if (valid)
+          bulk_g2s(dst + lane * 576, P.idx_pages + static_cast<int64_t>(page) * kIdxPageBytes + (blk & 15) * 576,
+                   576, full0 + 8 * s);
       }
     }
   } else if (warp == 5) {

@@ -54,6 +54,15 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_s
   return base + x - v;
 }
 
+// Adds 1 to hist[bin] for every lane with take == true; lanes of a warp that
+// hit the same bin are combined first (scores cluster in a few bins of the
+// first digit, so per-element shared atomics would serialise).
+__device__ __forceinline__ void warp_hist_add(uint32_t* hist, bool take, uint32_t bin) {
+  const uint32_t key = take ? bin : 0xFFFFFFFFu;
+  const uint32_t peers = __match_any_sync(0xffffffffu, key);
+  if (take && (threadIdx.x & 31) == static_cast<uint32_t>(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
+}
+
 // Row of n keys, pick k. `map` turns an element index into the output value.
 // mode 0: block top-k (value = block id); mode 1: pool top-k (value = position
 // pool[i / 8] * 8 + i % 8).
@@ -98,9 +107,10 @@ __global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __res
     const uint32_t nb = 1u << widths[pass];
     for (uint32_t i = tid; i < 2048; i += kThreads) hist[i] = 0;
     __syncthreads();
-    for (int64_t i = tid; i < n; i += kThreads) {
-      const uint32_t u = ordered_key(row[i]);
-      if (u != 0u && (u & mask) == prefix) atomicAdd(&hist[(u >> sh) & (nb - 1)], 1u);
+    const int64_t n_round = (n + kThreads - 1) / kThreads * kThreads;  // whole warps iterate together
+    for (int64_t i = tid; i < n_round; i += kThreads) {
+      const uint32_t u = i < n ? ordered_key(row[i]) : 0u;
+      warp_hist_add(hist, u != 0u && (u & mask) == prefix, (u >> sh) & (nb - 1));
     }
     __syncthreads();
     // Counts from the top: thread t owns bins [2t, 2t+1] in descending order.
@@ -237,6 +247,7 @@ __global__ void __launch_bounds__(kThreads) cluster_topk_kernel(const float* __r
   const int64_t hi = min(n, lo + chunk);
   const int m = hi > lo ? static_cast<int>(hi - lo) : 0;
   const float* row = keys + static_cast<int64_t>(q) * row_stride + lo;
+#pragma unroll 4
   for (int i = tid; i < m; i += kThreads) key[i] = ordered_key(row[i]);
   __syncthreads();
 
@@ -249,9 +260,10 @@ __global__ void __launch_bounds__(kThreads) cluster_topk_kernel(const float* __r
     const uint32_t nb = 1u << widths[pass];
     for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < m; i += kThreads) {
-      const uint32_t u = key[i];
-      if (u != 0u && (u & mask) == prefix) atomicAdd(&hist[(u >> sh) & (nb - 1)], 1u);
+    const int m_round = (m + kThreads - 1) / kThreads * kThreads;  // whole warps iterate together
+    for (int i = tid; i < m_round; i += kThreads) {
+      const uint32_t u = i < m ? key[i] : 0u;
+      warp_hist_add(hist, u != 0u && (u & mask) == prefix, (u >> sh) & (nb - 1));
     }
     cluster_sync_all();  // every local histogram is complete
     for (int i = tid; i < 2048; i += kThreads) {
@@ -413,7 +425,8 @@ cudaError_t launch_pool_topk(const float* scores, const int64_t* seq_len, int B,
                              const int32_t* pool, int32_t* topk, cudaStream_t stream) {
   const int Q = B * n_q;
   if (Q == 0) return cudaSuccess;
-  return launch_cluster_topk<1>(scores, 16384, seq_len, Q, n_q, 512, 1, pool, topk, stream);
+  // 16384 scores per token, 2048 per CTA of an 8-CTA cluster.
+  return launch_cluster_topk<1>(scores, 16384, seq_len, Q, n_q, 512, 8, pool, topk, stream);
 }
 
 }  // namespace csa2
