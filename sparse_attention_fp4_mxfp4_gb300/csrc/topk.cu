@@ -187,13 +187,20 @@ __global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __res
 // ---- cluster version: the row lives in shared memory ------------------------
 //
 // A cluster of C CTAs (C <= 16) selects from one row; CTA r keeps elements
-// [r * chunk, (r + 1) * chunk) of the row in its shared memory as ordered keys,
-// so the row is read from global memory once. Each radix pass builds a local
-// histogram; every CTA then sums all C histograms through distributed shared
-// memory and derives the same threshold digit. The ordered compaction uses
-// the per-CTA counts exchanged the same way. Control flow is uniform across
-// the cluster: every CTA executes every cluster barrier.
+// [r * chunk, (r + 1) * chunk) of the row in shared memory as ordered keys, so
+// the row is read from global memory once. Keys are offset by the
+// cluster-wide minimum and cut into 12-bit digits from the top of the actual
+// span, so usual score ranges resolve in two passes and spread over many bins.
+// Each pass builds a local histogram; every CTA sums all C histograms through
+// distributed shared memory (all remote loads of a thread in flight at once)
+// and derives the same threshold digit. The ordered compaction is warp
+// cooperative: consecutive lanes take consecutive elements, warps take
+// consecutive ranges, so index order is kept without bank conflicts. Control
+// flow is uniform across the cluster: every CTA executes every cluster barrier.
 constexpr int kChunk = 16384;  // elements per CTA
+constexpr int kDigit = 12;
+constexpr int kBins = 1 << kDigit;
+constexpr int kMaxC = 16;
 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -213,7 +220,7 @@ __device__ __forceinline__ uint32_t dsmem_ld(const uint32_t* local, uint32_t ran
 }
 
 template <int kMode>
-__global__ void __launch_bounds__(kThreads) cluster_topk_kernel(const float* __restrict__ keys,
+__global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* __restrict__ keys,
                                                                 int64_t row_stride,
                                                                 const int64_t* __restrict__ seq_len,
                                                                 int n_q, int k, int C,
@@ -221,143 +228,296 @@ __global__ void __launch_bounds__(kThreads) cluster_topk_kernel(const float* __r
                                                                 int32_t* __restrict__ out) {
   extern __shared__ uint32_t sm[];
   uint32_t* key = sm;                    // [kChunk] ordered keys of this CTA's slice
-  uint32_t* hist = sm + kChunk;          // [2048] local histogram
-  uint32_t* tot = hist + 2048;           // [2048] cluster-wide histogram
-  uint32_t* warp_sums = tot + 2048;      // [32]
-  uint32_t* xchg = warp_sums + 32;       // [4]: gt, eq of this CTA
-  uint32_t* s_sel = xchg + 4;            // [2]
+  uint32_t* hist = sm + kChunk;          // [kBins] local histogram
+  uint32_t* tot = hist + kBins;          // [kBins] cluster-wide histogram
+  uint32_t* warp_sums = tot + kBins;     // [32]
+  uint32_t* wsel = warp_sums + 32;       // [32] per-warp selection offsets
+  uint32_t* weq = wsel + 32;             // [32] per-warp equal-key takes
+  uint32_t* xchg = weq + 32;             // [8] values read by other CTAs (0-2 min/max/valid,
+                                         // 3 slice total, 6-7 gt/eq counts)
+  uint32_t* bc = xchg + 8;               // [8] block-wide broadcasts
+  int32_t* pool_sm = reinterpret_cast<int32_t*>(bc + 8);  // [2048] pool row (pool mode)
 
   const uint32_t r = cluster_rank();
   const int q = blockIdx.y;
   const int b = q / n_q, j = q % n_q;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int64_t n;
   if (kMode == 0) {
     const int64_t t = seq_len[b] - n_q + j;
     n = t >= 0 ? (t + 8) / 8 : 0;
-    if (n > row_stride || n > static_cast<int64_t>(C) * kChunk) {
-      if (tid == 0 && r == 0) report(CSA2_ERR_DEVICE_BOUNDS, 311);
-      n = min(row_stride, static_cast<int64_t>(C) * kChunk);
-    }
   } else {
     n = row_stride;
+  }
+  if (n > row_stride || n > static_cast<int64_t>(C) * kChunk) {
+    if (tid == 0 && r == 0) report(CSA2_ERR_DEVICE_BOUNDS, 311);
+    n = min(row_stride, static_cast<int64_t>(C) * kChunk);
   }
   const int64_t chunk = (n + C - 1) / C;
   const int64_t lo = static_cast<int64_t>(r) * chunk;
   const int64_t hi = min(n, lo + chunk);
   const int m = hi > lo ? static_cast<int>(hi - lo) : 0;
   const float* row = keys + static_cast<int64_t>(q) * row_stride + lo;
-#pragma unroll 4
-  for (int i = tid; i < m; i += kThreads) key[i] = ordered_key(row[i]);
-  __syncthreads();
 
-  uint32_t prefix = 0, mask = 0, remaining = static_cast<uint32_t>(k);
-  bool all_valid = false;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int sh = shifts[pass];
-    const uint32_t nb = 1u << widths[pass];
-    for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    const int m_round = (m + kThreads - 1) / kThreads * kThreads;  // whole warps iterate together
-    for (int i = tid; i < m_round; i += kThreads) {
-      const uint32_t u = i < m ? key[i] : 0u;
-      warp_hist_add(hist, u != 0u && (u & mask) == prefix, (u >> sh) & (nb - 1));
+  if (tid == 0) {
+    xchg[0] = 0xFFFFFFFFu;
+    xchg[1] = 0u;
+  }
+  __syncthreads();
+  uint32_t vmin = 0xFFFFFFFFu, vmax = 0u, nvalid = 0;
+  constexpr int kLoads = kChunk / kThreads;  // every load of a thread in flight at once
+  float f[kLoads];
+#pragma unroll
+  for (int it = 0; it < kLoads; ++it) {
+    const int i = tid + it * kThreads;
+    f[it] = i < m ? row[i] : -INFINITY;
+  }
+#pragma unroll
+  for (int it = 0; it < kLoads; ++it) {
+    const int i = tid + it * kThreads;
+    const uint32_t u = ordered_key(f[it]);
+    if (i < m) key[i] = u;
+    if (u != 0u) {
+      vmin = min(vmin, u);
+      vmax = max(vmax, u);
+      ++nvalid;
     }
-    cluster_sync_all();  // every local histogram is complete
-    for (int i = tid; i < 2048; i += kThreads) {
-      uint32_t s = 0;
-      for (int c = 0; c < C; ++c) s += dsmem_ld(&hist[i], c);
-      tot[i] = s;
+  }
+  if (kMode == 1) {  // the pool row, for turning slots into positions in the compaction
+    const int32_t* prow_g = pool + static_cast<int64_t>(q) * 2048;
+    for (int i = tid; i < 2048; i += kThreads) pool_sm[i] = prow_g[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    vmin = min(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
+    vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+  }
+  if (lane == 0) {
+    atomicMin(&xchg[0], vmin);
+    atomicMax(&xchg[1], vmax);
+  }
+  uint32_t cta_valid;
+  block_excl_scan(nvalid, warp_sums, &cta_valid);
+  if (tid == 0) xchg[2] = cta_valid;
+  cluster_sync_all();
+  if (warp == 0) {
+    uint32_t mn = 0xFFFFFFFFu, mx = 0u, nv = 0u;
+    if (lane < C) {
+      mn = dsmem_ld(&xchg[0], lane);
+      mx = dsmem_ld(&xchg[1], lane);
+      nv = dsmem_ld(&xchg[2], lane);
     }
-    cluster_sync_all();  // nobody reads a remote histogram any more
-    const uint32_t hi_bin = nb - 1 - 2 * tid, lo_bin = hi_bin - 1;
-    uint32_t c_hi = 0, c_lo = 0;
-    if (2 * static_cast<uint32_t>(tid) < nb) {
-      c_hi = tot[hi_bin];
-      c_lo = tot[lo_bin];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      nv += __shfl_xor_sync(0xffffffffu, nv, o);
     }
-    uint32_t total;
-    const uint32_t before = block_excl_scan(c_hi + c_lo, warp_sums, &total);
-    if (pass == 0 && total <= static_cast<uint32_t>(k)) {
-      all_valid = true;
-      break;
+    if (lane == 0) {
+      bc[0] = mn;
+      bc[1] = mx;
+      bc[2] = nv;
     }
-    if (2 * static_cast<uint32_t>(tid) < nb) {
-      if (before < remaining && before + c_hi >= remaining) {
-        s_sel[0] = hi_bin;
-        s_sel[1] = before;
-      } else if (before + c_hi < remaining && before + c_hi + c_lo >= remaining) {
-        s_sel[0] = lo_bin;
-        s_sel[1] = before + c_hi;
+  }
+  __syncthreads();
+  const uint32_t umin = bc[0], umax = bc[1], total_valid = bc[2];
+
+  // Threshold: take keys > T and the first need_eq keys equal to T.
+  uint32_t T = 0u, need_eq = 0u;
+  if (total_valid > static_cast<uint32_t>(k)) {
+    const uint32_t span = umax - umin;
+    const int bits = span ? 32 - __clz(span) : 0;
+    int shift = bits > kDigit ? bits - kDigit : 0;
+    uint32_t pref = 0u, hmask = 0u, remaining = static_cast<uint32_t>(k);
+    for (int pass = 0; pass < 3; ++pass) {
+      for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < m; i += kThreads) {
+        const uint32_t u = key[i];
+        const uint32_t d = u - umin;
+        if (u != 0u && (d & hmask) == pref) atomicAdd(&hist[(d >> shift) & (kBins - 1)], 1u);
+      }
+      cluster_sync_all();  // every local histogram is complete
+      // CTA r sums the bins of its slice [r * S, (r + 1) * S) over the cluster; a
+      // single CTA uses its own histogram as is.
+      const int S = kBins / C;
+      const uint32_t* totals = hist;
+      if (C > 1) {
+        uint32_t part = 0;
+        for (int bi = tid; bi < S; bi += kThreads) {
+          const int bin = static_cast<int>(r) * S + bi;
+          uint32_t v[kMaxC];
+#pragma unroll
+          for (int c = 0; c < kMaxC; ++c) v[c] = c < C ? dsmem_ld(&hist[bin], c) : 0u;
+          uint32_t sum = 0;
+#pragma unroll
+          for (int c = 0; c < kMaxC; ++c) sum += v[c];
+          tot[bin] = sum;
+          part += sum;
+        }
+        uint32_t slice_total;
+        block_excl_scan(part, warp_sums, &slice_total);
+        if (tid == 0) xchg[3] = slice_total;
+        totals = tot;
+      }
+      cluster_sync_all();  // slice sums complete; nobody reads a remote histogram any more
+      // The slice that holds the remaining-th largest key (slices of higher ranks
+      // hold higher digits), and the keys above it.
+      if (warp == 0) {
+        const uint32_t st = lane < C ? (C > 1 ? dsmem_ld(&xchg[3], lane) : 0u) : 0u;
+        uint32_t incl = st;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+          if (lane + o < 32) incl += y;
+        }
+        const uint32_t above = incl - st;
+        if (lane == 0) {
+          bc[3] = 0;
+          bc[4] = 0;
+        }
+        __syncwarp();
+        if (C > 1 && lane < C && above < remaining && above + st >= remaining) {
+          bc[3] = lane;
+          bc[4] = above;
+        }
+      }
+      __syncthreads();
+      const uint32_t target = bc[3] & static_cast<uint32_t>(C - 1);  // always a rank of this cluster
+      const uint32_t above_t = bc[4];
+      __syncthreads();
+      // Thread t owns kPer consecutive bins of the target slice counted from the top.
+      constexpr int kPer = kBins / kThreads;
+      uint32_t c4[kPer], own = 0;
+#pragma unroll
+      for (int it = 0; it < kPer; ++it) {
+        const int rank = tid * kPer + it;
+        c4[it] = 0;
+        if (rank < S) {
+          const int bin = static_cast<int>(target) * S + (S - 1 - rank);
+          c4[it] = C > 1 ? dsmem_ld(&totals[bin], target) : totals[bin];
+        }
+        own += c4[it];
+      }
+      uint32_t total;
+      uint32_t before = above_t + block_excl_scan(own, warp_sums, &total);
+#pragma unroll
+      for (int it = 0; it < kPer; ++it) {
+        const int rank = tid * kPer + it;
+        if (rank < S && before < remaining && before + c4[it] >= remaining) {
+          bc[5] = static_cast<uint32_t>(static_cast<int>(target) * S + (S - 1 - rank));
+          bc[6] = before;
+        }
+        before += c4[it];
+      }
+      __syncthreads();
+      remaining -= bc[6];
+      pref |= bc[5] << shift;
+      hmask = ~((1u << shift) - 1u);
+      __syncthreads();
+      if (shift == 0) break;
+      shift = shift > kDigit ? shift - kDigit : 0;
+    }
+    T = umin + pref;
+    need_eq = remaining;
+  }
+
+  // Warp-cooperative counts over this CTA's slice: warp w owns [w * wseg, (w + 1) * wseg).
+  const int wseg = ((m + 32 * 32 - 1) / (32 * 32)) * 32;
+  const int w0 = warp * wseg, w1 = min(m, w0 + wseg);
+  uint32_t gt = 0, eq = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t u = i < w1 ? key[i] : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, u > T));
+    eq += __popc(__ballot_sync(0xffffffffu, u == T && u != 0u));
+  }
+  if (lane == 0) {
+    wsel[warp] = gt;
+    weq[warp] = eq;
+  }
+  __syncthreads();
+  if (warp == 0) {  // per-warp prefix sums within the CTA
+    const uint32_t g = wsel[lane], e = weq[lane];
+    uint32_t gi = g, ei = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t yg = __shfl_up_sync(0xffffffffu, gi, o), ye = __shfl_up_sync(0xffffffffu, ei, o);
+      if (lane >= o) {
+        gi += yg;
+        ei += ye;
       }
     }
-    __syncthreads();
-    remaining -= s_sel[1];
-    prefix |= s_sel[0] << sh;
-    mask |= (nb - 1) << sh;
-    __syncthreads();
-  }
-  const uint32_t T = all_valid ? 0u : prefix;
-  const uint32_t need_eq = all_valid ? 0u : remaining;
-
-  // Per-thread contiguous segments of this CTA's slice keep index order.
-  const int seg = (m + kThreads - 1) / kThreads;
-  const int s0 = tid * seg, s1 = min(m, s0 + seg);
-  uint32_t gt = 0, eq = 0;
-  for (int i = s0; i < s1; ++i) {
-    const uint32_t u = key[i];
-    if (u > T) ++gt;
-    else if (u == T && u != 0u) ++eq;
-  }
-  uint32_t cta_eq, cta_gt;
-  const uint32_t eq_base_local = block_excl_scan(eq, warp_sums, &cta_eq);
-  block_excl_scan(gt, warp_sums, &cta_gt);
-  if (tid == 0) {
-    xchg[0] = cta_gt;
-    xchg[1] = cta_eq;
+    wsel[lane] = gi - g;  // gt keys in lower warps
+    weq[lane] = ei - e;   // equal keys in lower warps
+    if (lane == 31) {
+      xchg[6] = gi;
+      xchg[7] = ei;
+    }
   }
   cluster_sync_all();
-  // Ties go to the lowest indices: CTA slices are in index order.
-  uint32_t eq_before = 0, sel_before = 0, total_sel = 0, eq_cta_before = 0;
-  for (uint32_t c = 0; c < static_cast<uint32_t>(C); ++c) {
-    const uint32_t g = dsmem_ld(&xchg[0], c), e = dsmem_ld(&xchg[1], c);
-    const uint32_t take = need_eq > eq_before ? min(e, need_eq - eq_before) : 0u;
-    if (c < r) {
-      sel_before += g + take;
-      eq_cta_before += e;
+  if (warp == 0) {  // ties go to the lowest indices: CTA slices are in index order
+    const uint32_t g = lane < C ? dsmem_ld(&xchg[6], lane) : 0u;
+    const uint32_t e = lane < C ? dsmem_ld(&xchg[7], lane) : 0u;
+    uint32_t e_incl = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, e_incl, o);
+      if (lane >= o) e_incl += y;
     }
-    total_sel += g + take;
-    eq_before += e;
+    const uint32_t e_before = e_incl - e;
+    const uint32_t take = need_eq > e_before ? min(e, need_eq - e_before) : 0u;
+    uint32_t s_incl = g + take;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, s_incl, o);
+      if (lane >= o) s_incl += y;
+    }
+    const uint32_t total_sel = __shfl_sync(0xffffffffu, s_incl, 31);
+    if (lane == static_cast<int>(r)) {
+      bc[5] = s_incl - (g + take);  // selections in lower CTAs
+      bc[6] = e_before;             // equal keys in lower CTAs
+    }
+    if (lane == 0) bc[7] = total_sel;
   }
-  const uint32_t eq_base = eq_cta_before + eq_base_local;
-  const uint32_t take_eq = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
-  uint32_t cta_sel;
-  uint32_t o = sel_before + block_excl_scan(gt + take_eq, warp_sums, &cta_sel);
+  __syncthreads();
+  // This warp's equal keys that are taken: ranks [eq_base, eq_base + eq) among equals.
+  const uint32_t eq_base = bc[6] + weq[warp];
+  const uint32_t take_w = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
+  // Selections before this warp: lower CTAs, then lower warps (gt + their takes).
+  // Equal keys taken by lower warps of this CTA: min(eq before, remaining need).
+  const uint32_t eq_cta_before = bc[6];
+  const uint32_t need_here = need_eq > eq_cta_before ? need_eq - eq_cta_before : 0u;
+  const uint32_t taken_lower = min(weq[warp], need_here);
+  uint32_t o = bc[5] + wsel[warp] + taken_lower;
+  const uint32_t total_sel = bc[7];
   int32_t* orow = out + static_cast<int64_t>(q) * k;
-  const int32_t* prow = pool + static_cast<int64_t>(q) * 2048;
-  uint32_t taken_eq = 0;
-  for (int i = s0; i < s1; ++i) {
-    const uint32_t u = key[i];
-    bool sel = u > T;
-    if (!sel && u == T && u != 0u && taken_eq < take_eq) {
-      sel = true;
-      ++taken_eq;
-    }
+  uint32_t eq_taken = 0;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t u = i < w1 ? key[i] : 0u;
+    const bool is_gt = u > T;
+    const bool is_eq = u == T && u != 0u;
+    const uint32_t eq_ball = __ballot_sync(0xffffffffu, is_eq);
+    const uint32_t eq_rank = eq_taken + __popc(eq_ball & lt_mask);
+    const bool sel = is_gt || (is_eq && eq_rank < take_w);
+    const uint32_t sel_ball = __ballot_sync(0xffffffffu, sel);
     if (sel) {
+      const uint32_t pos = o + __popc(sel_ball & lt_mask);
       const int64_t gi = lo + i;
-      const int32_t v = kMode == 0 ? static_cast<int32_t>(gi) : prow[gi >> 3] * 8 + static_cast<int32_t>(gi & 7);
-      if (o < static_cast<uint32_t>(k)) orow[o] = v;  // never past the row, whatever the counts say
-      ++o;
+      const int32_t v = kMode == 0 ? static_cast<int32_t>(gi) : pool_sm[gi >> 3] * 8 + static_cast<int32_t>(gi & 7);
+      if (pos < static_cast<uint32_t>(k)) orow[pos] = v;  // never past the row, whatever the counts say
     }
+    o += __popc(sel_ball);
+    eq_taken += __popc(eq_ball);
   }
   if (r == 0)
     for (int i = static_cast<int>(min(total_sel, static_cast<uint32_t>(k))) + tid; i < k; i += kThreads) orow[i] = -1;
   cluster_sync_all();  // keep this CTA's shared memory alive until every remote read is done
 }
 
-constexpr size_t kClusterSmem = (kChunk + 2048 + 2048 + 32 + 4 + 4) * sizeof(uint32_t);
+constexpr size_t kClusterSmem = (kChunk + 2 * kBins + 32 * 3 + 8 + 8 + 2048) * sizeof(uint32_t);
 
 template <int kMode>
 cudaError_t launch_cluster_topk(const float* keys, int64_t row_stride, const int64_t* seq_len, int Q,

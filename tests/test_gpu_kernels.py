@@ -313,3 +313,36 @@ def test_host_validation_errors():
         csa2.csa2_sparse_attn(L.q, S.topk, S.seq_len, S.cache.block_table, S.cache.n_pages, S.cache.main_pages,
                               S.cache.rings, L.ring_idx, o, None, small)
     assert e.value.status == csa2.ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("weights", ["zero", "mixed_sign"])
+def test_indexer_full_ties_and_mixed_sign_scores(weights):
+    """All scores tied (zero head weights: the lowest blocks and positions win)
+    and scores of both signs (negative head weights), at a context whose block
+    selection spans several CTAs of a cluster."""
+    N, B = 140000, 2
+    wl = Workload(99, "t", "full", B=B, N=N, n_q=1)
+    S = H.build(wl, DEV, shuffle_seed=17, prefill_step=True)
+    L = S.layers[0]
+    if weights == "zero":
+        L.w.zero_()
+        L.w_np[:] = 0
+    else:
+        L.w.mul_(2.0).sub_(1.0)
+        L.w_np[:] = L.w.cpu().numpy()
+    csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
+    pool = torch.empty(B, 1, 2048, dtype=torch.int32, device=DEV)
+    topk = torch.empty(B, 1, 512, dtype=torch.int32, device=DEV)
+    ws = torch.empty(csa2.csa2_workspace_bytes(csa2.OP_INDEXER_FULL, B, 1, N), dtype=torch.uint8, device=DEV)
+    csa2.csa2_indexer_full(L.q_codes, L.q_scales, L.w, S.seq_len, N, S.cache.block_table, S.cache.n_pages,
+                           S.cache.idx_pages, pool, topk, ws)
+    gp, gt = pool.cpu().numpy(), topk.cpu().numpy()
+    _status_ok()
+    for b in range(B):
+        if weights == "zero":
+            assert gp[b, 0].tolist() == list(range(2048))
+            assert gt[b, 0].tolist() == list(range(512))
+        else:
+            ref = H.oracle_full(S, b, 0)
+            H.check_selection(gp[b, 0], ref["pool"], lambda i: ref["blockmax"][i], 2048, "pool")
+            H.check_selection(gt[b, 0], ref["topk"], lambda i: ref["scores"][i], 512, "topk")
