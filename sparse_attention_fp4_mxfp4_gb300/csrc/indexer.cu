@@ -70,8 +70,15 @@ __host__ __device__ constexpr TmemPlan tmem_plan(int n_q) {
   return TmemPlan{nacc, sf, sf + 16u, cols};
 }
 
-__host__ __device__ constexpr int smem_bytes_for(int n_q) {
-  return 1024 /*align*/ + kStages * kTileBytes + 32 * n_q * 64 /*q operand*/ + 2048 /*barriers, w*/;
+// Pool rescore: per pool slot of the CTA's tiles, the source (page * 16 + block
+// in page, or kNoSlot) and the number of causal positions in the block.
+constexpr int kPoolSlots = 2048;
+constexpr uint32_t kNoSlot = 0xFFFFFFFFu;
+constexpr int kPoolTableBytes = kPoolSlots * 5;
+
+__host__ __device__ constexpr int smem_bytes_for(int n_q, bool pool) {
+  return 1024 /*align*/ + kStages * kTileBytes + 32 * n_q * 64 /*q operand*/ + 2048 /*barriers, w*/ +
+         (pool ? kPoolTableBytes : 0);
 }
 
 template <bool kPool>
@@ -89,6 +96,8 @@ __global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 196);
   uint32_t* stage_mask = reinterpret_cast<uint32_t*>(misc + 200);  // kStages words
   float* wsm = reinterpret_cast<float*>(misc + 256);                 // n_cols floats
+  uint32_t* slot_src = reinterpret_cast<uint32_t*>(misc + 2048);      // pool mode: [n_tiles * 16]
+  uint8_t* slot_n = misc + 2048 + kPoolSlots * 4;                     // pool mode: [n_tiles * 16]
 
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[kStages]);
   const uint32_t sfull0 = smem_u32(&bars[2 * kStages]);
@@ -147,6 +156,31 @@ __global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P
       const int jj = kPool ? jq : i >> 5;
       wsm[i] = P.w[(static_cast<int64_t>(b) * P.n_q + jj) * 32 + (i & 31)];
     }
+    if (kPool) {
+      // Resolve every pool slot of this CTA's tiles up front (all lookups of a
+      // thread in flight together), so the producer issues copies without
+      // waiting on global memory.
+      const int64_t t_q = seq_n - P.n_q + jq;
+      const int32_t* prow = P.pool + (static_cast<int64_t>(b) * P.n_q + jq) * 2048 + first_tile * 16;
+      for (int e = tid; e < n_tiles * 16; e += 128) {
+        const int32_t blk = prow[e];
+        uint32_t src = kNoSlot;
+        int nv = 0;
+        if (blk >= 0 && static_cast<int64_t>(blk) * 8 <= t_q) {
+          const int64_t lp = static_cast<int64_t>(blk) >> 4;
+          const int32_t page = lp < P.max_pages ? P.block_table[static_cast<int64_t>(b) * P.max_pages + lp] : -1;
+          if (page < 0 || page >= P.n_pages) {
+            report(CSA2_ERR_DEVICE_BOUNDS, 203);
+          } else {
+            src = static_cast<uint32_t>(page) * 16u + static_cast<uint32_t>(blk & 15);
+            const int64_t left = t_q - static_cast<int64_t>(blk) * 8 + 1;
+            nv = left < 8 ? static_cast<int>(left) : 8;
+          }
+        }
+        slot_src[e] = src;
+        slot_n[e] = static_cast<uint8_t>(nv);
+      }
+    }
     fence_proxy_async();
   }
   tc_fence_before();
@@ -178,7 +212,6 @@ __global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P
 
   if (warp == 4) {
     // ---- producer (whole warp: lookups in parallel, one bulk copy per lane) ----
-    const int64_t t_q = seq_n - P.n_q + jq;
     int32_t next_pages = -1;  // scan: page id of tile (i & ~31) + lane
     for (int64_t i = 0; i < n_tiles; ++i) {
       const int s = static_cast<int>(i % kStages);
@@ -189,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P
         go = *abort_flag ? 0 : 1;
       }
       if (!__shfl_sync(0xffffffffu, go, 0)) break;
-      const int64_t tile = first_tile + i * tile_stride;
       const uint32_t dst = smem_u32(stages + s * kTileBytes);
       if (!kPool) {
         if ((i & 31) == 0) {  // page ids of the next 32 tiles, one per lane
@@ -210,18 +242,9 @@ __global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P
           }
         }
       } else {
-        // Lane g < 16 resolves pool slot g of this tile.
-        int32_t blk = -1, page = -1;
-        bool valid = false;
-        if (lane < 16) {
-          blk = P.pool[(static_cast<int64_t>(b) * P.n_q + jq) * 2048 + tile * 16 + lane];
-          if (blk >= 0 && static_cast<int64_t>(blk) * 8 <= t_q) {
-            const int64_t lp = static_cast<int64_t>(blk) >> 4;
-            page = lp < P.max_pages ? P.block_table[static_cast<int64_t>(b) * P.max_pages + lp] : -1;
-            if (page < 0 || page >= P.n_pages) report(CSA2_ERR_DEVICE_BOUNDS, 203);
-            else valid = true;
-          }
-        }
+        // Lane g < 16 copies pool slot g of this tile (resolved at start).
+        const uint32_t src = lane < 16 ? slot_src[i * 16 + lane] : kNoSlot;
+        const bool valid = src != kNoSlot;
         const uint32_t mask = __ballot_sync(0xffffffffu, valid) & 0xFFFFu;
         if (lane == 0) {
           stage_mask[s] = mask;
@@ -230,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P
         }
         __syncwarp();
         if (valid)
-          bulk_g2s(dst + lane * 576, P.idx_pages + static_cast<int64_t>(page) * kIdxPageBytes + (blk & 15) * 576,
+          bulk_g2s(dst + lane * 576, P.idx_pages + static_cast<int64_t>(src >> 4) * kIdxPageBytes + (src & 15) * 576,
                    576, full0 + 8 * s);
       }
     }
@@ -305,10 +328,8 @@ __global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P
           if ((tid & 7) == 0 && row_ok && p <= t_q)
             P.block_max[(static_cast<int64_t>(b) * P.n_q + jj) * P.max_blocks + (p >> 3)] = m;
         } else {
-          const int64_t t_q = seq_n - P.n_q + jq;
-          const int32_t blk = P.pool[(static_cast<int64_t>(b) * P.n_q + jq) * 2048 + tile * 16 + (tid >> 3)];
-          const int64_t p = static_cast<int64_t>(blk) * 8 + (tid & 7);
-          const float v = (row_ok && p <= t_q) ? s : -INFINITY;
+          const bool causal = (tid & 7) < slot_n[i * 16 + (tid >> 3)];
+          const float v = (row_ok && causal) ? s : -INFINITY;
           P.scores[(static_cast<int64_t>(b) * P.n_q + jq) * 16384 + tile * 128 + tid] = v;
         }
       }
@@ -346,13 +367,13 @@ __global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P
 
 template <bool kPool>
 cudaError_t launch(const ScanParams& p, dim3 grid, int n_q, cudaStream_t stream) {
-  const int smem = smem_bytes_for(kPool ? 1 : n_q);
+  const int smem = smem_bytes_for(kPool ? 1 : n_q, kPool);
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(indexer_kernel<kPool>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes_for(8));
+                                         smem_bytes_for(kPool ? 1 : 8, kPool));
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
@@ -374,8 +395,8 @@ int num_sms() {
 }
 
 // Resident CTAs per SM, bounded by shared memory and TMEM columns.
-int ctas_per_sm(int n_q) {
-  const int by_smem = (228 * 1024) / (smem_bytes_for(n_q) + 1024);
+int ctas_per_sm(int n_q, bool pool) {
+  const int by_smem = (228 * 1024) / (smem_bytes_for(n_q, pool) + 1024);
   const int by_tmem = 512 / static_cast<int>(tmem_plan(n_q).ncols);
   return std::max(1, std::min(by_smem, by_tmem));
 }
@@ -416,7 +437,7 @@ cudaError_t launch_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales,
   p.block_max = block_max;
   p.max_blocks = max_blocks;
   const int64_t pages = (max_ctx + 127) / 128;
-  const int64_t target = static_cast<int64_t>(ctas_per_sm(n_q)) * num_sms();
+  const int64_t target = static_cast<int64_t>(ctas_per_sm(n_q, false)) * num_sms();
   const int64_t per_seq = std::max<int64_t>(1, std::min<int64_t>(pages, (target + B - 1) / B));
   return launch<false>(p, dim3(static_cast<unsigned>(per_seq), B), n_q, stream);
 }
@@ -441,7 +462,7 @@ cudaError_t launch_pool_scores(const uint8_t* q_codes, const uint8_t* q_scales, 
   p.idx_pages = idx_pages;
   p.pool = pool;
   p.scores = scores;
-  const int64_t target = static_cast<int64_t>(ctas_per_sm(1)) * num_sms();
+  const int64_t target = static_cast<int64_t>(ctas_per_sm(1, true)) * num_sms();
   int splits = static_cast<int>(std::min<int64_t>(128, std::max<int64_t>(1, (target + Q - 1) / Q)));
   const int per = (128 + splits - 1) / splits;
   splits = (128 + per - 1) / per;

@@ -26,7 +26,9 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide exclusive prefix sum over 1024 threads; returns the total in *total.
+// Block-wide exclusive prefix sum over kWarps warps (the whole block); returns
+// the total in *total.
+template <int kWarps = 32>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
@@ -38,17 +40,17 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_s
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t s = warp_sums[lane];
+    uint32_t s = lane < kWarps ? warp_sums[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    warp_sums[lane] = s;  // inclusive
+    if (lane < kWarps) warp_sums[lane] = s;  // inclusive
   }
   __syncthreads();
   const uint32_t base = warp > 0 ? warp_sums[warp - 1] : 0u;
-  const uint32_t tot = warp_sums[31];
+  const uint32_t tot = warp_sums[kWarps - 1];
   __syncthreads();
   *total = tot;
   return base + x - v;
@@ -63,15 +65,13 @@ __device__ __forceinline__ void warp_hist_add(uint32_t* hist, bool take, uint32_
   if (take && (threadIdx.x & 31) == static_cast<uint32_t>(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
 }
 
-// Row of n keys, pick k. `map` turns an element index into the output value.
-// mode 0: block top-k (value = block id); mode 1: pool top-k (value = position
-// pool[i / 8] * 8 + i % 8).
-template <int kMode>
+// Block top-k of one row of block maxima (n = the causal blocks of the token),
+// pick k; the output values are block ids. Reads the row from global memory
+// on every pass: it serves rows too long for a cluster.
 __global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __restrict__ keys,
                                                               int64_t row_stride,
                                                               const int64_t* __restrict__ seq_len,
                                                               int n_q, int k,
-                                                              const int32_t* __restrict__ pool,
                                                               int32_t* __restrict__ out) {
   __shared__ uint32_t hist[2048];
   __shared__ uint32_t warp_sums[32];
@@ -82,18 +82,12 @@ __global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __res
   const int tid = threadIdx.x;
   const float* row = keys + static_cast<int64_t>(q) * row_stride;
   int32_t* orow = out + static_cast<int64_t>(q) * k;
-  int64_t n;
-  if (kMode == 0) {
-    const int64_t t = seq_len[b] - n_q + j;
-    n = t >= 0 ? (t + 8) / 8 : 0;
-    if (n > row_stride) {
-      if (tid == 0) report(CSA2_ERR_DEVICE_BOUNDS, 301);
-      n = row_stride;
-    }
-  } else {
+  const int64_t t = seq_len[b] - n_q + j;
+  int64_t n = t >= 0 ? (t + 8) / 8 : 0;
+  if (n > row_stride) {
+    if (tid == 0) report(CSA2_ERR_DEVICE_BOUNDS, 301);
     n = row_stride;
   }
-  const int32_t* prow = pool + static_cast<int64_t>(q) * 2048;
 
   // Radix passes. prefix/mask describe the bits fixed so far; `remaining`
   // counts how many elements still have to be taken among those matching.
@@ -171,13 +165,7 @@ __global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __res
       ++taken_eq;
     }
     if (sel) {
-      int32_t v;
-      if (kMode == 0) {
-        v = static_cast<int32_t>(i);
-      } else {
-        v = prow[i >> 3] * 8 + static_cast<int32_t>(i & 7);
-      }
-      if (o < static_cast<uint32_t>(k)) orow[o] = v;  // never past the row, whatever the counts say
+      if (o < static_cast<uint32_t>(k)) orow[o] = static_cast<int32_t>(i);  // never past the row, whatever the counts say
       ++o;
     }
   }
@@ -219,12 +207,10 @@ __device__ __forceinline__ uint32_t dsmem_ld(const uint32_t* local, uint32_t ran
   return v;
 }
 
-template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* __restrict__ keys,
                                                                 int64_t row_stride,
                                                                 const int64_t* __restrict__ seq_len,
                                                                 int n_q, int k, int C,
-                                                                const int32_t* __restrict__ pool,
                                                                 int32_t* __restrict__ out) {
   extern __shared__ uint32_t sm[];
   uint32_t* key = sm;                    // [kChunk] ordered keys of this CTA's slice
@@ -236,19 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
   uint32_t* xchg = weq + 32;             // [8] values read by other CTAs (0-2 min/max/valid,
                                          // 3 slice total, 6-7 gt/eq counts)
   uint32_t* bc = xchg + 8;               // [8] block-wide broadcasts
-  int32_t* pool_sm = reinterpret_cast<int32_t*>(bc + 8);  // [2048] pool row (pool mode)
 
   const uint32_t r = cluster_rank();
   const int q = blockIdx.y;
   const int b = q / n_q, j = q % n_q;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int64_t n;
-  if (kMode == 0) {
-    const int64_t t = seq_len[b] - n_q + j;
-    n = t >= 0 ? (t + 8) / 8 : 0;
-  } else {
-    n = row_stride;
-  }
+  const int64_t t = seq_len[b] - n_q + j;
+  int64_t n = t >= 0 ? (t + 8) / 8 : 0;
   if (n > row_stride || n > static_cast<int64_t>(C) * kChunk) {
     if (tid == 0 && r == 0) report(CSA2_ERR_DEVICE_BOUNDS, 311);
     n = min(row_stride, static_cast<int64_t>(C) * kChunk);
@@ -282,10 +262,6 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
       vmax = max(vmax, u);
       ++nvalid;
     }
-  }
-  if (kMode == 1) {  // the pool row, for turning slots into positions in the compaction
-    const int32_t* prow_g = pool + static_cast<int64_t>(q) * 2048;
-    for (int i = tid; i < 2048; i += kThreads) pool_sm[i] = prow_g[i];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -505,9 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
     const uint32_t sel_ball = __ballot_sync(0xffffffffu, sel);
     if (sel) {
       const uint32_t pos = o + __popc(sel_ball & lt_mask);
-      const int64_t gi = lo + i;
-      const int32_t v = kMode == 0 ? static_cast<int32_t>(gi) : pool_sm[gi >> 3] * 8 + static_cast<int32_t>(gi & 7);
-      if (pos < static_cast<uint32_t>(k)) orow[pos] = v;  // never past the row, whatever the counts say
+      if (pos < static_cast<uint32_t>(k)) orow[pos] = static_cast<int32_t>(lo + i);  // never past the row, whatever the counts say
     }
     o += __popc(sel_ball);
     eq_taken += __popc(eq_ball);
@@ -517,20 +491,18 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
   cluster_sync_all();  // keep this CTA's shared memory alive until every remote read is done
 }
 
-constexpr size_t kClusterSmem = (kChunk + 2 * kBins + 32 * 3 + 8 + 8 + 2048) * sizeof(uint32_t);
+constexpr size_t kClusterSmem = (kChunk + 2 * kBins + 32 * 3 + 8 + 8) * sizeof(uint32_t);
 
-template <int kMode>
 cudaError_t launch_cluster_topk(const float* keys, int64_t row_stride, const int64_t* seq_len, int Q,
-                                int n_q, int k, int C, const int32_t* pool, int32_t* out,
-                                cudaStream_t stream) {
+                                int n_q, int k, int C, int32_t* out, cudaStream_t stream) {
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(cluster_topk_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(cluster_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kClusterSmem));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(cluster_topk_kernel<kMode>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      e = cudaFuncSetAttribute(cluster_topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
@@ -546,7 +518,284 @@ cudaError_t launch_cluster_topk(const float* keys, int64_t row_stride, const int
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, cluster_topk_kernel<kMode>, keys, row_stride, seq_len, n_q, k, C, pool, out);
+  return cudaLaunchKernelEx(&cfg, cluster_topk_kernel, keys, row_stride, seq_len, n_q, k, C, out);
+}
+
+// ---- pool top-k: one CTA per token, the row in registers --------------------
+//
+// A token's pool row holds 16384 scores (2048 blocks x 8 positions). Each of
+// 1024 threads keeps 16 consecutive ordered keys in registers (4 float4 loads
+// in flight at once), so the row is read once and no pass touches global
+// memory. Warp shuffles are the scarce resource here (one warp instruction per
+// clock per SM), so reductions use redux.sync and work that needs a shuffle
+// scan is done by one warp, not redundantly by all 32.
+//
+// The threshold search first narrows the row to a candidate set: T0 = the
+// median over warps of each warp's second-largest sample (one sample per
+// lane) sits near the 6% quantile, so usually between k and 2048 keys are
+// >= T0. Those candidates go to shared memory and the span-based 12-bit radix
+// select runs on them alone (two keys per thread at most, hence few
+// shared-memory atomics). When the count falls outside [k, 2048] (heavy ties,
+// adversarial orders) the radix select runs on all keys instead; the result is
+// the same either way, only the cost differs. The compaction is one block
+// prefix sum of each thread's count of keys above and equal to the threshold,
+// packed into one word (16 bits each; a row has at most 16384 of either).
+constexpr int kPoolRow = 16384;
+constexpr int kPoolThreads = 1024;
+constexpr int kPoolWarps = kPoolThreads / 32;
+constexpr int kPoolKeys = kPoolRow / kPoolThreads;  // 16 consecutive keys per thread
+constexpr int kCandMax = 2048;
+
+struct SelectShared {
+  uint32_t hist[kBins];
+  uint32_t wtot[32];  // per-warp bin totals
+  uint32_t bc[4];     // crossing warp and keys above it; selected bin and keys above it
+};
+
+// The bin that holds the remaining-th largest counted key, scanning bins from
+// the top, and the number of keys in the bins above it; every thread gets both.
+// Warp w owns 128 consecutive bins from the top, lane l four of them; warp 0
+// finds the warp whose range holds the crossing, that warp finds the bin.
+// Three barriers; the block has 32 warps.
+__device__ __forceinline__ void find_bin(SelectShared& S, uint32_t remaining, uint32_t& bin, uint32_t& above) {
+  constexpr int kR = kBins / 32, kL = kR / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t c[kL], own = 0;
+#pragma unroll
+  for (int i = 0; i < kL; ++i) {
+    c[i] = S.hist[kBins - 1 - (warp * kR + lane * kL + i)];
+    own += c[i];
+  }
+  const uint32_t wsum = __reduce_add_sync(0xffffffffu, own);
+  if (lane == 0) S.wtot[warp] = wsum;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t wt = S.wtot[lane];
+    uint32_t incl = wt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (incl - wt < remaining && incl >= remaining) {
+      S.bc[0] = static_cast<uint32_t>(lane);
+      S.bc[1] = incl - wt;
+    }
+  }
+  __syncthreads();
+  if (warp == static_cast<int>(S.bc[0])) {
+    uint32_t incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    uint32_t before = S.bc[1] + incl - own;
+#pragma unroll
+    for (int i = 0; i < kL; ++i) {
+      if (before < remaining && before + c[i] >= remaining) {
+        S.bc[2] = static_cast<uint32_t>(kBins - 1 - (warp * kR + lane * kL + i));
+        S.bc[3] = before;
+      }
+      before += c[i];
+    }
+  }
+  __syncthreads();
+  bin = S.bc[2];
+  above = S.bc[3];
+}
+
+// Radix select over the valid keys >= lo (all of them <= hi) that visit()
+// hands to its callback: T = the k-th largest of them (at least k exist) and
+// need_eq = how many keys equal to T the top k take. Digits of 12 bits from
+// the top of the span hi - lo; at most three passes.
+template <class Visit>
+__device__ __forceinline__ void radix_threshold(const Visit& visit, uint32_t k, uint32_t lo, uint32_t hi,
+                                                SelectShared& S, uint32_t& T, uint32_t& need_eq) {
+  const uint32_t span = hi - lo;
+  const int bits = span ? 32 - __clz(span) : 0;
+  int shift = bits > kDigit ? bits - kDigit : 0;
+  uint32_t pref = 0u, hmask = 0u, remaining = k;
+  for (int pass = 0; pass < 3; ++pass) {
+    for (int i = threadIdx.x; i < kBins; i += blockDim.x) S.hist[i] = 0;
+    __syncthreads();
+    visit([&](uint32_t u) {
+      const uint32_t d = u - lo;
+      if (u != 0u && u >= lo && (d & hmask) == pref) atomicAdd(&S.hist[(d >> shift) & (kBins - 1)], 1u);
+    });
+    __syncthreads();
+    uint32_t bin, above;
+    find_bin(S, remaining, bin, above);
+    remaining -= above;
+    pref |= bin << shift;
+    hmask = ~((1u << shift) - 1u);
+    if (shift == 0) break;
+    shift = shift > kDigit ? shift - kDigit : 0;
+  }
+  T = lo + pref;
+  need_eq = remaining;
+}
+
+__global__ void __launch_bounds__(kPoolThreads, 1) pool_topk_kernel(const float* __restrict__ scores,
+                                                                    const int32_t* __restrict__ pool, int k,
+                                                                    int32_t* __restrict__ out) {
+  __shared__ SelectShared S;
+  __shared__ uint32_t cand[kCandMax];
+  __shared__ int32_t pool_sm[2048];
+  __shared__ uint32_t red[7 * 32];  // per-warp values; every use has its own 32 slots
+  __shared__ uint32_t misc[4];      // candidate count, T0, packed selection total
+
+  const int q = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float4* row = reinterpret_cast<const float4*>(scores + static_cast<int64_t>(q) * kPoolRow);
+  float4 f[kPoolKeys / 4];
+#pragma unroll
+  for (int j = 0; j < kPoolKeys / 4; ++j) f[j] = row[tid * (kPoolKeys / 4) + j];
+  const int32_t* prow = pool + static_cast<int64_t>(q) * 2048;
+#pragma unroll
+  for (int i = 0; i < 2048 / kPoolThreads; ++i) pool_sm[tid + i * kPoolThreads] = prow[tid + i * kPoolThreads];
+  if (tid == 0) misc[0] = 0;
+
+  uint32_t u[kPoolKeys];
+#pragma unroll
+  for (int j = 0; j < kPoolKeys / 4; ++j) {
+    u[4 * j + 0] = ordered_key(f[j].x);
+    u[4 * j + 1] = ordered_key(f[j].y);
+    u[4 * j + 2] = ordered_key(f[j].z);
+    u[4 * j + 3] = ordered_key(f[j].w);
+  }
+  // One sample per thread: the first or the eighth key of its run.
+  const uint32_t smp = (lane & 1) ? u[7] : u[0];
+  // Invalid keys are 0: u - 1 wraps them above every valid key for the minimum.
+  uint32_t vmin = 0xFFFFFFFFu, vmax = 0u, nvalid = 0u;
+#pragma unroll
+  for (int i = 0; i < kPoolKeys; ++i) {
+    vmin = min(vmin, u[i] - 1u);
+    vmax = max(vmax, u[i]);
+    nvalid += u[i] != 0u ? 1u : 0u;
+  }
+  vmin += 1u;  // 0 when every key of the thread is invalid: then vmax is 0 too
+  if (nvalid == 0u) vmin = 0xFFFFFFFFu;
+  // The warp's second-largest sample (the largest taken once).
+  const uint32_t m1 = __reduce_max_sync(0xffffffffu, smp);
+  const int first = __ffs(__ballot_sync(0xffffffffu, smp == m1)) - 1;
+  const uint32_t m2 = __reduce_max_sync(0xffffffffu, lane == first ? 0u : smp);
+  vmin = __reduce_min_sync(0xffffffffu, vmin);
+  vmax = __reduce_max_sync(0xffffffffu, vmax);
+  nvalid = __reduce_add_sync(0xffffffffu, nvalid);
+  if (lane == 0) {
+    red[warp] = vmin;
+    red[32 + warp] = vmax;
+    red[64 + warp] = nvalid;
+    red[96 + warp] = m2;
+  }
+  __syncthreads();
+  const uint32_t umin = __reduce_min_sync(0xffffffffu, red[lane]);
+  const uint32_t umax = __reduce_max_sync(0xffffffffu, red[32 + lane]);
+  const uint32_t total_valid = __reduce_add_sync(0xffffffffu, red[64 + lane]);
+
+  // Threshold: take keys > T and the first need_eq keys equal to T.
+  uint32_t T = 0u, need_eq = 0u;
+  if (total_valid > static_cast<uint32_t>(k)) {
+    if (warp == 0) {  // T0 = the 16th largest of the warps' second-largest samples
+      const uint32_t v = red[96 + lane];
+      uint32_t rank = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t x = __shfl_sync(0xffffffffu, v, j);
+        rank += (x > v || (x == v && j < lane)) ? 1u : 0u;
+      }
+      if (rank == 15u) misc[1] = v;
+    }
+    __syncthreads();
+    const uint32_t T0 = misc[1];
+    uint32_t c = 0;  // T0 >= 1 whenever it is used, so invalid keys never count
+#pragma unroll
+    for (int i = 0; i < kPoolKeys; ++i) c += u[i] >= T0 ? 1u : 0u;
+    const uint32_t cw = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) red[128 + warp] = cw;
+    __syncthreads();
+    const uint32_t n_cand = __reduce_add_sync(0xffffffffu, red[128 + lane]);
+    if (T0 != 0u && n_cand >= static_cast<uint32_t>(k) && n_cand <= static_cast<uint32_t>(kCandMax)) {
+      // Candidates to shared memory (any order).
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t base = 0;
+      if (lane == 31) base = atomicAdd(&misc[0], incl);
+      uint32_t o = __shfl_sync(0xffffffffu, base, 31) + incl - c;
+#pragma unroll
+      for (int i = 0; i < kPoolKeys; ++i)
+        if (u[i] >= T0) cand[o++] = u[i];
+      __syncthreads();
+      radix_threshold([&](auto&& fn) {
+        for (int i = tid; i < static_cast<int>(n_cand); i += kPoolThreads) fn(cand[i]);
+      }, static_cast<uint32_t>(k), T0, umax, S, T, need_eq);
+    } else {
+      radix_threshold([&](auto&& fn) {
+#pragma unroll
+        for (int i = 0; i < kPoolKeys; ++i) fn(u[i]);
+      }, static_cast<uint32_t>(k), umin, umax, S, T, need_eq);
+    }
+  }
+
+  // Ordered compaction: one block prefix sum of the packed (above, equal)
+  // counts, then each thread writes its selected slots in order. When T = 0
+  // (every valid key is taken) the "equal" keys are the invalid ones and
+  // need_eq = 0 takes none of them.
+  uint32_t gm = 0, em = 0;  // per-key masks: above T, equal to T
+#pragma unroll
+  for (int i = 0; i < kPoolKeys; ++i) {
+    gm |= (u[i] > T ? 1u : 0u) << i;
+    em |= (u[i] == T ? 1u : 0u) << i;
+  }
+  const uint32_t v = (static_cast<uint32_t>(__popc(gm)) << 16) | static_cast<uint32_t>(__popc(em));
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) red[160 + warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t wt = red[160 + lane];
+    uint32_t wi = wt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    red[192 + lane] = wi - wt;
+    if (lane == 31) misc[2] = wi;
+  }
+  __syncthreads();
+  const uint32_t tot = misc[2];
+  const uint32_t n_sel = min((tot >> 16) + min(tot & 0xFFFFu, need_eq), static_cast<uint32_t>(k));
+  int32_t* orow = out + static_cast<int64_t>(q) * k;
+  const uint32_t base = red[192 + warp] + incl - v;
+  const uint32_t gb = base >> 16, eb = base & 0xFFFFu;  // keys above / equal to T in lower threads
+  // This thread's equal keys that are taken: the lowest min(popc, need_eq - eb) of them.
+  uint32_t take = need_eq > eb ? need_eq - eb : 0u;
+  uint32_t sel = gm, rest = em;
+  while (take > 0u && rest != 0u) {
+    const uint32_t lowest = rest & (0u - rest);
+    sel |= lowest;
+    rest ^= lowest;
+    --take;
+  }
+  uint32_t pos = gb + min(eb, need_eq);
+  while (sel != 0u) {
+    const int i = __ffs(sel) - 1;
+    sel &= sel - 1u;
+    const int slot = tid * kPoolKeys + i;
+    if (pos < static_cast<uint32_t>(k)) orow[pos] = pool_sm[slot >> 3] * 8 + (slot & 7);
+    ++pos;
+  }
+  for (int i = static_cast<int>(n_sel) + tid; i < k; i += kPoolThreads) orow[i] = -1;
 }
 
 }  // namespace
@@ -571,22 +820,22 @@ cudaError_t launch_block_topk(const float* block_max, const int64_t* seq_len, in
   if (Q == 0) return cudaSuccess;
   const int64_t C = (max_blocks + kChunk - 1) / kChunk;
   if (C <= 16) {
-    const cudaError_t e = launch_cluster_topk<0>(block_max, max_blocks, seq_len, Q, n_q, 2048,
-                                                 static_cast<int>(C < 1 ? 1 : C), nullptr, pool, stream);
+    const cudaError_t e = launch_cluster_topk(block_max, max_blocks, seq_len, Q, n_q, 2048,
+                                              static_cast<int>(C < 1 ? 1 : C), pool, stream);
     if (e == cudaSuccess || C <= 8) return e;
     cudaGetLastError();  // a 16-CTA cluster may not fit this GPU: use the global-memory select
   }
-  radix_topk_kernel<0><<<Q, kThreads, 0, stream>>>(block_max, max_blocks, seq_len, n_q, 2048,
-                                                   nullptr, pool);
+  radix_topk_kernel<<<Q, kThreads, 0, stream>>>(block_max, max_blocks, seq_len, n_q, 2048, pool);
   return cudaGetLastError();
 }
 
 cudaError_t launch_pool_topk(const float* scores, const int64_t* seq_len, int B, int n_q,
                              const int32_t* pool, int32_t* topk, cudaStream_t stream) {
+  (void)seq_len;  // causality is already in the scores: masked slots are -inf
   const int Q = B * n_q;
   if (Q == 0) return cudaSuccess;
-  // 16384 scores per token, 2048 per CTA of an 8-CTA cluster.
-  return launch_cluster_topk<1>(scores, 16384, seq_len, Q, n_q, 512, 8, pool, topk, stream);
+  pool_topk_kernel<<<Q, kPoolThreads, 0, stream>>>(scores, pool, 512, topk);
+  return cudaGetLastError();
 }
 
 }  // namespace csa2
