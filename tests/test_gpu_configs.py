@@ -9,7 +9,8 @@ times (tests.harness.Runner), on outputs the oracle can compute one by one:
      token) pairs and the attention of all four layers for them
 
 Selections: equal up to ties within 1e-5 relative of the oracle's k-th score.
-Attention: within 4e-3 max-relative per head row (bf16 output, as timed).
+Attention: within 2e-3 + 2^-8 (1 + 2e-3) ~ 5.9e-3 max-relative per head row (bf16
+output, as timed: the fp32 bound plus bf16 rounding).
 """
 import numpy as np
 import pytest
