@@ -201,26 +201,52 @@ def run_ours(args, wl, rank, world, local):
     if st != csa2.OK:
         raise RuntimeError("device status after warm-up: " + csa2.device_status_message())
 
+    # The step's launches are captured once in a CUDA graph (a decode step has
+    # the same shape every time); the graph is what the headline times.
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            R.step()
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            R.step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        st = csa2.csa2_check_device_status()
+        if st != csa2.OK:
+            raise RuntimeError("device status after graph warm-up: " + csa2.device_status_message())
+
+    def timed(run_step, steps):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            run_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) / steps
+
     clocks = ClockSampler(local)
     clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        R.step(mark)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    # Per-kernel durations: the same steps launched one by one with events
+    # around every stage, back to back on the launching stream.
+    stage_steps = args.steps if graph is None else max(3, min(args.steps, 500))
+    ms_eager = timed(lambda: R.step(mark), stage_steps)
+    ms = timed(graph.replay, args.steps) if graph is not None else ms_eager
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(ms, world, dev)
     stage_ms = {}
     for name in ("scan", "blocktopk", "rescore", "attn"):
         if name + "0" in ev:
             tt = [a.elapsed_time(b) for a, b in zip(ev[name + "0"], ev[name + "1"])]
-            stage_ms[name] = sum(tt) / args.steps  # per step (all layers)
+            stage_ms[name] = sum(tt) / stage_steps  # per step (all layers)
     st = csa2.csa2_check_device_status()
     if st != csa2.OK:
         raise RuntimeError("device status after timing: " + csa2.device_status_message())
@@ -265,7 +291,9 @@ def run_ours(args, wl, rank, world, local):
                    "query_tokens": n_q, "queries_per_step": Q,
                    "l2": "inputs larger than L2 (store of %.1f GB; the step reads %.0f MB)" % (
                        S.cache.nbytes() / 1e9, step_bytes(wl) / 1e6),
-                   "parallelism": f"replicas x{world} (independent sequences)", "setup_s": round(setup_s, 1)},
+                   "parallelism": f"replicas x{world} (independent sequences)", "setup_s": round(setup_s, 1),
+                   "launch": "CUDA graph of the whole step" if graph is not None else "eager launches",
+                   "ms_per_step_eager": ms_eager, "stage_steps": stage_steps},
         "hbm_fraction_step": (sb / (ms_max * 1e-3) / 1e9) / peak,
         "stage_ms": stage_ms,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -449,6 +477,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--B", type=int, default=None, help="override the batch (profiling captures only)")

@@ -200,6 +200,10 @@ class Runner:
         self.out = [torch.empty(B, n_q, 64, 512, dtype=out_dtype, device=dev) for _ in S.layers]
         self.lse = [torch.empty(B, n_q, 64, dtype=torch.float32, device=dev) for _ in S.layers]
         self.launches = 0
+        # The attention launch splits a token's five key chunks over several
+        # CTAs (plus a merge kernel) only while there are fewer tokens than SMs.
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.attn_launches = 1 if min(5, max(1, sms // Q)) == 1 else 2
 
     def step(self, mark=None):
         csa2, S, c = self.csa2, self.S, self.S.cache
@@ -231,7 +235,7 @@ class Runner:
             csa2.csa2_sparse_attn(L.q, self.topk, S.seq_len, c.block_table, c.n_pages, c.main_pages, c.rings,
                                   L.ring_idx, self.out[li], self.lse[li], self.ws)
             mark("attn1")
-            n += 2
+            n += self.attn_launches
         self.launches = n
 
 
