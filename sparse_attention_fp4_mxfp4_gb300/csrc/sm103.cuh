@@ -62,6 +62,21 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try, but the thread may be suspended until the phase completes or
+// about `hint_ns` nanoseconds pass, instead of spinning: a waiting warp then
+// takes no issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete. Gives up after about
 // 2 s (or 2^30 polls), records CSA2_ERR_DEVICE_TIMEOUT and returns false. When
 // `abort_flag` is given and another role of the CTA has set it, returns false
@@ -71,8 +86,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int whe
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0; i < (1u << 30); ++i) {
-    if (mbar_try(bar, parity)) return true;
-    if ((i & 255u) == 255u) {
+    if (mbar_try_suspend(bar, parity, 100000u)) return true;
+    if ((i & 15u) == 15u) {
       if (abort_flag && *abort_flag) return false;
       if (globaltimer_ns() - t0 > kWaitTimeoutNs) break;
     }

@@ -172,379 +172,9 @@ __global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __res
   for (int i = static_cast<int>(tot_sel) + tid; i < k; i += kThreads) orow[i] = -1;
 }
 
-// ---- cluster version: the row lives in shared memory ------------------------
-//
-// A cluster of C CTAs (C <= 16) selects from one row; CTA r keeps elements
-// [r * chunk, (r + 1) * chunk) of the row in shared memory as ordered keys, so
-// the row is read from global memory once. Keys are offset by the
-// cluster-wide minimum and cut into 12-bit digits from the top of the actual
-// span, so usual score ranges resolve in two passes and spread over many bins.
-// Each pass builds a local histogram; every CTA sums all C histograms through
-// distributed shared memory (all remote loads of a thread in flight at once)
-// and derives the same threshold digit. The ordered compaction is warp
-// cooperative: consecutive lanes take consecutive elements, warps take
-// consecutive ranges, so index order is kept without bank conflicts. Control
-// flow is uniform across the cluster: every CTA executes every cluster barrier.
-constexpr int kChunk = 16384;  // elements per CTA
+// ---- exact selection over a key set held by the block ------------------------
 constexpr int kDigit = 12;
 constexpr int kBins = 1 << kDigit;
-constexpr int kMaxC = 16;
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t dsmem_ld(const uint32_t* local, uint32_t rank) {
-  uint32_t ra, v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
-  return v;
-}
-
-__global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* __restrict__ keys,
-                                                                int64_t row_stride,
-                                                                const int64_t* __restrict__ seq_len,
-                                                                int n_q, int k, int C,
-                                                                int32_t* __restrict__ out) {
-  extern __shared__ uint32_t sm[];
-  uint32_t* key = sm;                    // [kChunk] ordered keys of this CTA's slice
-  uint32_t* hist = sm + kChunk;          // [kBins] local histogram
-  uint32_t* tot = hist + kBins;          // [kBins] cluster-wide histogram
-  uint32_t* warp_sums = tot + kBins;     // [32]
-  uint32_t* wsel = warp_sums + 32;       // [32] per-warp selection offsets
-  uint32_t* weq = wsel + 32;             // [32] per-warp equal-key takes
-  uint32_t* xchg = weq + 32;             // [8] values read by other CTAs (0-2 min/max/valid,
-                                         // 3 slice total, 6-7 gt/eq counts)
-  uint32_t* bc = xchg + 8;               // [8] block-wide broadcasts
-
-  const uint32_t r = cluster_rank();
-  const int q = blockIdx.y;
-  const int b = q / n_q, j = q % n_q;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t t = seq_len[b] - n_q + j;
-  int64_t n = t >= 0 ? (t + 8) / 8 : 0;
-  if (n > row_stride || n > static_cast<int64_t>(C) * kChunk) {
-    if (tid == 0 && r == 0) report(CSA2_ERR_DEVICE_BOUNDS, 311);
-    n = min(row_stride, static_cast<int64_t>(C) * kChunk);
-  }
-  const int64_t chunk = (n + C - 1) / C;
-  const int64_t lo = static_cast<int64_t>(r) * chunk;
-  const int64_t hi = min(n, lo + chunk);
-  const int m = hi > lo ? static_cast<int>(hi - lo) : 0;
-  const float* row = keys + static_cast<int64_t>(q) * row_stride + lo;
-
-  if (tid == 0) {
-    xchg[0] = 0xFFFFFFFFu;
-    xchg[1] = 0u;
-  }
-  __syncthreads();
-  uint32_t vmin = 0xFFFFFFFFu, vmax = 0u, nvalid = 0;
-  constexpr int kLoads = kChunk / kThreads;  // every load of a thread in flight at once
-  float f[kLoads];
-#pragma unroll
-  for (int it = 0; it < kLoads; ++it) {
-    const int i = tid + it * kThreads;
-    f[it] = i < m ? row[i] : -INFINITY;
-  }
-#pragma unroll
-  for (int it = 0; it < kLoads; ++it) {
-    const int i = tid + it * kThreads;
-    const uint32_t u = ordered_key(f[it]);
-    if (i < m) key[i] = u;
-    if (u != 0u) {
-      vmin = min(vmin, u);
-      vmax = max(vmax, u);
-      ++nvalid;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    vmin = min(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
-    vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
-  }
-  if (lane == 0) {
-    atomicMin(&xchg[0], vmin);
-    atomicMax(&xchg[1], vmax);
-  }
-  uint32_t cta_valid;
-  block_excl_scan(nvalid, warp_sums, &cta_valid);
-  if (tid == 0) xchg[2] = cta_valid;
-  cluster_sync_all();
-  if (warp == 0) {
-    uint32_t mn = 0xFFFFFFFFu, mx = 0u, nv = 0u;
-    if (lane < C) {
-      mn = dsmem_ld(&xchg[0], lane);
-      mx = dsmem_ld(&xchg[1], lane);
-      nv = dsmem_ld(&xchg[2], lane);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      nv += __shfl_xor_sync(0xffffffffu, nv, o);
-    }
-    if (lane == 0) {
-      bc[0] = mn;
-      bc[1] = mx;
-      bc[2] = nv;
-    }
-  }
-  __syncthreads();
-  const uint32_t umin = bc[0], umax = bc[1], total_valid = bc[2];
-
-  // Threshold: take keys > T and the first need_eq keys equal to T.
-  uint32_t T = 0u, need_eq = 0u;
-  if (total_valid > static_cast<uint32_t>(k)) {
-    const uint32_t span = umax - umin;
-    const int bits = span ? 32 - __clz(span) : 0;
-    int shift = bits > kDigit ? bits - kDigit : 0;
-    uint32_t pref = 0u, hmask = 0u, remaining = static_cast<uint32_t>(k);
-    for (int pass = 0; pass < 3; ++pass) {
-      for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      for (int i = tid; i < m; i += kThreads) {
-        const uint32_t u = key[i];
-        const uint32_t d = u - umin;
-        if (u != 0u && (d & hmask) == pref) atomicAdd(&hist[(d >> shift) & (kBins - 1)], 1u);
-      }
-      cluster_sync_all();  // every local histogram is complete
-      // CTA r sums the bins of its slice [r * S, (r + 1) * S) over the cluster; a
-      // single CTA uses its own histogram as is.
-      const int S = kBins / C;
-      const uint32_t* totals = hist;
-      if (C > 1) {
-        uint32_t part = 0;
-        for (int bi = tid; bi < S; bi += kThreads) {
-          const int bin = static_cast<int>(r) * S + bi;
-          uint32_t v[kMaxC];
-#pragma unroll
-          for (int c = 0; c < kMaxC; ++c) v[c] = c < C ? dsmem_ld(&hist[bin], c) : 0u;
-          uint32_t sum = 0;
-#pragma unroll
-          for (int c = 0; c < kMaxC; ++c) sum += v[c];
-          tot[bin] = sum;
-          part += sum;
-        }
-        uint32_t slice_total;
-        block_excl_scan(part, warp_sums, &slice_total);
-        if (tid == 0) xchg[3] = slice_total;
-        totals = tot;
-      }
-      cluster_sync_all();  // slice sums complete; nobody reads a remote histogram any more
-      // The slice that holds the remaining-th largest key (slices of higher ranks
-      // hold higher digits), and the keys above it.
-      if (warp == 0) {
-        const uint32_t st = lane < C ? (C > 1 ? dsmem_ld(&xchg[3], lane) : 0u) : 0u;
-        uint32_t incl = st;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
-          if (lane + o < 32) incl += y;
-        }
-        const uint32_t above = incl - st;
-        if (lane == 0) {
-          bc[3] = 0;
-          bc[4] = 0;
-        }
-        __syncwarp();
-        if (C > 1 && lane < C && above < remaining && above + st >= remaining) {
-          bc[3] = lane;
-          bc[4] = above;
-        }
-      }
-      __syncthreads();
-      const uint32_t target = bc[3] & static_cast<uint32_t>(C - 1);  // always a rank of this cluster
-      const uint32_t above_t = bc[4];
-      __syncthreads();
-      // Thread t owns kPer consecutive bins of the target slice counted from the top.
-      constexpr int kPer = kBins / kThreads;
-      uint32_t c4[kPer], own = 0;
-#pragma unroll
-      for (int it = 0; it < kPer; ++it) {
-        const int rank = tid * kPer + it;
-        c4[it] = 0;
-        if (rank < S) {
-          const int bin = static_cast<int>(target) * S + (S - 1 - rank);
-          c4[it] = C > 1 ? dsmem_ld(&totals[bin], target) : totals[bin];
-        }
-        own += c4[it];
-      }
-      uint32_t total;
-      uint32_t before = above_t + block_excl_scan(own, warp_sums, &total);
-#pragma unroll
-      for (int it = 0; it < kPer; ++it) {
-        const int rank = tid * kPer + it;
-        if (rank < S && before < remaining && before + c4[it] >= remaining) {
-          bc[5] = static_cast<uint32_t>(static_cast<int>(target) * S + (S - 1 - rank));
-          bc[6] = before;
-        }
-        before += c4[it];
-      }
-      __syncthreads();
-      remaining -= bc[6];
-      pref |= bc[5] << shift;
-      hmask = ~((1u << shift) - 1u);
-      __syncthreads();
-      if (shift == 0) break;
-      shift = shift > kDigit ? shift - kDigit : 0;
-    }
-    T = umin + pref;
-    need_eq = remaining;
-  }
-
-  // Warp-cooperative counts over this CTA's slice: warp w owns [w * wseg, (w + 1) * wseg).
-  const int wseg = ((m + 32 * 32 - 1) / (32 * 32)) * 32;
-  const int w0 = warp * wseg, w1 = min(m, w0 + wseg);
-  uint32_t gt = 0, eq = 0;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint32_t u = i < w1 ? key[i] : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, u > T));
-    eq += __popc(__ballot_sync(0xffffffffu, u == T && u != 0u));
-  }
-  if (lane == 0) {
-    wsel[warp] = gt;
-    weq[warp] = eq;
-  }
-  __syncthreads();
-  if (warp == 0) {  // per-warp prefix sums within the CTA
-    const uint32_t g = wsel[lane], e = weq[lane];
-    uint32_t gi = g, ei = e;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t yg = __shfl_up_sync(0xffffffffu, gi, o), ye = __shfl_up_sync(0xffffffffu, ei, o);
-      if (lane >= o) {
-        gi += yg;
-        ei += ye;
-      }
-    }
-    wsel[lane] = gi - g;  // gt keys in lower warps
-    weq[lane] = ei - e;   // equal keys in lower warps
-    if (lane == 31) {
-      xchg[6] = gi;
-      xchg[7] = ei;
-    }
-  }
-  cluster_sync_all();
-  if (warp == 0) {  // ties go to the lowest indices: CTA slices are in index order
-    const uint32_t g = lane < C ? dsmem_ld(&xchg[6], lane) : 0u;
-    const uint32_t e = lane < C ? dsmem_ld(&xchg[7], lane) : 0u;
-    uint32_t e_incl = e;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, e_incl, o);
-      if (lane >= o) e_incl += y;
-    }
-    const uint32_t e_before = e_incl - e;
-    const uint32_t take = need_eq > e_before ? min(e, need_eq - e_before) : 0u;
-    uint32_t s_incl = g + take;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, s_incl, o);
-      if (lane >= o) s_incl += y;
-    }
-    const uint32_t total_sel = __shfl_sync(0xffffffffu, s_incl, 31);
-    if (lane == static_cast<int>(r)) {
-      bc[5] = s_incl - (g + take);  // selections in lower CTAs
-      bc[6] = e_before;             // equal keys in lower CTAs
-    }
-    if (lane == 0) bc[7] = total_sel;
-  }
-  __syncthreads();
-  // This warp's equal keys that are taken: ranks [eq_base, eq_base + eq) among equals.
-  const uint32_t eq_base = bc[6] + weq[warp];
-  const uint32_t take_w = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
-  // Selections before this warp: lower CTAs, then lower warps (gt + their takes).
-  // Equal keys taken by lower warps of this CTA: min(eq before, remaining need).
-  const uint32_t eq_cta_before = bc[6];
-  const uint32_t need_here = need_eq > eq_cta_before ? need_eq - eq_cta_before : 0u;
-  const uint32_t taken_lower = min(weq[warp], need_here);
-  uint32_t o = bc[5] + wsel[warp] + taken_lower;
-  const uint32_t total_sel = bc[7];
-  int32_t* orow = out + static_cast<int64_t>(q) * k;
-  uint32_t eq_taken = 0;
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint32_t u = i < w1 ? key[i] : 0u;
-    const bool is_gt = u > T;
-    const bool is_eq = u == T && u != 0u;
-    const uint32_t eq_ball = __ballot_sync(0xffffffffu, is_eq);
-    const uint32_t eq_rank = eq_taken + __popc(eq_ball & lt_mask);
-    const bool sel = is_gt || (is_eq && eq_rank < take_w);
-    const uint32_t sel_ball = __ballot_sync(0xffffffffu, sel);
-    if (sel) {
-      const uint32_t pos = o + __popc(sel_ball & lt_mask);
-      if (pos < static_cast<uint32_t>(k)) orow[pos] = static_cast<int32_t>(lo + i);  // never past the row, whatever the counts say
-    }
-    o += __popc(sel_ball);
-    eq_taken += __popc(eq_ball);
-  }
-  if (r == 0)
-    for (int i = static_cast<int>(min(total_sel, static_cast<uint32_t>(k))) + tid; i < k; i += kThreads) orow[i] = -1;
-  cluster_sync_all();  // keep this CTA's shared memory alive until every remote read is done
-}
-
-constexpr size_t kClusterSmem = (kChunk + 2 * kBins + 32 * 3 + 8 + 8) * sizeof(uint32_t);
-
-cudaError_t launch_cluster_topk(const float* keys, int64_t row_stride, const int64_t* seq_len, int Q,
-                                int n_q, int k, int C, int32_t* out, cudaStream_t stream) {
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(cluster_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kClusterSmem));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(cluster_topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) configured[dev] = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, Q, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kClusterSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, cluster_topk_kernel, keys, row_stride, seq_len, n_q, k, C, out);
-}
-
-// ---- pool top-k: one CTA per token, the row in registers --------------------
-//
-// A token's pool row holds 16384 scores (2048 blocks x 8 positions). Each of
-// 1024 threads keeps 16 consecutive ordered keys in registers (4 float4 loads
-// in flight at once), so the row is read once and no pass touches global
-// memory. Warp shuffles are the scarce resource here (one warp instruction per
-// clock per SM), so reductions use redux.sync and work that needs a shuffle
-// scan is done by one warp, not redundantly by all 32.
-//
-// The threshold search first narrows the row to a candidate set: T0 = the
-// median over warps of each warp's second-largest sample (one sample per
-// lane) sits near the 6% quantile, so usually between k and 2048 keys are
-// >= T0. Those candidates go to shared memory and the span-based 12-bit radix
-// select runs on them alone (two keys per thread at most, hence few
-// shared-memory atomics). When the count falls outside [k, 2048] (heavy ties,
-// adversarial orders) the radix select runs on all keys instead; the result is
-// the same either way, only the cost differs. The compaction is one block
-// prefix sum of each thread's count of keys above and equal to the threshold,
-// packed into one word (16 bits each; a row has at most 16384 of either).
-constexpr int kPoolRow = 16384;
-constexpr int kPoolThreads = 1024;
-constexpr int kPoolWarps = kPoolThreads / 32;
-constexpr int kPoolKeys = kPoolRow / kPoolThreads;  // 16 consecutive keys per thread
-constexpr int kCandMax = 2048;
 
 struct SelectShared {
   uint32_t hist[kBins];
@@ -635,6 +265,525 @@ __device__ __forceinline__ void radix_threshold(const Visit& visit, uint32_t k, 
   T = lo + pref;
   need_eq = remaining;
 }
+
+// ---- cluster version: the row lives in shared memory ------------------------
+//
+// A cluster of C CTAs (C <= 16) selects from one row; CTA r keeps elements
+// [r * chunk, (r + 1) * chunk) of the row in shared memory (and registers) as
+// ordered keys, so the row is read from global memory once.
+//
+// The threshold search first narrows the row to a candidate set with samples:
+// each warp sorts one sample per lane and takes the j-th largest, j chosen so
+// that about 2k/n of the row lies above it; a CTA takes the median over its
+// warps, the cluster the median over CTAs (T0). When between k and 8192 keys
+// are >= T0, every CTA writes its candidates into CTA 0's shared memory and
+// CTA 0 runs the span-based 12-bit radix select on them alone. Otherwise (short
+// rows, heavy ties) every pass runs over the whole row: each CTA builds a local
+// histogram, every CTA sums all C histograms through distributed shared memory
+// and derives the same threshold digit. Either way the result is the same.
+// The ordered compaction is warp cooperative: consecutive lanes take
+// consecutive elements, warps take consecutive ranges, so index order is kept
+// without bank conflicts. Control flow is uniform across the cluster: every
+// CTA executes every cluster barrier.
+constexpr int kChunk = 16384;  // elements per CTA
+constexpr int kMaxC = 16;
+constexpr int kBlkCandMax = 8192;  // candidate set of the sample filter (in CTA 0)
+
+struct ClusterShared {
+  uint32_t key[kChunk];         // ordered keys of this CTA's slice
+  SelectShared S;               // histogram and bin search
+  uint32_t tot[kBins];          // cluster-wide histogram slice (whole-row passes)
+  uint32_t cand[kBlkCandMax];   // CTA 0: the candidates of the whole row
+  uint32_t wred[4][32];         // per warp: min, max, valid count, sample statistic
+  uint32_t woff[32];            // per warp: offset of its candidates within the CTA
+  uint32_t warp_sums[32];
+  uint32_t wsel[32];            // per-warp selection offsets
+  uint32_t weq[32];             // per-warp equal-key takes
+  uint32_t xchg[16];            // read by other CTAs: 0-3 min/max/valid/sample median,
+                                // 4 candidate count, 5 slice total, 6-7 gt/eq counts,
+                                // 8-9 threshold and equal-key takes (CTA 0)
+  uint32_t bc[16];              // block-wide broadcasts
+};
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  return ra;
+}
+
+__device__ __forceinline__ uint32_t dsmem_ld(const uint32_t* local, uint32_t rank) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(dsmem_addr(local, rank)) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Ascending bitonic sort of one value per lane (lane 0 ends with the smallest).
+__device__ __forceinline__ uint32_t warp_sort_asc(uint32_t v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool asc = (lane & size) == 0;
+      const bool low = (lane & stride) == 0;
+      v = (low == asc) ? min(v, o) : max(v, o);
+    }
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* __restrict__ keys,
+                                                                int64_t row_stride,
+                                                                const int64_t* __restrict__ seq_len,
+                                                                int n_q, int k, int C,
+                                                                int32_t* __restrict__ out) {
+  extern __shared__ __align__(16) uint8_t cs_raw[];
+  ClusterShared& cs = *reinterpret_cast<ClusterShared*>(cs_raw);
+  uint32_t* key = cs.key;
+  uint32_t* hist = cs.S.hist;
+  uint32_t* tot = cs.tot;
+  uint32_t* warp_sums = cs.warp_sums;
+  uint32_t* wsel = cs.wsel;
+  uint32_t* weq = cs.weq;
+  uint32_t* xchg = cs.xchg;
+  uint32_t* bc = cs.bc;
+
+  const uint32_t r = cluster_rank();
+  const int q = blockIdx.y;
+  const int b = q / n_q, j = q % n_q;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t t = seq_len[b] - n_q + j;
+  int64_t n = t >= 0 ? (t + 8) / 8 : 0;
+  if (n > row_stride || n > static_cast<int64_t>(C) * kChunk) {
+    if (tid == 0 && r == 0) report(CSA2_ERR_DEVICE_BOUNDS, 311);
+    n = min(row_stride, static_cast<int64_t>(C) * kChunk);
+  }
+  const int64_t chunk = (n + C - 1) / C;
+  const int64_t lo = static_cast<int64_t>(r) * chunk;
+  const int64_t hi = min(n, lo + chunk);
+  const int m = hi > lo ? static_cast<int>(hi - lo) : 0;
+  const float* row = keys + static_cast<int64_t>(q) * row_stride + lo;
+
+  // Sample statistic: the j-th largest of a warp's 32 samples sits near the
+  // (j - 1/3) / (32 + 1/3) quantile; aim at 2k/n. Rows where that is above 1/2
+  // skip the sample filter.
+  // In integers (floating point here would be fp64, which this GPU runs
+  // slowly): j = floor((2k/n) * 97/3 + 5/6), filter only while 4k < n.
+  const bool try_filter = n > 4 * static_cast<int64_t>(k);
+  int jrank = n > 0 ? static_cast<int>((194 * static_cast<int64_t>(k) + 5 * n / 2) / (3 * n)) : 32;
+  jrank = jrank < 1 ? 1 : (jrank > 32 ? 32 : jrank);
+
+  constexpr int kLoads = kChunk / kThreads;  // every load of a thread in flight at once
+  uint32_t u[kLoads];
+  {
+    float f[kLoads];
+#pragma unroll
+    for (int it = 0; it < kLoads; ++it) {
+      const int i = tid + it * kThreads;
+      f[it] = i < m ? row[i] : -INFINITY;
+    }
+#pragma unroll
+    for (int it = 0; it < kLoads; ++it) {
+      const int i = tid + it * kThreads;
+      u[it] = ordered_key(f[it]);
+      if (i < m) key[i] = u[it];
+    }
+  }
+  uint32_t smp = u[0], vmin = 0xFFFFFFFFu, vmax = 0u, nvalid = 0u;
+#pragma unroll
+  for (int it = 0; it < kLoads; ++it) {
+    if (it == ((tid * 7) & (kLoads - 1))) smp = u[it];
+    vmin = min(vmin, u[it] - 1u);  // invalid keys (0) wrap above every valid one
+    vmax = max(vmax, u[it]);
+    nvalid += u[it] != 0u ? 1u : 0u;
+  }
+  vmin = nvalid ? vmin + 1u : 0xFFFFFFFFu;
+  vmin = __reduce_min_sync(0xffffffffu, vmin);
+  vmax = __reduce_max_sync(0xffffffffu, vmax);
+  nvalid = __reduce_add_sync(0xffffffffu, nvalid);
+  const uint32_t sorted = warp_sort_asc(smp, lane);
+  const uint32_t stat = __shfl_sync(0xffffffffu, sorted, 32 - jrank);
+  if (lane == 0) {
+    cs.wred[0][warp] = vmin;
+    cs.wred[1][warp] = vmax;
+    cs.wred[2][warp] = nvalid;
+    cs.wred[3][warp] = stat;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t mn = __reduce_min_sync(0xffffffffu, cs.wred[0][lane]);
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, cs.wred[1][lane]);
+    const uint32_t nv = __reduce_add_sync(0xffffffffu, cs.wred[2][lane]);
+    const uint32_t med = __shfl_sync(0xffffffffu, warp_sort_asc(cs.wred[3][lane], lane), 16);
+    if (lane == 0) {
+      xchg[0] = mn;
+      xchg[1] = mx;
+      xchg[2] = nv;
+      xchg[3] = med;
+    }
+  }
+  cluster_sync_all();
+  if (warp == 0) {
+    const bool in = lane < C;
+    const uint32_t mn = __reduce_min_sync(0xffffffffu, in ? dsmem_ld(&xchg[0], lane) : 0xFFFFFFFFu);
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, in ? dsmem_ld(&xchg[1], lane) : 0u);
+    const uint32_t nv = __reduce_add_sync(0xffffffffu, in ? dsmem_ld(&xchg[2], lane) : 0u);
+    const uint32_t tr = in ? dsmem_ld(&xchg[3], lane) : 0u;
+    uint32_t rank = 0;  // among the C CTA medians, ties by rank
+#pragma unroll
+    for (int l = 0; l < kMaxC; ++l) {
+      const uint32_t x = __shfl_sync(0xffffffffu, tr, l);
+      rank += (l < C && (x > tr || (x == tr && l < lane))) ? 1u : 0u;
+    }
+    const int pick = __ffs(__ballot_sync(0xffffffffu, in && rank == static_cast<uint32_t>(C / 2))) - 1;
+    const uint32_t T0 = __shfl_sync(0xffffffffu, tr, pick);
+    if (lane == 0) {
+      bc[0] = mn;
+      bc[1] = mx;
+      bc[2] = nv;
+      bc[3] = T0;
+    }
+  }
+  __syncthreads();
+  const uint32_t umin = bc[0], umax = bc[1], total_valid = bc[2], T0 = bc[3];
+
+  // Threshold: take keys > T and the first need_eq keys equal to T.
+  uint32_t T = 0u, need_eq = 0u;
+  if (total_valid > static_cast<uint32_t>(k)) {
+    bool filtered = false;
+    if (try_filter && T0 != 0u) {
+      uint32_t c = 0;  // T0 >= 1, so invalid keys never count
+#pragma unroll
+      for (int it = 0; it < kLoads; ++it) c += u[it] >= T0 ? 1u : 0u;
+      const uint32_t cw = __reduce_add_sync(0xffffffffu, c);
+      if (lane == 0) cs.wred[0][warp] = cw;  // wred[0] was last read before the cluster barrier
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t wv = cs.wred[0][lane];
+        uint32_t incl = wv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        cs.woff[lane] = incl - wv;
+        if (lane == 31) xchg[4] = incl;
+      }
+      cluster_sync_all();
+      if (warp == 0) {
+        const uint32_t cr = lane < C ? dsmem_ld(&xchg[4], lane) : 0u;
+        uint32_t incl = cr;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t base = __shfl_sync(0xffffffffu, incl - cr, static_cast<int>(r));
+        const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+        if (lane == 0) {
+          bc[4] = base;
+          bc[5] = total;
+        }
+      }
+      __syncthreads();
+      const uint32_t n_cand = bc[5];
+      if (n_cand >= static_cast<uint32_t>(k) && n_cand <= static_cast<uint32_t>(kBlkCandMax)) {
+        filtered = true;
+        // Candidates into CTA 0's shared memory (any order).
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t dst0 = dsmem_addr(cs.cand, 0);
+        uint32_t pos = bc[4] + cs.woff[warp] + incl - c;
+#pragma unroll
+        for (int it = 0; it < kLoads; ++it) {
+          if (u[it] >= T0) {
+            dsmem_st(dst0 + 4u * pos, u[it]);
+            ++pos;
+          }
+        }
+        cluster_sync_all();  // every candidate is in CTA 0
+        if (r == 0) {
+          radix_threshold([&](auto&& fn) {
+            for (int i = tid; i < static_cast<int>(n_cand); i += kThreads) fn(cs.cand[i]);
+          }, static_cast<uint32_t>(k), T0, umax, cs.S, T, need_eq);
+          if (tid == 0) {
+            xchg[8] = T;
+            xchg[9] = need_eq;
+          }
+        }
+        cluster_sync_all();  // CTA 0's threshold is published
+        if (tid == 0) {
+          bc[6] = dsmem_ld(&xchg[8], 0);
+          bc[7] = dsmem_ld(&xchg[9], 0);
+        }
+        __syncthreads();
+        T = bc[6];
+        need_eq = bc[7];
+      }
+    }
+    if (!filtered) {
+      const uint32_t span = umax - umin;
+      const int bits = span ? 32 - __clz(span) : 0;
+      int shift = bits > kDigit ? bits - kDigit : 0;
+      uint32_t pref = 0u, hmask = 0u, remaining = static_cast<uint32_t>(k);
+      for (int pass = 0; pass < 3; ++pass) {
+        for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < m; i += kThreads) {
+          const uint32_t uu = key[i];
+          const uint32_t d = uu - umin;
+          if (uu != 0u && (d & hmask) == pref) atomicAdd(&hist[(d >> shift) & (kBins - 1)], 1u);
+        }
+        cluster_sync_all();  // every local histogram is complete
+        // CTA r sums the bins of its slice [r * S, (r + 1) * S) over the cluster; a
+        // single CTA uses its own histogram as is.
+        const int Sn = kBins / C;
+        const uint32_t* totals = hist;
+        if (C > 1) {
+          uint32_t part = 0;
+          for (int bi = tid; bi < Sn; bi += kThreads) {
+            const int bin = static_cast<int>(r) * Sn + bi;
+            uint32_t v[kMaxC];
+#pragma unroll
+            for (int cc = 0; cc < kMaxC; ++cc) v[cc] = cc < C ? dsmem_ld(&hist[bin], cc) : 0u;
+            uint32_t sum = 0;
+#pragma unroll
+            for (int cc = 0; cc < kMaxC; ++cc) sum += v[cc];
+            tot[bin] = sum;
+            part += sum;
+          }
+          uint32_t slice_total;
+          block_excl_scan(part, warp_sums, &slice_total);
+          if (tid == 0) xchg[5] = slice_total;
+          totals = tot;
+        }
+        cluster_sync_all();  // slice sums complete; nobody reads a remote histogram any more
+        // The slice that holds the remaining-th largest key (slices of higher ranks
+        // hold higher digits), and the keys above it.
+        if (warp == 0) {
+          const uint32_t st = lane < C ? (C > 1 ? dsmem_ld(&xchg[5], lane) : 0u) : 0u;
+          uint32_t incl = st;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+            if (lane + o < 32) incl += y;
+          }
+          const uint32_t above = incl - st;
+          if (lane == 0) {
+            bc[8] = 0;
+            bc[9] = 0;
+          }
+          __syncwarp();
+          if (C > 1 && lane < C && above < remaining && above + st >= remaining) {
+            bc[8] = lane;
+            bc[9] = above;
+          }
+        }
+        __syncthreads();
+        const uint32_t target = bc[8] & static_cast<uint32_t>(C - 1);  // always a rank of this cluster
+        const uint32_t above_t = bc[9];
+        __syncthreads();
+        // Thread t owns kPer consecutive bins of the target slice counted from the top.
+        constexpr int kPer = kBins / kThreads;
+        uint32_t c4[kPer], own = 0;
+#pragma unroll
+        for (int it = 0; it < kPer; ++it) {
+          const int rank = tid * kPer + it;
+          c4[it] = 0;
+          if (rank < Sn) {
+            const int bin = static_cast<int>(target) * Sn + (Sn - 1 - rank);
+            c4[it] = C > 1 ? dsmem_ld(&totals[bin], target) : totals[bin];
+          }
+          own += c4[it];
+        }
+        uint32_t total;
+        uint32_t before = above_t + block_excl_scan(own, warp_sums, &total);
+#pragma unroll
+        for (int it = 0; it < kPer; ++it) {
+          const int rank = tid * kPer + it;
+          if (rank < Sn && before < remaining && before + c4[it] >= remaining) {
+            bc[10] = static_cast<uint32_t>(static_cast<int>(target) * Sn + (Sn - 1 - rank));
+            bc[11] = before;
+          }
+          before += c4[it];
+        }
+        __syncthreads();
+        remaining -= bc[11];
+        pref |= bc[10] << shift;
+        hmask = ~((1u << shift) - 1u);
+        __syncthreads();
+        if (shift == 0) break;
+        shift = shift > kDigit ? shift - kDigit : 0;
+      }
+      T = umin + pref;
+      need_eq = remaining;
+    }
+  }
+
+  // Warp-cooperative counts over this CTA's slice: warp w owns [w * wseg, (w + 1) * wseg).
+  const int wseg = ((m + 32 * 32 - 1) / (32 * 32)) * 32;
+  const int w0 = warp * wseg, w1 = min(m, w0 + wseg);
+  uint32_t gt = 0, eq = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t x = i < w1 ? key[i] : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, x > T));
+    eq += __popc(__ballot_sync(0xffffffffu, x == T && x != 0u));
+  }
+  if (lane == 0) {
+    wsel[warp] = gt;
+    weq[warp] = eq;
+  }
+  __syncthreads();
+  if (warp == 0) {  // per-warp prefix sums within the CTA
+    const uint32_t g = wsel[lane], e = weq[lane];
+    uint32_t gi = g, ei = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t yg = __shfl_up_sync(0xffffffffu, gi, o), ye = __shfl_up_sync(0xffffffffu, ei, o);
+      if (lane >= o) {
+        gi += yg;
+        ei += ye;
+      }
+    }
+    wsel[lane] = gi - g;  // gt keys in lower warps
+    weq[lane] = ei - e;   // equal keys in lower warps
+    if (lane == 31) {
+      xchg[6] = gi;
+      xchg[7] = ei;
+    }
+  }
+  cluster_sync_all();
+  if (warp == 0) {  // ties go to the lowest indices: CTA slices are in index order
+    const uint32_t g = lane < C ? dsmem_ld(&xchg[6], lane) : 0u;
+    const uint32_t e = lane < C ? dsmem_ld(&xchg[7], lane) : 0u;
+    uint32_t e_incl = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, e_incl, o);
+      if (lane >= o) e_incl += y;
+    }
+    const uint32_t e_before = e_incl - e;
+    const uint32_t take = need_eq > e_before ? min(e, need_eq - e_before) : 0u;
+    uint32_t s_incl = g + take;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, s_incl, o);
+      if (lane >= o) s_incl += y;
+    }
+    const uint32_t total_sel = __shfl_sync(0xffffffffu, s_incl, 31);
+    if (lane == static_cast<int>(r)) {
+      bc[12] = s_incl - (g + take);  // selections in lower CTAs
+      bc[13] = e_before;             // equal keys in lower CTAs
+    }
+    if (lane == 0) bc[14] = total_sel;
+  }
+  __syncthreads();
+  // This warp's equal keys that are taken: ranks [eq_base, eq_base + eq) among equals.
+  const uint32_t eq_base = bc[13] + weq[warp];
+  const uint32_t take_w = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
+  // Selections before this warp: lower CTAs, then lower warps (gt + their takes).
+  // Equal keys taken by lower warps of this CTA: min(eq before, remaining need).
+  const uint32_t eq_cta_before = bc[13];
+  const uint32_t need_here = need_eq > eq_cta_before ? need_eq - eq_cta_before : 0u;
+  const uint32_t taken_lower = min(weq[warp], need_here);
+  uint32_t o = bc[12] + wsel[warp] + taken_lower;
+  const uint32_t total_sel = bc[14];
+  int32_t* orow = out + static_cast<int64_t>(q) * k;
+  uint32_t eq_taken = 0;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t x = i < w1 ? key[i] : 0u;
+    const bool is_gt = x > T;
+    const bool is_eq = x == T && x != 0u;
+    const uint32_t eq_ball = __ballot_sync(0xffffffffu, is_eq);
+    const uint32_t eq_rank = eq_taken + __popc(eq_ball & lt_mask);
+    const bool sel = is_gt || (is_eq && eq_rank < take_w);
+    const uint32_t sel_ball = __ballot_sync(0xffffffffu, sel);
+    if (sel) {
+      const uint32_t pos = o + __popc(sel_ball & lt_mask);
+      if (pos < static_cast<uint32_t>(k)) orow[pos] = static_cast<int32_t>(lo + i);  // never past the row, whatever the counts say
+    }
+    o += __popc(sel_ball);
+    eq_taken += __popc(eq_ball);
+  }
+  if (r == 0)
+    for (int i = static_cast<int>(min(total_sel, static_cast<uint32_t>(k))) + tid; i < k; i += kThreads) orow[i] = -1;
+  cluster_sync_all();  // keep this CTA's shared memory alive until every remote read is done
+}
+
+constexpr size_t kClusterSmem = sizeof(ClusterShared);
+
+cudaError_t launch_cluster_topk(const float* keys, int64_t row_stride, const int64_t* seq_len, int Q,
+                                int n_q, int k, int C, int32_t* out, cudaStream_t stream) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(cluster_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kClusterSmem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(cluster_topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, Q, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kClusterSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, cluster_topk_kernel, keys, row_stride, seq_len, n_q, k, C, out);
+}
+
+// ---- pool top-k: one CTA per token, the row in registers --------------------
+//
+// A token's pool row holds 16384 scores (2048 blocks x 8 positions). Each of
+// 1024 threads keeps 16 consecutive ordered keys in registers (4 float4 loads
+// in flight at once), so the row is read once and no pass touches global
+// memory. Warp shuffles are the scarce resource here (one warp instruction per
+// clock per SM), so reductions use redux.sync and work that needs a shuffle
+// scan is done by one warp, not redundantly by all 32.
+//
+// The threshold search first narrows the row to a candidate set: T0 = the
+// median over warps of each warp's second-largest sample (one sample per
+// lane) sits near the 6% quantile, so usually between k and 2048 keys are
+// >= T0. Those candidates go to shared memory and the span-based 12-bit radix
+// select runs on them alone (two keys per thread at most, hence few
+// shared-memory atomics). When the count falls outside [k, 2048] (heavy ties,
+// adversarial orders) the radix select runs on all keys instead; the result is
+// the same either way, only the cost differs. The compaction is one block
+// prefix sum of each thread's count of keys above and equal to the threshold,
+// packed into one word (16 bits each; a row has at most 16384 of either).
+constexpr int kPoolRow = 16384;
+constexpr int kPoolThreads = 1024;
+constexpr int kPoolKeys = kPoolRow / kPoolThreads;  // 16 consecutive keys per thread
+constexpr int kCandMax = 2048;
 
 __global__ void __launch_bounds__(kPoolThreads, 1) pool_topk_kernel(const float* __restrict__ scores,
                                                                     const int32_t* __restrict__ pool, int k,
