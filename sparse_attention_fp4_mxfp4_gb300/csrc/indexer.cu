@@ -30,7 +30,7 @@
 namespace csa2 {
 namespace {
 
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kTileBytes = 16 * 576;     // one indexer page / 16 pool blocks
 constexpr int kThreads = 192;
 constexpr int kIdxPageBytes = 16 * 576;
@@ -82,7 +82,7 @@ __host__ __device__ constexpr int smem_bytes_for(int n_q, bool pool) {
 }
 
 template <bool kPool>
-__global__ void __launch_bounds__(kThreads, 3) indexer_kernel(const ScanParams P) {
+__global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int n_q = kPool ? 1 : P.n_q;
