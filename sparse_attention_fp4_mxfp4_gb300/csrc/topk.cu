@@ -266,11 +266,11 @@ __device__ __forceinline__ void radix_threshold(const Visit& visit, uint32_t k, 
   need_eq = remaining;
 }
 
-// ---- cluster version: the row lives in shared memory ------------------------
+// ---- cluster version: the row lives in registers -----------------------------
 //
 // A cluster of C CTAs (C <= 16) selects from one row; CTA r keeps elements
-// [r * chunk, (r + 1) * chunk) of the row in shared memory (and registers) as
-// ordered keys, so the row is read from global memory once.
+// [r * chunk, (r + 1) * chunk) of the row in registers as ordered keys (thread
+// t holds elements t + 1024 i), so the row is read from global memory once.
 //
 // The threshold search first narrows the row to a candidate set with samples:
 // each warp sorts one sample per lane and takes the j-th largest, j chosen so
@@ -281,24 +281,25 @@ __device__ __forceinline__ void radix_threshold(const Visit& visit, uint32_t k, 
 // rows, heavy ties) every pass runs over the whole row: each CTA builds a local
 // histogram, every CTA sums all C histograms through distributed shared memory
 // and derives the same threshold digit. Either way the result is the same.
-// The ordered compaction is warp cooperative: consecutive lanes take
-// consecutive elements, warps take consecutive ranges, so index order is kept
-// without bank conflicts. Control flow is uniform across the cluster: every
-// CTA executes every cluster barrier.
-constexpr int kChunk = 16384;  // elements per CTA
+// The ordered compaction counts, per (register slot i, warp), the keys above
+// and equal to the threshold with ballots; one prefix sum over those counts in
+// (i, warp) order, plus the counts of lower CTAs, gives every selected key its
+// output position in index order. Control flow is uniform across the cluster:
+// every CTA executes every cluster barrier.
+constexpr int kChunk = 16384;  // elements per CTA at most
 constexpr int kMaxC = 16;
+constexpr int kSlots = kChunk / kThreads;  // register slots per thread
 constexpr int kBlkCandMax = 8192;  // candidate set of the sample filter (in CTA 0)
 
 struct ClusterShared {
-  uint32_t key[kChunk];         // ordered keys of this CTA's slice
   SelectShared S;               // histogram and bin search
   uint32_t tot[kBins];          // cluster-wide histogram slice (whole-row passes)
   uint32_t cand[kBlkCandMax];   // CTA 0: the candidates of the whole row
   uint32_t wred[4][32];         // per warp: min, max, valid count, sample statistic
   uint32_t woff[32];            // per warp: offset of its candidates within the CTA
+  uint32_t cgt[kSlots][32];     // per (slot, warp): keys above T, then their prefix
+  uint32_t ceq[kSlots][32];     // per (slot, warp): keys equal to T, then their prefix
   uint32_t warp_sums[32];
-  uint32_t wsel[32];            // per-warp selection offsets
-  uint32_t weq[32];             // per-warp equal-key takes
   uint32_t xchg[16];            // read by other CTAs: 0-3 min/max/valid/sample median,
                                 // 4 candidate count, 5 slice total, 6-7 gt/eq counts,
                                 // 8-9 threshold and equal-key takes (CTA 0)
@@ -353,12 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
                                                                 int32_t* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t cs_raw[];
   ClusterShared& cs = *reinterpret_cast<ClusterShared*>(cs_raw);
-  uint32_t* key = cs.key;
   uint32_t* hist = cs.S.hist;
   uint32_t* tot = cs.tot;
   uint32_t* warp_sums = cs.warp_sums;
-  uint32_t* wsel = cs.wsel;
-  uint32_t* weq = cs.weq;
   uint32_t* xchg = cs.xchg;
   uint32_t* bc = cs.bc;
 
@@ -367,46 +365,39 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
   const int b = q / n_q, j = q % n_q;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t t = seq_len[b] - n_q + j;
-  int64_t n = t >= 0 ? (t + 8) / 8 : 0;
-  if (n > row_stride || n > static_cast<int64_t>(C) * kChunk) {
+  int64_t n64 = t >= 0 ? (t + 8) / 8 : 0;
+  if (n64 > row_stride || n64 > static_cast<int64_t>(C) * kChunk) {
     if (tid == 0 && r == 0) report(CSA2_ERR_DEVICE_BOUNDS, 311);
-    n = min(row_stride, static_cast<int64_t>(C) * kChunk);
+    n64 = min(row_stride, static_cast<int64_t>(C) * kChunk);
   }
-  const int64_t chunk = (n + C - 1) / C;
-  const int64_t lo = static_cast<int64_t>(r) * chunk;
-  const int64_t hi = min(n, lo + chunk);
-  const int m = hi > lo ? static_cast<int>(hi - lo) : 0;
+  const int n = static_cast<int>(n64);  // at most 16 * 16384
+  const int chunk = (n + C - 1) / C;
+  const int lo = static_cast<int>(r) * chunk;
+  const int m = max(0, min(n - lo, chunk));
   const float* row = keys + static_cast<int64_t>(q) * row_stride + lo;
 
   // Sample statistic: the j-th largest of a warp's 32 samples sits near the
-  // (j - 1/3) / (32 + 1/3) quantile; aim at 2k/n. Rows where that is above 1/2
-  // skip the sample filter.
-  // In integers (floating point here would be fp64, which this GPU runs
-  // slowly): j = floor((2k/n) * 97/3 + 5/6), filter only while 4k < n.
-  const bool try_filter = n > 4 * static_cast<int64_t>(k);
-  int jrank = n > 0 ? static_cast<int>((194 * static_cast<int64_t>(k) + 5 * n / 2) / (3 * n)) : 32;
+  // (j - 1/3) / (32 + 1/3) quantile; aim at 2k/n, j = floor((2k/n) 97/3 + 5/6),
+  // in integers. Rows where 2k/n >= 1/2 skip the sample filter.
+  const bool try_filter = n > 4 * k;
+  int jrank = n > 0 ? (194 * k + 5 * (n / 2)) / (3 * n) : 32;
   jrank = jrank < 1 ? 1 : (jrank > 32 ? 32 : jrank);
 
-  constexpr int kLoads = kChunk / kThreads;  // every load of a thread in flight at once
-  uint32_t u[kLoads];
+  uint32_t u[kSlots];
   {
-    float f[kLoads];
+    float f[kSlots];
 #pragma unroll
-    for (int it = 0; it < kLoads; ++it) {
+    for (int it = 0; it < kSlots; ++it) {
       const int i = tid + it * kThreads;
       f[it] = i < m ? row[i] : -INFINITY;
     }
 #pragma unroll
-    for (int it = 0; it < kLoads; ++it) {
-      const int i = tid + it * kThreads;
-      u[it] = ordered_key(f[it]);
-      if (i < m) key[i] = u[it];
-    }
+    for (int it = 0; it < kSlots; ++it) u[it] = ordered_key(f[it]);
   }
-  uint32_t smp = u[0], vmin = 0xFFFFFFFFu, vmax = 0u, nvalid = 0u;
+  const uint32_t smp = (lane & 1) ? u[kSlots / 2] : u[0];
+  uint32_t vmin = 0xFFFFFFFFu, vmax = 0u, nvalid = 0u;
 #pragma unroll
-  for (int it = 0; it < kLoads; ++it) {
-    if (it == ((tid * 7) & (kLoads - 1))) smp = u[it];
+  for (int it = 0; it < kSlots; ++it) {
     vmin = min(vmin, u[it] - 1u);  // invalid keys (0) wrap above every valid one
     vmax = max(vmax, u[it]);
     nvalid += u[it] != 0u ? 1u : 0u;
@@ -415,8 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
   vmin = __reduce_min_sync(0xffffffffu, vmin);
   vmax = __reduce_max_sync(0xffffffffu, vmax);
   nvalid = __reduce_add_sync(0xffffffffu, nvalid);
-  const uint32_t sorted = warp_sort_asc(smp, lane);
-  const uint32_t stat = __shfl_sync(0xffffffffu, sorted, 32 - jrank);
+  const uint32_t stat = __shfl_sync(0xffffffffu, warp_sort_asc(smp, lane), 32 - jrank);
   if (lane == 0) {
     cs.wred[0][warp] = vmin;
     cs.wred[1][warp] = vmax;
@@ -468,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
     if (try_filter && T0 != 0u) {
       uint32_t c = 0;  // T0 >= 1, so invalid keys never count
 #pragma unroll
-      for (int it = 0; it < kLoads; ++it) c += u[it] >= T0 ? 1u : 0u;
+      for (int it = 0; it < kSlots; ++it) c += u[it] >= T0 ? 1u : 0u;
       const uint32_t cw = __reduce_add_sync(0xffffffffu, c);
       if (lane == 0) cs.wred[0][warp] = cw;  // wred[0] was last read before the cluster barrier
       __syncthreads();
@@ -513,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
         const uint32_t dst0 = dsmem_addr(cs.cand, 0);
         uint32_t pos = bc[4] + cs.woff[warp] + incl - c;
 #pragma unroll
-        for (int it = 0; it < kLoads; ++it) {
+        for (int it = 0; it < kSlots; ++it) {
           if (u[it] >= T0) {
             dsmem_st(dst0 + 4u * pos, u[it]);
             ++pos;
@@ -547,26 +537,24 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
       for (int pass = 0; pass < 3; ++pass) {
         for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
         __syncthreads();
-        for (int i = tid; i < m; i += kThreads) {
-          const uint32_t uu = key[i];
+#pragma unroll
+        for (int it = 0; it < kSlots; ++it) {
+          const uint32_t uu = u[it];
           const uint32_t d = uu - umin;
           if (uu != 0u && (d & hmask) == pref) atomicAdd(&hist[(d >> shift) & (kBins - 1)], 1u);
         }
         cluster_sync_all();  // every local histogram is complete
-        // CTA r sums the bins of its slice [r * S, (r + 1) * S) over the cluster; a
-        // single CTA uses its own histogram as is.
-        const int Sn = kBins / C;
+        // CTA r sums the bins of its slice [r * Sn, (r + 1) * Sn) over the cluster
+        // (the last slice may be short); a single CTA uses its own histogram as is.
+        const int Sn = (kBins + C - 1) / C;
         const uint32_t* totals = hist;
         if (C > 1) {
           uint32_t part = 0;
           for (int bi = tid; bi < Sn; bi += kThreads) {
             const int bin = static_cast<int>(r) * Sn + bi;
-            uint32_t v[kMaxC];
-#pragma unroll
-            for (int cc = 0; cc < kMaxC; ++cc) v[cc] = cc < C ? dsmem_ld(&hist[bin], cc) : 0u;
+            if (bin >= kBins) break;
             uint32_t sum = 0;
-#pragma unroll
-            for (int cc = 0; cc < kMaxC; ++cc) sum += v[cc];
+            for (int cc = 0; cc < C; ++cc) sum += dsmem_ld(&hist[bin], cc);
             tot[bin] = sum;
             part += sum;
           }
@@ -598,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
           }
         }
         __syncthreads();
-        const uint32_t target = bc[8] & static_cast<uint32_t>(C - 1);  // always a rank of this cluster
+        const uint32_t target = min(bc[8], static_cast<uint32_t>(C - 1));  // always a rank of this cluster
         const uint32_t above_t = bc[9];
         __syncthreads();
         // Thread t owns kPer consecutive bins of the target slice counted from the top.
@@ -608,10 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
         for (int it = 0; it < kPer; ++it) {
           const int rank = tid * kPer + it;
           c4[it] = 0;
-          if (rank < Sn) {
-            const int bin = static_cast<int>(target) * Sn + (Sn - 1 - rank);
-            c4[it] = C > 1 ? dsmem_ld(&totals[bin], target) : totals[bin];
-          }
+          const int bin = static_cast<int>(target) * Sn + (Sn - 1 - rank);
+          if (rank < Sn && bin < kBins) c4[it] = C > 1 ? dsmem_ld(&totals[bin], target) : totals[bin];
           own += c4[it];
         }
         uint32_t total;
@@ -638,24 +624,29 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
     }
   }
 
-  // Warp-cooperative counts over this CTA's slice: warp w owns [w * wseg, (w + 1) * wseg).
-  const int wseg = ((m + 32 * 32 - 1) / (32 * 32)) * 32;
-  const int w0 = warp * wseg, w1 = min(m, w0 + wseg);
-  uint32_t gt = 0, eq = 0;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint32_t x = i < w1 ? key[i] : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, x > T));
-    eq += __popc(__ballot_sync(0xffffffffu, x == T && x != 0u));
-  }
-  if (lane == 0) {
-    wsel[warp] = gt;
-    weq[warp] = eq;
+  // Ordered compaction. Keys equal to T are all valid when T > 0; when T = 0
+  // every valid key is taken and need_eq = 0 takes no "equal" (invalid) key.
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int it = 0; it < kSlots; ++it) {
+    const uint32_t gb = __ballot_sync(0xffffffffu, u[it] > T);
+    const uint32_t eb = __ballot_sync(0xffffffffu, u[it] == T);
+    if (lane == 0) {
+      cs.cgt[it][warp] = __popc(gb);
+      cs.ceq[it][warp] = __popc(eb);
+    }
   }
   __syncthreads();
-  if (warp == 0) {  // per-warp prefix sums within the CTA
-    const uint32_t g = wsel[lane], e = weq[lane];
-    uint32_t gi = g, ei = e;
+  if (warp == 0) {  // exclusive prefixes over (slot, warp) order; lane l takes slot l / 2's half
+    constexpr int kPer = kSlots * 32 / 32;  // entries per lane
+    uint32_t gs = 0, es = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = lane * kPer + i;
+      gs += cs.cgt[idx / 32][idx % 32];
+      es += cs.ceq[idx / 32][idx % 32];
+    }
+    uint32_t gi = gs, ei = es;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t yg = __shfl_up_sync(0xffffffffu, gi, o), ye = __shfl_up_sync(0xffffffffu, ei, o);
@@ -664,8 +655,16 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
         ei += ye;
       }
     }
-    wsel[lane] = gi - g;  // gt keys in lower warps
-    weq[lane] = ei - e;   // equal keys in lower warps
+    uint32_t gr = gi - gs, er = ei - es;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = lane * kPer + i;
+      const uint32_t g = cs.cgt[idx / 32][idx % 32], e = cs.ceq[idx / 32][idx % 32];
+      cs.cgt[idx / 32][idx % 32] = gr;
+      cs.ceq[idx / 32][idx % 32] = er;
+      gr += g;
+      er += e;
+    }
     if (lane == 31) {
       xchg[6] = gi;
       xchg[7] = ei;
@@ -675,56 +674,39 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
   if (warp == 0) {  // ties go to the lowest indices: CTA slices are in index order
     const uint32_t g = lane < C ? dsmem_ld(&xchg[6], lane) : 0u;
     const uint32_t e = lane < C ? dsmem_ld(&xchg[7], lane) : 0u;
-    uint32_t e_incl = e;
+    uint32_t g_incl = g, e_incl = e;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, e_incl, o);
-      if (lane >= o) e_incl += y;
+      const uint32_t yg = __shfl_up_sync(0xffffffffu, g_incl, o), ye = __shfl_up_sync(0xffffffffu, e_incl, o);
+      if (lane >= o) {
+        g_incl += yg;
+        e_incl += ye;
+      }
     }
-    const uint32_t e_before = e_incl - e;
-    const uint32_t take = need_eq > e_before ? min(e, need_eq - e_before) : 0u;
-    uint32_t s_incl = g + take;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, s_incl, o);
-      if (lane >= o) s_incl += y;
-    }
-    const uint32_t total_sel = __shfl_sync(0xffffffffu, s_incl, 31);
+    const uint32_t gt_all = __shfl_sync(0xffffffffu, g_incl, 31);
+    const uint32_t eq_all = __shfl_sync(0xffffffffu, e_incl, 31);
     if (lane == static_cast<int>(r)) {
-      bc[12] = s_incl - (g + take);  // selections in lower CTAs
-      bc[13] = e_before;             // equal keys in lower CTAs
+      bc[12] = g_incl - g;  // keys above T in lower CTAs
+      bc[13] = e_incl - e;  // keys equal to T in lower CTAs
     }
-    if (lane == 0) bc[14] = total_sel;
+    if (lane == 0) bc[14] = gt_all + min(eq_all, need_eq);  // keys selected in the whole row
   }
   __syncthreads();
-  // This warp's equal keys that are taken: ranks [eq_base, eq_base + eq) among equals.
-  const uint32_t eq_base = bc[13] + weq[warp];
-  const uint32_t take_w = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
-  // Selections before this warp: lower CTAs, then lower warps (gt + their takes).
-  // Equal keys taken by lower warps of this CTA: min(eq before, remaining need).
-  const uint32_t eq_cta_before = bc[13];
-  const uint32_t need_here = need_eq > eq_cta_before ? need_eq - eq_cta_before : 0u;
-  const uint32_t taken_lower = min(weq[warp], need_here);
-  uint32_t o = bc[12] + wsel[warp] + taken_lower;
-  const uint32_t total_sel = bc[14];
+  const uint32_t gt_cta = bc[12], eq_cta = bc[13], total_sel = bc[14];
   int32_t* orow = out + static_cast<int64_t>(q) * k;
-  uint32_t eq_taken = 0;
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint32_t x = i < w1 ? key[i] : 0u;
-    const bool is_gt = x > T;
-    const bool is_eq = x == T && x != 0u;
-    const uint32_t eq_ball = __ballot_sync(0xffffffffu, is_eq);
-    const uint32_t eq_rank = eq_taken + __popc(eq_ball & lt_mask);
-    const bool sel = is_gt || (is_eq && eq_rank < take_w);
-    const uint32_t sel_ball = __ballot_sync(0xffffffffu, sel);
-    if (sel) {
-      const uint32_t pos = o + __popc(sel_ball & lt_mask);
-      if (pos < static_cast<uint32_t>(k)) orow[pos] = static_cast<int32_t>(lo + i);  // never past the row, whatever the counts say
+#pragma unroll
+  for (int it = 0; it < kSlots; ++it) {
+    const bool is_gt = u[it] > T;
+    const bool is_eq = u[it] == T;
+    const uint32_t gb = __ballot_sync(0xffffffffu, is_gt);
+    const uint32_t eb = __ballot_sync(0xffffffffu, is_eq);
+    const uint32_t eq_before = eq_cta + cs.ceq[it][warp] + __popc(eb & lt_mask);
+    const bool take = is_gt || (is_eq && eq_before < need_eq);
+    if (take) {
+      const uint32_t gt_before = gt_cta + cs.cgt[it][warp] + __popc(gb & lt_mask);
+      const uint32_t pos = gt_before + min(eq_before, need_eq);
+      if (pos < static_cast<uint32_t>(k)) orow[pos] = lo + tid + it * kThreads;  // never past the row
     }
-    o += __popc(sel_ball);
-    eq_taken += __popc(eq_ball);
   }
   if (r == 0)
     for (int i = static_cast<int>(min(total_sel, static_cast<uint32_t>(k))) + tid; i < k; i += kThreads) orow[i] = -1;
@@ -967,7 +949,10 @@ cudaError_t launch_block_topk(const float* block_max, const int64_t* seq_len, in
                               int64_t max_blocks, int32_t* pool, cudaStream_t stream) {
   const int Q = B * n_q;
   if (Q == 0) return cudaSuccess;
-  const int64_t C = (max_blocks + kChunk - 1) / kChunk;
+  // Half-full CTAs (8192 elements) while few rows make few 16-CTA clusters
+  // (a cluster of 16 needs 16 free SMs of one GPC), else full ones.
+  int64_t C = (max_blocks + 8191) / 8192;
+  if (C > 16 || static_cast<int64_t>(Q) * C > 64) C = (max_blocks + kChunk - 1) / kChunk;
   if (C <= 16) {
     const cudaError_t e = launch_cluster_topk(block_max, max_blocks, seq_len, Q, n_q, 2048,
                                               static_cast<int>(C < 1 ? 1 : C), pool, stream);
