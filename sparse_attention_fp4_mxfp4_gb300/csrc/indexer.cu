@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
   if (warp == 4) {
     // ---- producer (whole warp: lookups in parallel, one bulk copy per lane) ----
     int32_t next_pages = -1;  // scan: page id of tile (i & ~31) + lane
-    for (int64_t i = 0; i < n_tiles; ++i) {
-      const int s = static_cast<int>(i % kStages);
-      const int64_t u = i / kStages;
+    const int nt = static_cast<int>(n_tiles);
+    int s = 0, u = 0;  // stage of tile i and the round of the ring it is in (i = u * kStages + s)
+    for (int i = 0; i < nt; ++i, s = (s + 1 == kStages) ? 0 : s + 1, u += (s == 0) ? 1 : 0) {
       int go = 1;
       if (lane == 0) {
         if (u > 0 && !mbar_wait(empty0 + 8 * s, (u - 1) & 1, 201, abort_flag)) *abort_flag = 1;
@@ -262,13 +262,15 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
     if (lane == 0) {
       const uint32_t idesc = idesc_mxf4nvf4(128, n_cols);
       const uint32_t qb = smem_u32(qbuf);
-      int64_t issued = 0;
-      for (int64_t i = 0; i < n_tiles; ++i) {
-        const int s = static_cast<int>(i % kStages);
+      const bool two = plan.nacc == 2;
+      const int nt = static_cast<int>(n_tiles);
+      int issued = 0;
+      int s = 0, u = 0;
+      for (int i = 0; i < nt; ++i, s = (s + 1 == kStages) ? 0 : s + 1, u += (s == 0) ? 1 : 0) {
         const int a = static_cast<int>(i & 1);
-        const int acc = static_cast<int>(i % plan.nacc);
-        const int64_t ub = i / plan.nacc;
-        if (!mbar_wait(full0 + 8 * s, (i / kStages) & 1, 210, abort_flag)) { *abort_flag = 1; break; }
+        const int acc = two ? (i & 1) : 0;
+        const int ub = two ? (i >> 1) : i;
+        if (!mbar_wait(full0 + 8 * s, u & 1, 210, abort_flag)) { *abort_flag = 1; break; }
         if (!mbar_wait(sfull0 + 8 * a, (i >> 1) & 1, 211, abort_flag)) { *abort_flag = 1; break; }
         if (ub > 0 && !mbar_wait(dempty0 + 8 * acc, (ub - 1) & 1, 212, abort_flag)) { *abort_flag = 1; break; }
         if (*abort_flag) break;
@@ -289,14 +291,15 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
       // Before TMEM is released, the last MMAs must have finished (they have on
       // the normal path: the epilogue waited for them).
       if (issued > 0)
-        mbar_wait(dfull0 + 8 * ((issued - 1) % plan.nacc), ((issued - 1) / plan.nacc) & 1, 213);
+        mbar_wait(dfull0 + 8 * (two ? ((issued - 1) & 1) : 0), (two ? ((issued - 1) >> 1) : (issued - 1)) & 1, 213);
     }
   } else {
     // ---- scales to TMEM + epilogue (warps 0-3, thread t <-> row t) ----
     uint32_t valid_rows[2] = {0, 0};  // per 8-row group, tiles i and i-1
-    auto epilogue = [&](int64_t i) -> bool {
-      const int acc = static_cast<int>(i % plan.nacc);
-      if (!mbar_wait(dfull0 + 8 * acc, (i / plan.nacc) & 1, 221, abort_flag)) return false;
+    const bool two = plan.nacc == 2;
+    auto epilogue = [&](int i) -> bool {
+      const int acc = two ? (i & 1) : 0;
+      if (!mbar_wait(dfull0 + 8 * acc, (two ? (i >> 1) : i) & 1, 221, abort_flag)) return false;
       tc_fence_after();
       const int64_t tile = first_tile + i * tile_stride;
       const bool row_ok = (valid_rows[i & 1] >> (tid >> 3)) & 1u;
@@ -309,13 +312,14 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
           mbar_arrive(dempty0 + 8 * acc);
         }
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        const float* wj = wsm + jj * 32;
+        const float4* wj = reinterpret_cast<const float4*>(wsm + jj * 32);  // 16-byte aligned
 #pragma unroll
         for (int h = 0; h < 32; h += 4) {
-          s0 = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.f), s0);
-          s1 = fmaf(wj[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
-          s2 = fmaf(wj[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
-          s3 = fmaf(wj[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
+          const float4 wv = wj[h >> 2];
+          s0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), s0);
+          s1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
+          s2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
+          s3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
         }
         const float s = (s0 + s1) + (s2 + s3);
         if (!kPool) {
@@ -337,10 +341,11 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
     };
     bool ok = true;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    for (int64_t i = 0; i < n_tiles && ok; ++i) {
-      const int s = static_cast<int>(i % kStages);
+    const int nt = static_cast<int>(n_tiles);
+    int s = 0, u = 0;
+    for (int i = 0; i < nt && ok; ++i, s = (s + 1 == kStages) ? 0 : s + 1, u += (s == 0) ? 1 : 0) {
       const int a = static_cast<int>(i & 1);
-      if (!mbar_wait(full0 + 8 * s, (i / kStages) & 1, 231, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(full0 + 8 * s, u & 1, 231, abort_flag)) { ok = false; break; }
       valid_rows[a] = stage_mask[s];
       // Row t's 8 scale bytes: blocks 0-3 feed the first K = 64 step, 4-7 the second.
       const uint8_t* grp = stages + s * kTileBytes + (tid >> 3) * 576;
