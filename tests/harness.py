@@ -204,17 +204,35 @@ class Runner:
         # CTAs (plus a merge kernel) only while there are fewer tokens than SMs.
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         self.attn_launches = 1 if min(5, max(1, sms // Q)) == 1 else 2
+        self.side = None
 
     def step(self, mark=None):
+        """The window-ring appends and the indexer-query quantisations do not
+        depend on the main append, so they run on two side streams forked from
+        the current one and joined before their first consumer."""
         csa2, S, c = self.csa2, self.S, self.S.cache
         mark = mark or (lambda name: None)
         n = 0
-        append_step(S)
+        main = torch.cuda.current_stream()
+        if self.side is None:
+            self.side = (torch.cuda.Stream(device=main.device), torch.cuda.Stream(device=main.device))
+        s_swa, s_q = self.side
+        s_swa.wait_stream(main)
+        s_q.wait_stream(main)
+        with torch.cuda.stream(s_swa):
+            for li in range(len(S.layers)):
+                csa2.csa2_append_swa(S.step_swa[li], S.step_ring_idx[li], S.step_pos, c.rings)
+        with torch.cuda.stream(s_q):
+            for L in S.layers:
+                if L.kind in ("full", "reindex"):
+                    csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
+                    n += 1
+        csa2.csa2_append_kv(S.step_latent, S.step_idx_key, S.step_seq, S.step_pos, c.block_table, c.main_pages,
+                            c.idx_pages)
         n += 1 + len(S.layers)
+        main.wait_stream(s_q)
+        swa_joined = False
         for li, L in enumerate(S.layers):
-            if L.kind in ("full", "reindex"):
-                csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
-                n += 1
             if L.kind == "full":
                 mark("scan0")
                 csa2.csa2_indexer_scan(L.q_codes, L.q_scales, L.w, S.seq_len, S.N, c.block_table, c.n_pages,
@@ -231,6 +249,9 @@ class Runner:
                                           c.idx_pages, pool, self.topk, self.rws)
                 mark("rescore1")
                 n += 2
+            if not swa_joined:
+                main.wait_stream(s_swa)
+                swa_joined = True
             mark("attn0")
             csa2.csa2_sparse_attn(L.q, self.topk, S.seq_len, c.block_table, c.n_pages, c.main_pages, c.rings,
                                   L.ring_idx, self.out[li], self.lse[li], self.ws)
