@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
     const int32_t* __restrict__ seq_idx, const int64_t* __restrict__ pos, int T,
     const int32_t* __restrict__ block_table, int B, int max_pages, int64_t n_pages,
     uint8_t* __restrict__ main_pages, uint8_t* __restrict__ idx_pages) {
+  griddep_wait();
+  griddep_launch();
   const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (tok >= T) return;
@@ -70,6 +72,8 @@ __global__ void __launch_bounds__(256) append_swa_kernel(const uint16_t* __restr
                                                          const int64_t* __restrict__ pos, int T,
                                                          int64_t n_rings,
                                                          uint8_t* __restrict__ rings) {
+  griddep_wait();
+  griddep_launch();
   const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (tok >= T) return;
@@ -94,6 +98,8 @@ __global__ void __launch_bounds__(256) append_swa_kernel(const uint16_t* __restr
 
 __global__ void quant_mxfp4_kernel(const uint16_t* __restrict__ x, int64_t nblocks,
                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  griddep_wait();
+  griddep_launch();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= nblocks) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + 16 * i);
@@ -150,27 +156,24 @@ cudaError_t launch_append_kv(const void* latent, const void* idx_key, const int3
                              int max_pages, int64_t n_pages, uint8_t* main_pages,
                              uint8_t* idx_pages, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  append_kv_kernel<<<(T + 7) / 8, 256, 0, stream>>>(
-      static_cast<const uint16_t*>(latent), static_cast<const uint16_t*>(idx_key), seq_idx, pos, T,
-      block_table, B, max_pages, n_pages, main_pages, idx_pages);
-  return cudaGetLastError();
+  return launch_pdl(append_kv_kernel, dim3((T + 7) / 8), dim3(256), 0, stream, 0,
+                    static_cast<const uint16_t*>(latent), static_cast<const uint16_t*>(idx_key), seq_idx, pos, T,
+                    block_table, B, max_pages, n_pages, main_pages, idx_pages);
 }
 
 cudaError_t launch_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, int T,
                               int64_t n_rings, uint8_t* rings, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  append_swa_kernel<<<(T + 7) / 8, 256, 0, stream>>>(static_cast<const uint16_t*>(x), ring_idx, pos,
-                                                     T, n_rings, rings);
-  return cudaGetLastError();
+  return launch_pdl(append_swa_kernel, dim3((T + 7) / 8), dim3(256), 0, stream, 0,
+                    static_cast<const uint16_t*>(x), ring_idx, pos, T, n_rings, rings);
 }
 
 cudaError_t launch_quant_mxfp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales,
                                cudaStream_t stream) {
   const int64_t nb = n / 16;
   if (nb == 0) return cudaSuccess;
-  quant_mxfp4_kernel<<<static_cast<unsigned>((nb + 255) / 256), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(x), nb, codes, scales);
-  return cudaGetLastError();
+  return launch_pdl(quant_mxfp4_kernel, dim3(static_cast<unsigned>((nb + 255) / 256)), dim3(256), 0, stream, 0,
+                    static_cast<const uint16_t*>(x), nb, codes, scales);
 }
 
 cudaError_t launch_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t n,

@@ -110,15 +110,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
   const uint32_t sfull = smem_u32(&bars[4]), drain = smem_u32(&bars[5]);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x;
-  const int q = blockIdx.y;
-  const int b = q / P.n_q, jq = q % P.n_q;
-  const int64_t N = P.seq_len[b];
-  const int64_t t = N - P.n_q + jq;
-  const int per = kChunks / P.nsplit, rem = kChunks % P.nsplit;
-  const int c0 = split * per + (split < rem ? split : rem);
-  const int nc = per + (split < rem ? 1 : 0);
-
   if (tid == 0) {
     mbar_init(kfull_lo, kGdThreads);
     mbar_init(kfull_hi, kGdThreads);
@@ -134,6 +125,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
     lsum[tid] = 0.f;
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 512);
+  griddep_wait();  // everything below may read what earlier kernels wrote
+  griddep_launch();
+  const int split = blockIdx.x;
+  const int q = blockIdx.y;
+  const int b = q / P.n_q, jq = q % P.n_q;
+  const int64_t N = P.seq_len[b];
+  const int64_t t = N - P.n_q + jq;
+  const int per = kChunks / P.nsplit, rem = kChunks % P.nsplit;
+  const int c0 = split * per + (split < rem ? split : rem);
+  const int nc = per + (split < rem ? 1 : 0);
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -465,6 +467,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
                                                            const float2* __restrict__ stats, int nsplit,
                                                            int out_dtype, void* __restrict__ out,
                                                            float* __restrict__ lse) {
+  griddep_wait();
+  griddep_launch();
   const int q = blockIdx.x;
   const int h = blockIdx.y;
   const int tid = threadIdx.x;
@@ -575,12 +579,12 @@ cudaError_t launch_sparse_attn(const void* q, const int32_t* topk, const int64_t
   const size_t part_bytes = static_cast<size_t>(Q) * kChunks * 64 * 512 * sizeof(float);
   p.part = static_cast<float*>(ws);
   p.stats = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + ((part_bytes + 255) & ~size_t(255)));
-  attn_kernel<<<dim3(static_cast<unsigned>(p.nsplit), static_cast<unsigned>(Q)), kThreads, kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(attn_kernel, dim3(static_cast<unsigned>(p.nsplit), static_cast<unsigned>(Q)),
+                             dim3(kThreads), kSmemBytes, stream, 0, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  attn_combine_kernel<<<dim3(static_cast<unsigned>(Q), 64), 256, 0, stream>>>(p.part, p.stats, p.nsplit, out_dtype,
-                                                                              out, lse);
-  return cudaGetLastError();
+  return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(Q), 64), dim3(256), 0, stream, 0,
+                    static_cast<const float*>(p.part), static_cast<const float2*>(p.stats), p.nsplit, out_dtype,
+                    out, lse);
 }
 
 }  // namespace csa2

@@ -104,6 +104,22 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
   const uint32_t dfull0 = smem_u32(&bars[2 * kStages + 2]), dempty0 = smem_u32(&bars[2 * kStages + 4]);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sfull0 + 8 * i, 128);
+      mbar_init(dfull0 + 8 * i, 1);
+      mbar_init(dempty0 + 8 * i, 128);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), plan.ncols);
+  griddep_wait();  // everything below may read what earlier kernels wrote
+  griddep_launch();
   int b, jq = 0;  // sequence, query token (pool mode)
   int64_t first_tile, n_tiles, tile_stride;
   if (kPool) {
@@ -127,20 +143,6 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
     n_tiles = 0;
   }
 
-  if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(sfull0 + 8 * i, 128);
-      mbar_init(dfull0 + 8 * i, 1);
-      mbar_init(dempty0 + 8 * i, 128);
-    }
-    *abort_flag = 0;
-    mbar_init_fence();
-  }
-  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), plan.ncols);
 
   // Query operand: packed E2M1 codes of the CTA's query tokens, rows
   // n = token * 32 + head, in core-matrix order [n / 8][chunk][n % 8][16 B].
@@ -382,8 +384,7 @@ cudaError_t launch(const ScanParams& p, dim3 grid, int n_q, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
-  indexer_kernel<kPool><<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(indexer_kernel<kPool>, grid, dim3(kThreads), smem, stream, 0, p);
 }
 
 int num_sms() {

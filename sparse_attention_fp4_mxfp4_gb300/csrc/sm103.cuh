@@ -118,6 +118,42 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------------
+// Kernels of this library are launched so that a kernel may start while the
+// previous kernel of its stream is finishing. A kernel does only local setup
+// (barriers, tensor memory) before griddep_wait(), which returns once every
+// preceding kernel has completed and its writes are visible; it then lets the
+// next kernel start launching with griddep_launch(). Without the launch
+// attribute both are no-ops.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launches a kernel with programmatic stream serialisation (and, when
+// cluster_x > 0, a cluster of cluster_x CTAs along x).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  unsigned n = 1;
+  if (cluster_x > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- tcgen05: tensor memory ----------------------------------------------------
 // Must be executed by one full warp. Writes the TMEM base address to *slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {

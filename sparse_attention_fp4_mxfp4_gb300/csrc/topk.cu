@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __res
                                                               const int64_t* __restrict__ seq_len,
                                                               int n_q, int k,
                                                               int32_t* __restrict__ out) {
+  griddep_wait();
+  griddep_launch();
   __shared__ uint32_t hist[2048];
   __shared__ uint32_t warp_sums[32];
   __shared__ uint32_t s_sel[2];
@@ -360,6 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
   uint32_t* xchg = cs.xchg;
   uint32_t* bc = cs.bc;
 
+  griddep_wait();
+  griddep_launch();
   const uint32_t r = cluster_rank();
   const int q = blockIdx.y;
   const int b = q / n_q, j = q % n_q;
@@ -728,19 +732,8 @@ cudaError_t launch_cluster_topk(const float* keys, int64_t row_stride, const int
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, Q, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kClusterSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, cluster_topk_kernel, keys, row_stride, seq_len, n_q, k, C, out);
+  return launch_pdl(cluster_topk_kernel, dim3(C, Q, 1), dim3(kThreads), kClusterSmem, stream,
+                    static_cast<unsigned>(C), keys, row_stride, seq_len, n_q, k, C, out);
 }
 
 // ---- pool top-k: one CTA per token, the row in registers --------------------
@@ -776,6 +769,8 @@ __global__ void __launch_bounds__(kPoolThreads, 1) pool_topk_kernel(const float*
   __shared__ uint32_t red[7 * 32];  // per-warp values; every use has its own 32 slots
   __shared__ uint32_t misc[4];      // candidate count, T0, packed selection total
 
+  griddep_wait();
+  griddep_launch();
   const int q = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float4* row = reinterpret_cast<const float4*>(scores + static_cast<int64_t>(q) * kPoolRow);
@@ -959,8 +954,8 @@ cudaError_t launch_block_topk(const float* block_max, const int64_t* seq_len, in
     if (e == cudaSuccess || C <= 8) return e;
     cudaGetLastError();  // a 16-CTA cluster may not fit this GPU: use the global-memory select
   }
-  radix_topk_kernel<<<Q, kThreads, 0, stream>>>(block_max, max_blocks, seq_len, n_q, 2048, pool);
-  return cudaGetLastError();
+  return launch_pdl(radix_topk_kernel, dim3(Q), dim3(kThreads), 0, stream, 0, block_max, max_blocks, seq_len, n_q,
+                    2048, pool);
 }
 
 cudaError_t launch_pool_topk(const float* scores, const int64_t* seq_len, int B, int n_q,
@@ -968,8 +963,7 @@ cudaError_t launch_pool_topk(const float* scores, const int64_t* seq_len, int B,
   (void)seq_len;  // causality is already in the scores: masked slots are -inf
   const int Q = B * n_q;
   if (Q == 0) return cudaSuccess;
-  pool_topk_kernel<<<Q, kPoolThreads, 0, stream>>>(scores, pool, 512, topk);
-  return cudaGetLastError();
+  return launch_pdl(pool_topk_kernel, dim3(Q), dim3(kPoolThreads), 0, stream, 0, scores, pool, 512, topk);
 }
 
 }  // namespace csa2
