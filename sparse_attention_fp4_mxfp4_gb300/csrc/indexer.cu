@@ -72,13 +72,14 @@ __host__ __device__ constexpr TmemPlan tmem_plan(int n_q) {
 
 // Pool rescore: per pool slot of the CTA's tiles, the source (page * 16 + block
 // in page, or kNoSlot) and the number of causal positions in the block.
-constexpr int kPoolSlots = 2048;
 constexpr uint32_t kNoSlot = 0xFFFFFFFFu;
-constexpr int kPoolTableBytes = kPoolSlots * 5;
 
-__host__ __device__ constexpr int smem_bytes_for(int n_q, bool pool) {
+__host__ __device__ constexpr int pool_table_bytes(int pool_tiles) { return (pool_tiles * 16 * 5 + 15) & ~15; }
+
+// pool_tiles: tiles per CTA in pool mode (sizes the slot table), 0 for the scan.
+__host__ __device__ constexpr int smem_bytes_for(int n_q, int pool_tiles) {
   return 1024 /*align*/ + kStages * kTileBytes + 32 * n_q * 64 /*q operand*/ + 2048 /*barriers, w*/ +
-         (pool ? kPoolTableBytes : 0);
+         pool_table_bytes(pool_tiles);
 }
 
 template <bool kPool>
@@ -96,8 +97,8 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 196);
   uint32_t* stage_mask = reinterpret_cast<uint32_t*>(misc + 200);  // kStages words
   float* wsm = reinterpret_cast<float*>(misc + 256);                 // n_cols floats
-  uint32_t* slot_src = reinterpret_cast<uint32_t*>(misc + 2048);      // pool mode: [n_tiles * 16]
-  uint8_t* slot_n = misc + 2048 + kPoolSlots * 4;                     // pool mode: [n_tiles * 16]
+  uint32_t* slot_src = reinterpret_cast<uint32_t*>(misc + 2048);      // pool mode: [tiles_per_cta * 16]
+  uint8_t* slot_n = misc + 2048 + (kPool ? P.tiles_per_cta * 16 * 4 : 0);  // pool mode: [tiles_per_cta * 16]
 
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[kStages]);
   const uint32_t sfull0 = smem_u32(&bars[2 * kStages]);
@@ -374,13 +375,13 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
 
 template <bool kPool>
 cudaError_t launch(const ScanParams& p, dim3 grid, int n_q, cudaStream_t stream) {
-  const int smem = smem_bytes_for(kPool ? 1 : n_q, kPool);
+  const int smem = smem_bytes_for(kPool ? 1 : n_q, kPool ? p.tiles_per_cta : 0);
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(indexer_kernel<kPool>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes_for(kPool ? 1 : 8, kPool));
+                                         smem_bytes_for(kPool ? 1 : 8, kPool ? 128 : 0));
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
@@ -401,8 +402,8 @@ int num_sms() {
 }
 
 // Resident CTAs per SM, bounded by shared memory and TMEM columns.
-int ctas_per_sm(int n_q, bool pool) {
-  const int by_smem = (228 * 1024) / (smem_bytes_for(n_q, pool) + 1024);
+int ctas_per_sm(int n_q, int pool_tiles) {
+  const int by_smem = (228 * 1024) / (smem_bytes_for(n_q, pool_tiles) + 1024);
   const int by_tmem = 512 / static_cast<int>(tmem_plan(n_q).ncols);
   return std::max(1, std::min(by_smem, by_tmem));
 }
@@ -443,7 +444,7 @@ cudaError_t launch_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales,
   p.block_max = block_max;
   p.max_blocks = max_blocks;
   const int64_t pages = (max_ctx + 127) / 128;
-  const int64_t target = static_cast<int64_t>(ctas_per_sm(n_q, false)) * num_sms();
+  const int64_t target = static_cast<int64_t>(ctas_per_sm(n_q, 0)) * num_sms();
   const int64_t per_seq = std::max<int64_t>(1, std::min<int64_t>(pages, (target + B - 1) / B));
   return launch<false>(p, dim3(static_cast<unsigned>(per_seq), B), n_q, stream);
 }
@@ -468,10 +469,17 @@ cudaError_t launch_pool_scores(const uint8_t* q_codes, const uint8_t* q_scales, 
   p.idx_pages = idx_pages;
   p.pool = pool;
   p.scores = scores;
-  const int64_t target = static_cast<int64_t>(ctas_per_sm(1, true)) * num_sms();
-  int splits = static_cast<int>(std::min<int64_t>(128, std::max<int64_t>(1, (target + Q - 1) / Q)));
-  const int per = (128 + splits - 1) / splits;
-  splits = (128 + per - 1) / per;
+  // The 128 tiles of a token are cut into equal runs so that all CTAs are
+  // resident at once (one wave) where the batch allows it; a run's slot table
+  // is sized to the run, so short runs leave room for more CTAs per SM.
+  int splits = 1, per = 128;
+  for (int cps = 4; cps >= 1; --cps) {
+    const int64_t target = static_cast<int64_t>(cps) * num_sms();
+    splits = static_cast<int>(std::min<int64_t>(128, std::max<int64_t>(1, target / Q)));
+    per = (128 + splits - 1) / splits;
+    splits = (128 + per - 1) / per;
+    if (ctas_per_sm(1, per) >= cps) break;
+  }
   p.tiles_per_cta = per;
   return launch<true>(p, dim3(splits, static_cast<unsigned>(Q)), 1, stream);
 }
