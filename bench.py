@@ -154,6 +154,28 @@ def attn_bytes_per_query() -> int:
     return 512 * 288 + 128 * 512 + 64 * 512 * 2 + 512 * 4
 
 
+def stage_roofline(wl, kinds, stage_ms, peak) -> dict:
+    """Per stage: the bytes the method must read in it per step, the rate its
+    measured (eager, event-timed) duration gives, and that rate as a fraction
+    of the measured HBM peak and of 8000 GB/s."""
+    q = wl.B * wl.n_q
+    n_full, n_reidx = kinds.count("full"), kinds.count("reindex")
+    stage_bytes = {
+        "scan": n_full * scan_bytes(wl),
+        "blocktopk": n_full * q * 4 * ((wl.N + 7) // 8),
+        "rescore": (n_full + n_reidx) * q * (2048 * 576 + 32 * 72 + 32 * 4 + 2048 * 4),
+        "attn": len(kinds) * q * attn_bytes_per_query(),
+    }
+    out = {}
+    for name, ms in stage_ms.items():
+        b = stage_bytes.get(name, 0)
+        if not b or not ms:
+            continue
+        gbs = b / (ms * 1e-3) / 1e9
+        out[name] = {"bytes_per_step": b, "gbs": gbs, "frac_measured": gbs / peak, "frac_8000": gbs / 8000.0}
+    return out
+
+
 def step_bytes(wl) -> int:
     """Reads the method must do per step, summed over the workload's layers."""
     q = wl.B * wl.n_q
@@ -296,6 +318,7 @@ def run_ours(args, wl, rank, world, local):
                    "ms_per_step_eager": ms_eager, "stage_steps": stage_steps},
         "hbm_fraction_step": (sb / (ms_max * 1e-3) / 1e9) / peak,
         "stage_ms": stage_ms,
+        "stage_roofline": stage_roofline(wl, kinds, stage_ms, peak),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": (achieved / peak) if achieved else None, "traffic": traffic,
                      "algorithmic_bytes_per_launch": dom_bytes, "peak_source": peak_kind},

@@ -25,6 +25,16 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
   const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (tok >= T) return;
+  // The entry's values do not depend on where it goes: load them first, so
+  // their latency overlaps the position and page lookups.
+  const uint4* lsrc = reinterpret_cast<const uint4*>(latent + static_cast<int64_t>(tok) * 512) + 2 * lane;
+  const uint4 l0 = lsrc[0], l1 = lsrc[1];
+  uint4 k0 = make_uint4(0, 0, 0, 0), k1 = k0;
+  if (lane < 8) {
+    const uint4* ksrc = reinterpret_cast<const uint4*>(idx_key + static_cast<int64_t>(tok) * 128) + 2 * lane;
+    k0 = ksrc[0];
+    k1 = ksrc[1];
+  }
   const int b = seq_idx[tok];
   const int64_t p = pos[tok];
   if (b < 0 || b >= B || p < 0 || (p >> 7) >= max_pages) {
@@ -40,10 +50,9 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
 
   // Main latent: lane -> channels 16*lane .. 16*lane+15.
   {
-    const uint4* src = reinterpret_cast<const uint4*>(latent + static_cast<int64_t>(tok) * 512) + 2 * lane;
     float v[16];
-    bf16x8_to_f32(src[0], v);
-    bf16x8_to_f32(src[1], v + 8);
+    bf16x8_to_f32(l0, v);
+    bf16x8_to_f32(l1, v + 8);
     uint8_t sc;
     uint32_t lo, hi;
     mxfp4_block(v, sc, lo, hi);
@@ -53,10 +62,9 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
   }
   // Indexer key: lanes 0..7 -> channel blocks 0..7.
   if (lane < 8) {
-    const uint4* src = reinterpret_cast<const uint4*>(idx_key + static_cast<int64_t>(tok) * 128) + 2 * lane;
     float v[16];
-    bf16x8_to_f32(src[0], v);
-    bf16x8_to_f32(src[1], v + 8);
+    bf16x8_to_f32(k0, v);
+    bf16x8_to_f32(k1, v + 8);
     uint8_t sc;
     uint32_t lo, hi;
     mxfp4_block(v, sc, lo, hi);
