@@ -63,6 +63,7 @@ def lib():
         L.orc_reindex.restype = i64
         L.orc_window_positions.argtypes, L.orc_window_positions.restype = [i64, i64, i64, p], i64
         L.orc_sparse_attention.argtypes = [p, i32, i32, p, i64, p, i64, d, p, p]
+        L.orc_output_derotate.argtypes = [p, i64, i32, i64]
         _lib = L
     return _lib
 
@@ -217,3 +218,12 @@ def sparse_attention(q_bf16, main_rows_bf16, win_rows_bf16, tau):
     lib().orc_sparse_attention(_p(q), H, D, _p(mr), mr.shape[0], _p(wr), wr.shape[0], float(tau),
                                _p(out), _p(lse))
     return out, lse
+
+
+def output_derotate(rows, t):
+    """Rows fp64 [n, D] (or [D]) of attention output for query position t, with
+    the last 64 channels rotated back by t (pairs 2i, 2i+1; see oracle.cpp)."""
+    a = np.array(rows, dtype=np.float64, order="C", copy=True)
+    D = a.shape[-1]
+    lib().orc_output_derotate(_p(a), a.size // D, D, int(t))
+    return a

@@ -408,4 +408,25 @@ void orc_sparse_attention(const uint16_t* q, int heads, int dim, const uint16_t*
   }
 }
 
+// Output de-rotation ("DeepSeek-V4 model structure (7): structure decides the
+// system", closing summary: the output is rotated back to restore relative
+// position). K = V carries the rotary position of its own entry on the last 64
+// channels, as interleaved pairs (448 + 2i, 449 + 2i) rotated by p * theta_i,
+// theta_i = 10000^(-2i/64). Rotating an output row's pairs by -t * theta_i,
+// t the query position, leaves every value term rotated by (p - t) * theta_i:
+// relative position. rows: [n, dim] fp64, in place.
+void orc_output_derotate(double* rows, int64_t n, int dim, int64_t t) {
+  for (int i = 0; i < 32; ++i) {
+    const double theta = std::pow(10000.0, -2.0 * i / 64.0);
+    const double a = -static_cast<double>(t) * theta;
+    const double c = std::cos(a), s = std::sin(a);
+    for (int64_t r = 0; r < n; ++r) {
+      double* x = rows + r * dim + (dim - 64) + 2 * i;
+      const double x0 = x[0], x1 = x[1];
+      x[0] = x0 * c - x1 * s;
+      x[1] = x0 * s + x1 * c;
+    }
+  }
+}
+
 }  // extern "C"

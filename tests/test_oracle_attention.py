@@ -11,6 +11,7 @@ closing summary on K = V single-head MQA over top-k plus 128 window entries).
 import math
 
 import numpy as np
+import pytest
 import torch
 
 import oracle
@@ -81,3 +82,43 @@ def test_window_positions_rule():
     assert oracle.window_positions(N - 6, N).tolist() == list(range(N - 128, N - 5))  # 123 entries
     assert oracle.window_positions(5, 6).tolist() == list(range(0, 6))
     assert len(oracle.window_positions(N - 6, N)) == 123
+
+
+# ---- output de-rotation ---------------------------------------------------------------
+
+def _rotary_as_complex(rows):
+    r = np.asarray(rows, np.float64)[..., 448:]
+    return r[..., 0::2] + 1j * r[..., 1::2]
+
+
+def test_derotation_is_complex_multiplication_by_the_inverse_phase():
+    """Pairs (448+2i, 449+2i) as complex numbers x0 + i x1: rotating back by
+    position t multiplies pair i by exp(-i t theta_i), theta_i = 10000^(-2i/64)
+    (numpy's complex exponential, not the oracle's cos/sin)."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((5, 512))
+    for t in (1, 7, 4095, 1 << 20):
+        got = oracle.output_derotate(x, t)
+        theta = 10000.0 ** (-2.0 * np.arange(32) / 64.0)
+        want = _rotary_as_complex(x) * np.exp(-1j * t * theta)
+        # t * theta reaches 1e6 rad, whose double has an ulp of 1.2e-10: the two
+        # routes may round the angle differently by that much (|x| < 5 here).
+        np.testing.assert_allclose(_rotary_as_complex(got), want, rtol=0, atol=1e-9)
+        assert np.array_equal(got[:, :448], x[:, :448])  # the other channels are untouched
+
+
+def test_derotation_worked_values_and_group_laws():
+    x = np.zeros((1, 512))
+    x[0, 448] = 1.0  # pair 0, theta_0 = 1
+    y = oracle.output_derotate(x, 1)
+    assert y[0, 448] == pytest.approx(math.cos(1.0), abs=1e-15)
+    assert y[0, 449] == pytest.approx(-math.sin(1.0), abs=1e-15)
+    rng = np.random.default_rng(4)
+    r = rng.standard_normal((3, 512))
+    assert np.array_equal(oracle.output_derotate(r, 0), r)  # position 0: identity
+    a = oracle.output_derotate(oracle.output_derotate(r, 300), 700)
+    b = oracle.output_derotate(r, 1000)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)  # rotations compose
+    pr = r[:, 448:].reshape(3, 32, 2)
+    pd = oracle.output_derotate(r, 12345)[:, 448:].reshape(3, 32, 2)
+    np.testing.assert_allclose(np.hypot(pd[..., 0], pd[..., 1]), np.hypot(pr[..., 0], pr[..., 1]), rtol=1e-13)
