@@ -97,6 +97,13 @@ extern "C" {
 
 #define CSA2_OUT_F32 0
 #define CSA2_OUT_BF16 1
+/* OR'ed into out_dtype: rotate the output back by the query position
+ * ("DeepSeek-V4 model structure (7): structure decides the system", closing
+ * summary: the output is rotated back to restore relative position). The last
+ * 64 channels of every output row, as pairs (448 + 2i, 449 + 2i), are rotated
+ * by -t * theta_i with theta_i = 10000^(-2i/64) and t the token's position
+ * N - n_q + j, the inverse of the rotary layout of the stored latents. */
+#define CSA2_OUT_DEROTATE 0x100
 
 #define CSA2_MODE_FULL 0
 #define CSA2_MODE_REINDEX 1
@@ -222,7 +229,8 @@ int csa2_indexer_full(const uint8_t* q_codes, const uint8_t* q_scales, const flo
  * window entries, duplicates kept. 64 heads x 512 dims, fp32 softmax.
  *   q: bf16 [B, n_q, 64, 512]; topk: int32 [B, n_q, 512]; ring_idx: int32 [B]
  *   out: [B, n_q, 64, 512] fp32 (out_dtype CSA2_OUT_F32) or bf16
- *   (CSA2_OUT_BF16); lse: fp32 [B, n_q, 64] natural-log sum of exp of the
+ *   (CSA2_OUT_BF16), optionally | CSA2_OUT_DEROTATE (see its definition;
+ *   lse is unchanged by it); lse: fp32 [B, n_q, 64] natural-log sum of exp of the
  *   scaled logits (may be NULL).
  *   ws: csa2_workspace_bytes(CSA2_OP_SPARSE_ATTN, ...). */
 int csa2_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len, int B, int n_q,

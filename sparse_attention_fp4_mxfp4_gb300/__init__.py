@@ -25,6 +25,7 @@ TOPK, POOL_BLOCKS, BLOCK, WINDOW, PAGE_TOKENS = 512, 2048, 8, 128, 128
 MAIN_ENTRY_BYTES, IDX_ENTRY_BYTES, MAX_NQ = 288, 72, 8
 PLANE_MAIN, PLANE_INDEX = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
+OUT_DEROTATE = 0x100  # OR'ed into out_dtype: rotate the output back by the query position
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 OP_INDEXER_FULL, OP_INDEXER_REINDEX, OP_SPARSE_ATTN, OP_DECODE_LAYER = 1, 2, 3, 4
 
@@ -250,11 +251,12 @@ def csa2_indexer_full(q_codes, q_scales, w, seq_len, max_ctx, block_table, n_pag
 # ---- attention ----------------------------------------------------------------
 
 def csa2_sparse_attn(q, topk, seq_len, block_table, n_pages, main_pages, rings, ring_idx, out, lse, ws,
-                     softmax_scale=1.0 / math.sqrt(LATENT_DIM), stream=None):
-    """q bf16 [B,n_q,64,512], topk int32 [B,n_q,512] -> out [B,n_q,64,512] (fp32 or bf16), lse fp32 [B,n_q,64]."""
+                     softmax_scale=1.0 / math.sqrt(LATENT_DIM), stream=None, derotate=False):
+    """q bf16 [B,n_q,64,512], topk int32 [B,n_q,512] -> out [B,n_q,64,512] (fp32 or bf16), lse fp32 [B,n_q,64].
+    derotate: rotate the output's last 64 channels back by the token position (CSA2_OUT_DEROTATE)."""
     _need(q, "q", torch.bfloat16, 4)
     B, n_q = q.shape[0], q.shape[1]
-    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    out_dtype = (OUT_F32 if out.dtype == torch.float32 else OUT_BF16) | (OUT_DEROTATE if derotate else 0)
     _check(lib.csa2_sparse_attn(_ptr(q), _ptr(topk), _ptr(seq_len), B, n_q, _ptr(block_table),
                                 block_table.shape[1], n_pages, _ptr(main_pages), _ptr(rings), _ptr(ring_idx),
                                 rings.shape[0], softmax_scale, out_dtype, _ptr(out), _ptr(lse), _ptr(ws),
@@ -265,7 +267,7 @@ def csa2_sparse_attn(q, topk, seq_len, block_table, n_pages, main_pages, rings, 
 
 def layer_args(mode, *, B, n_q, max_ctx, seq_len, block_table, n_pages, main_pages, idx_pages, rings,
                ring_idx, q, out, ws, q_idx_codes=None, q_idx_scales=None, w=None, pool=None, topk=None,
-               lse=None, softmax_scale=1.0 / math.sqrt(LATENT_DIM)) -> LayerArgs:
+               lse=None, softmax_scale=1.0 / math.sqrt(LATENT_DIM), derotate=False) -> LayerArgs:
     a = LayerArgs()
     a.mode, a.B, a.n_q, a.max_ctx = mode, B, n_q, max_ctx
     a.seq_len, a.block_table, a.max_pages, a.n_pages = _ptr(seq_len), _ptr(block_table), block_table.shape[1], n_pages
@@ -274,7 +276,7 @@ def layer_args(mode, *, B, n_q, max_ctx, seq_len, block_table, n_pages, main_pag
     a.q_idx_codes, a.q_idx_scales, a.w, a.q = _ptr(q_idx_codes), _ptr(q_idx_scales), _ptr(w), _ptr(q)
     a.pool, a.topk = _ptr(pool), _ptr(topk)
     a.softmax_scale = softmax_scale
-    a.out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    a.out_dtype = (OUT_F32 if out.dtype == torch.float32 else OUT_BF16) | (OUT_DEROTATE if derotate else 0)
     a.out, a.lse = _ptr(out), _ptr(lse)
     a.ws, a.ws_bytes = _ptr(ws), ws.numel() * ws.element_size()
     return a

@@ -89,6 +89,22 @@ __device__ __forceinline__ void warp_reduce_scatter32(float (&v)[32], int lane, 
   }
 }
 
+// cos and sin of -t * theta_i, theta_i = 10000^(-2i/64) (output de-rotation).
+// The angle is formed and reduced to [-pi, pi] in double precision (t * theta
+// reaches 1e9 rad), then evaluated in single precision.
+__device__ __forceinline__ void derotate_cs(int64_t t, int i, float& c, float& s) {
+  const double theta = exp2(-static_cast<double>(i) * (13.287712379549449 / 32.0));  // log2(10000) = 13.2877...
+  double a = -static_cast<double>(t) * theta;
+  a -= 6.283185307179586 * rint(a * 0.15915494309189535);
+  sincosf(static_cast<float>(a), &s, &c);
+}
+
+// Rotates this lane's value x of output channel d (pairs (448 + 2i, 449 + 2i))
+// by -t * theta_i, given its partner lane's value y (lane ^ 1 holds channel d ^ 1).
+__device__ __forceinline__ float derotate_value(float x, float y, int d, float c, float s) {
+  return (d & 1) ? (y * s + x * c) : (x * c - y * s);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -432,14 +448,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
         tmem_ld32(tmem + lane_base + 64 + 64 * mt + 32 * hh, v);
         tmem_wait_ld();
         if (final_out) {
-          if (P.out_dtype == CSA2_OUT_F32) {
+          float y[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(v[i]) * lsum[32 * hh + i];
+          if ((P.out_dtype & CSA2_OUT_DEROTATE) && d >= 448) {  // whole warps: rows 64..127 of the last M tile
+            float c, sn;
+            derotate_cs(t, (d - 448) >> 1, c, sn);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float other = __shfl_xor_sync(0xffffffffu, y[i], 1);
+              y[i] = derotate_value(y[i], other, d, c, sn);
+            }
+          }
+          if ((P.out_dtype & ~CSA2_OUT_DEROTATE) == CSA2_OUT_F32) {
             float* o = static_cast<float*>(P.out) + (static_cast<int64_t>(q) * 64 + 32 * hh) * 512 + d;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i * 512] = __uint_as_float(v[i]) * lsum[32 * hh + i];
+            for (int i = 0; i < 32; ++i) o[i * 512] = y[i];
           } else {
             __nv_bfloat16* o = static_cast<__nv_bfloat16*>(P.out) + (static_cast<int64_t>(q) * 64 + 32 * hh) * 512 + d;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i * 512] = __float2bfloat16_rn(__uint_as_float(v[i]) * lsum[32 * hh + i]);
+            for (int i = 0; i < 32; ++i) o[i * 512] = __float2bfloat16_rn(y[i]);
           }
         } else {
           float* o = part + (32 * hh) * 512 + d;
@@ -466,7 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part,
                                                            const float2* __restrict__ stats, int nsplit,
                                                            int out_dtype, void* __restrict__ out,
-                                                           float* __restrict__ lse) {
+                                                           float* __restrict__ lse,
+                                                           const int64_t* __restrict__ seq_len, int n_q) {
   griddep_wait();
   griddep_launch();
   const int q = blockIdx.x;
@@ -497,9 +526,16 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
 #pragma unroll
     for (int s = 0; s < kChunks; ++s)
       if (s < nsplit) acc += f[s] * part[((static_cast<int64_t>(q) * kChunks + s) * 64 + h) * 512 + d];
-    const float o = acc * inv;
+    float o = acc * inv;
+    if ((out_dtype & CSA2_OUT_DEROTATE) && d >= 448) {  // whole warps: threads 192..255, second pass
+      const int64_t t = seq_len[q / n_q] - n_q + q % n_q;
+      float c, sn;
+      derotate_cs(t, (d - 448) >> 1, c, sn);
+      const float other = __shfl_xor_sync(0xffffffffu, o, 1);
+      o = derotate_value(o, other, d, c, sn);
+    }
     const int64_t oi = (static_cast<int64_t>(q) * 64 + h) * 512 + d;
-    if (out_dtype == CSA2_OUT_F32) static_cast<float*>(out)[oi] = o;
+    if ((out_dtype & ~CSA2_OUT_DEROTATE) == CSA2_OUT_F32) static_cast<float*>(out)[oi] = o;
     else static_cast<__nv_bfloat16*>(out)[oi] = __float2bfloat16_rn(o);
   }
   if (tid == 0 && lse)
@@ -584,7 +620,7 @@ cudaError_t launch_sparse_attn(const void* q, const int32_t* topk, const int64_t
   if (e != cudaSuccess || p.nsplit == 1) return e;
   return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(Q), 64), dim3(256), 0, stream, 0,
                     static_cast<const float*>(p.part), static_cast<const float2*>(p.stats), p.nsplit, out_dtype,
-                    out, lse);
+                    out, lse, seq_len, n_q);
 }
 
 }  // namespace csa2

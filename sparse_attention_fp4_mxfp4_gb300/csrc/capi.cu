@@ -287,7 +287,8 @@ int csa2_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len,
   CHECK_PTR(ring_idx, "ring_idx");
   if (n_rings < 1) return fail(CSA2_ERR_INVALID_ARG, "n_rings < 1");
   CHECK_PTR(out, "out");
-  if (out_dtype != CSA2_OUT_F32 && out_dtype != CSA2_OUT_BF16)
+  const int base_dtype = out_dtype & ~CSA2_OUT_DEROTATE;
+  if (base_dtype != CSA2_OUT_F32 && base_dtype != CSA2_OUT_BF16)
     return fail(CSA2_ERR_INVALID_ARG, "unknown out_dtype %d", out_dtype);
   if (!(softmax_scale > 0.f) || softmax_scale > 1e30f) return fail(CSA2_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
   const int64_t Q = static_cast<int64_t>(B) * n_q;

@@ -210,6 +210,31 @@ def test_sparse_attention(N, n_q, B, out):
             np.testing.assert_allclose(gl[b, j], rl, rtol=1e-4, atol=1e-4)
 
 
+@pytest.mark.parametrize("B,n_q,out", [(2, 3, "f32"), (40, 4, "f32"), (3, 2, "bf16")])
+def test_sparse_attention_derotated(B, n_q, out):
+    """CSA2_OUT_DEROTATE: the output's rotary channels rotated back by the token
+    position, against the oracle's attention followed by its de-rotation. 160
+    tokens take the one-CTA-per-token path, 6 the split-and-merge path."""
+    N = 5000
+    wl = Workload(93, "t", "reuse", B=B, N=N, n_q=n_q, layers=("reuse",))
+    S = H.build(wl, DEV, shuffle_seed=12, prefill_step=True)
+    L = S.layers[0]
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    o = torch.empty(B, n_q, 64, 512, dtype=dt, device=DEV)
+    ws = torch.empty(csa2.csa2_workspace_bytes(csa2.OP_SPARSE_ATTN, B, n_q, N), dtype=torch.uint8, device=DEV)
+    csa2.csa2_sparse_attn(L.q, S.topk, S.seq_len, S.cache.block_table, S.cache.n_pages, S.cache.main_pages,
+                          S.cache.rings, L.ring_idx, o, None, ws, derotate=True)
+    go = o.float().cpu().numpy()
+    tk = S.topk.cpu().numpy()
+    _status_ok()
+    rng = np.random.default_rng(5)
+    pairs = {(int(rng.integers(B)), int(rng.integers(n_q))) for _ in range(12)}
+    for b, j in sorted(pairs)[:6]:
+        ro, _ = H.oracle_attention(S, b, j, 0, tk[b, j])
+        ro = oracle.output_derotate(ro, S.t(j))
+        H.check_attention(go[b, j], ro, H.TOL_ATTN_F32 if out == "f32" else H.TOL_ATTN_BF16)
+
+
 def test_sparse_attention_with_padded_topk():
     """Fewer than 512 selected positions (-1 padding), e.g. a short context."""
     wl = Workload(95, "t", "reuse", B=2, N=3000, n_q=1, layers=("reuse",))
