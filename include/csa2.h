@@ -56,8 +56,14 @@
  *     p of a sequence lives in slot p % 128 of its ring.
  *   - Query token j of n_q of sequence b sits at position
  *     t = seq_len[b] - n_q + j (seq_len counts the entries already appended,
- *     including this step's tokens). Its sliding window is the positions
- *     max(0, t - 127, seq_len[b] - 128) .. t still resident in the ring.
+ *     including this step's tokens). At decode (csa2_sparse_attn) its sliding
+ *     window is the positions max(0, t - 127, seq_len[b] - 128) .. t still
+ *     resident in the ring; in a prefill call (csa2_sparse_attn_prefill) it is
+ *     exactly max(0, t - 127) .. t.
+ *   - Query tokens per sequence: the indexer calls and the prefill attention
+ *     take n_q <= CSA2_MAX_PREFILL_NQ (the Full scan serves them in groups of
+ *     8 tokens), the decode attention n_q <= CSA2_MAX_NQ; every call takes
+ *     B * n_q <= CSA2_MAX_TOKENS. Larger shapes return CSA2_ERR_UNSUPPORTED.
  */
 #ifndef CSA2_H_
 #define CSA2_H_
@@ -90,7 +96,9 @@ extern "C" {
 #define CSA2_PAGE_TOKENS 128   /* entries per page */
 #define CSA2_MAIN_ENTRY_BYTES 288
 #define CSA2_IDX_ENTRY_BYTES 72
-#define CSA2_MAX_NQ 8          /* query tokens per sequence in one call */
+#define CSA2_MAX_NQ 8          /* query tokens per sequence in one decode call */
+#define CSA2_MAX_PREFILL_NQ 4096  /* query tokens per sequence in one prefill call */
+#define CSA2_MAX_TOKENS 65535  /* B * n_q in one call */
 
 #define CSA2_PLANE_MAIN 0
 #define CSA2_PLANE_INDEX 1
@@ -144,9 +152,28 @@ int csa2_append_kv(const void* latent, const void* idx_key, const int32_t* seq_i
 
 /* E4M3 (round to nearest even, saturating, no scale) of T new window entries
  * x: bf16 [T, 512] into slot pos % 128 of ring ring_idx[i] of rings
- * [n_rings, 128, 512]. */
+ * [n_rings, 128, 512]. Entries of one call must go to distinct slots (at most
+ * 128 consecutive positions per ring); a prefill chunk longer than that uses
+ * csa2_quant_fp8_entries + csa2_ring_refill. */
 int csa2_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, int T,
                     int64_t n_rings, uint8_t* rings, void* stream);
+
+/* The same E4M3 encoding of T window entries x: bf16 [T, 512] into out: u8
+ * [T, 512] (16-byte aligned), row for row. A prefill chunk's own window
+ * entries are encoded this way for csa2_sparse_attn_prefill before the ring
+ * receives the last 128 of them (csa2_ring_refill). */
+int csa2_quant_fp8_entries(const void* x, int T, uint8_t* out, void* stream);
+
+/* Ring refill ([RN] 2.4, SWA Bounded Replay: the window state is rebuilt from
+ * the last n_win tokens alone). entries: E4M3 [B, n, 512], the window entries
+ * of positions seq_len[b] - n .. seq_len[b] - 1 of sequence b; the last
+ * min(n, 128) of them go to slot position % 128 of ring ring_idx[b] of rings
+ * [n_rings, 128, 512]; the other slots keep their bytes. With n >= 128 the
+ * ring afterwards holds exactly positions seq_len[b] - 128 .. seq_len[b] - 1.
+ * Entries at a negative position or of a ring index out of range are skipped
+ * and set CSA2_ERR_DEVICE_BOUNDS. */
+int csa2_ring_refill(const uint8_t* entries, const int64_t* seq_len, int B, int n,
+                     const int32_t* ring_idx, int64_t n_rings, uint8_t* rings, void* stream);
 
 /* ---- codec utilities -------------------------------------------------------- */
 /* MXFP4 quantisation of n bf16 values (n % 16 == 0): codes [n/2], scales
@@ -239,6 +266,22 @@ int csa2_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len,
                      int64_t n_rings, float softmax_scale, int out_dtype, void* out, float* lse,
                      void* ws, size_t ws_bytes, void* stream);
 
+/* Prefill (chunked prefill) of n_q <= CSA2_MAX_PREFILL_NQ new tokens per
+ * sequence ([RN] 2.2, [AB] 3.3: the same attention over a causal run of query
+ * tokens). As csa2_sparse_attn, except for the window: token t sees exactly
+ * the entries of positions max(0, t - 127) .. t. Those of the call's own
+ * positions N - n_q .. N - 1 come from swa_chunk: E4M3 [B, n_q, 512]
+ * (csa2_quant_fp8_entries), 16-byte aligned; older ones from the rings, which
+ * must still hold the 128 positions before the chunk (refill them with
+ * csa2_ring_refill after the call). ws: csa2_workspace_bytes(CSA2_OP_SPARSE_ATTN,
+ * ...), zero bytes (ws may be NULL) from 256 tokens on. */
+int csa2_sparse_attn_prefill(const void* q, const int32_t* topk, const int64_t* seq_len, int B,
+                             int n_q, const int32_t* block_table, int max_pages, int64_t n_pages,
+                             const uint8_t* main_pages, const uint8_t* rings,
+                             const int32_t* ring_idx, int64_t n_rings, const uint8_t* swa_chunk,
+                             float softmax_scale, int out_dtype, void* out, float* lse, void* ws,
+                             size_t ws_bytes, void* stream);
+
 /* ---- mode dispatcher ([RN] 2.2, [AB] 3.3) ----------------------------------- */
 typedef struct csa2_layer_args {
   int mode;                 /* CSA2_MODE_FULL / _REINDEX / _REUSE */
@@ -265,11 +308,16 @@ typedef struct csa2_layer_args {
   float* lse;               /* may be NULL */
   void* ws;
   size_t ws_bytes;          /* csa2_workspace_bytes(CSA2_OP_DECODE_LAYER, ...) */
+  const uint8_t* swa_chunk; /* NULL: decode (n_q <= CSA2_MAX_NQ, window from the ring).
+                               Else prefill: the chunk's E4M3 window entries
+                               [B, n_q, 512], attention as csa2_sparse_attn_prefill */
 } csa2_layer_args;
 
 /* One layer: FULL = indexer_full then sparse_attn; REINDEX = indexer_reindex
  * (on the given or latest pool) then sparse_attn; REUSE = sparse_attn on the
- * given or latest top-k. */
+ * given or latest top-k. With swa_chunk set, the attention is
+ * csa2_sparse_attn_prefill (the ring is not written: refill it after the
+ * chunk's last layer). */
 int csa2_decode_layer(const csa2_layer_args* layer, void* stream);
 
 /* Layers in order on one stream. A REINDEX layer with pool == NULL uses the

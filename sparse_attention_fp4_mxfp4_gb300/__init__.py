@@ -23,6 +23,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOU
 LATENT_DIM, Q_HEADS, IDX_HEADS, IDX_DIM = 512, 64, 32, 128
 TOPK, POOL_BLOCKS, BLOCK, WINDOW, PAGE_TOKENS = 512, 2048, 8, 128, 128
 MAIN_ENTRY_BYTES, IDX_ENTRY_BYTES, MAX_NQ = 288, 72, 8
+MAX_PREFILL_NQ, MAX_TOKENS = 4096, 65535
 PLANE_MAIN, PLANE_INDEX = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
 OUT_DEROTATE = 0x100  # OR'ed into out_dtype: rotate the output back by the query position
@@ -32,9 +33,10 @@ OP_INDEXER_FULL, OP_INDEXER_REINDEX, OP_SPARSE_ATTN, OP_DECODE_LAYER = 1, 2, 3, 
 # Exported entry points of include/csa2.h.
 EXPORTS = (
     "csa2_status_string", "csa2_last_error", "csa2_version", "csa2_page_bytes", "csa2_ring_bytes",
-    "csa2_workspace_bytes", "csa2_append_kv", "csa2_append_swa", "csa2_quant_mxfp4",
+    "csa2_workspace_bytes", "csa2_append_kv", "csa2_append_swa", "csa2_quant_fp8_entries",
+    "csa2_ring_refill", "csa2_quant_mxfp4",
     "csa2_dequant_mxfp4", "csa2_quant_fp8", "csa2_indexer_scan", "csa2_block_topk",
-    "csa2_indexer_reindex", "csa2_indexer_reindex_noalloc", "csa2_indexer_full", "csa2_sparse_attn", "csa2_decode_layer",
+    "csa2_indexer_reindex", "csa2_indexer_reindex_noalloc", "csa2_indexer_full", "csa2_sparse_attn", "csa2_sparse_attn_prefill", "csa2_decode_layer",
     "csa2_decode_group", "csa2_check_device_status",
 )
 
@@ -56,6 +58,7 @@ class LayerArgs(ctypes.Structure):
         ("w", ctypes.c_void_p), ("q", ctypes.c_void_p), ("pool", ctypes.c_void_p), ("topk", ctypes.c_void_p),
         ("softmax_scale", ctypes.c_float), ("out_dtype", ctypes.c_int), ("out", ctypes.c_void_p),
         ("lse", ctypes.c_void_p), ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
+        ("swa_chunk", ctypes.c_void_p),
     ]
 
 
@@ -74,6 +77,8 @@ def _load():
         "csa2_workspace_bytes": ([i32, i32, i32, i64, psz], i32),
         "csa2_append_kv": ([p, p, p, p, i32, p, i32, i32, i64, p, p, p], i32),
         "csa2_append_swa": ([p, p, p, i32, i64, p, p], i32),
+        "csa2_quant_fp8_entries": ([p, i32, p, p], i32),
+        "csa2_ring_refill": ([p, p, i32, i32, p, i64, p, p], i32),
         "csa2_quant_mxfp4": ([p, i64, p, p, p], i32),
         "csa2_dequant_mxfp4": ([p, p, i64, p, p], i32),
         "csa2_quant_fp8": ([p, i64, p, p], i32),
@@ -83,6 +88,8 @@ def _load():
         "csa2_indexer_reindex_noalloc": ([p, p, p, p, i32, i32, p, i32, i64, p, p, p, p], i32),
         "csa2_indexer_full": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, p, p, sz, p], i32),
         "csa2_sparse_attn": ([p, p, p, i32, i32, p, i32, i64, p, p, p, i64, f32, i32, p, p, p, sz, p], i32),
+        "csa2_sparse_attn_prefill": ([p, p, p, i32, i32, p, i32, i64, p, p, p, i64, p, f32, i32, p, p, p, sz, p],
+                                     i32),
         "csa2_decode_layer": ([ctypes.POINTER(LayerArgs), p], i32),
         "csa2_decode_group": ([ctypes.POINTER(LayerArgs), i32, p], i32),
         "csa2_check_device_status": ([p, ctypes.POINTER(ctypes.c_int)], i32),
@@ -170,6 +177,25 @@ def csa2_append_swa(x, ring_idx, pos, rings, stream=None):
     T = x.shape[0]
     _check(lib.csa2_append_swa(_ptr(x), _ptr(ring_idx), _ptr(pos), T, rings.shape[0], _ptr(rings),
                                _stream(stream)))
+
+
+def csa2_quant_fp8_entries(x, out=None, stream=None):
+    """x bf16 [T,512] -> E4M3 uint8 [T,512] (a prefill chunk's own window entries)."""
+    _need(x, "x", torch.bfloat16, 2)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib.csa2_quant_fp8_entries(_ptr(x), x.shape[0], _ptr(out), _stream(stream)))
+    return out
+
+
+def csa2_ring_refill(entries, seq_len, ring_idx, rings, stream=None):
+    """entries uint8 [B,n,512] (E4M3, positions seq_len-n .. seq_len-1), ring_idx int32 [B]:
+    the last min(n,128) entries of each sequence into their ring slots."""
+    _need(entries, "entries", torch.uint8, 3)
+    _need(ring_idx, "ring_idx", torch.int32, 1)
+    B, n = entries.shape[0], entries.shape[1]
+    _check(lib.csa2_ring_refill(_ptr(entries), _ptr(seq_len), B, n, _ptr(ring_idx), rings.shape[0], _ptr(rings),
+                                _stream(stream)))
 
 
 # ---- codecs -------------------------------------------------------------------
@@ -263,11 +289,26 @@ def csa2_sparse_attn(q, topk, seq_len, block_table, n_pages, main_pages, rings, 
                                 ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def csa2_sparse_attn_prefill(q, topk, seq_len, block_table, n_pages, main_pages, rings, ring_idx, swa_chunk, out,
+                             lse, ws=None, softmax_scale=1.0 / math.sqrt(LATENT_DIM), stream=None, derotate=False):
+    """As csa2_sparse_attn, with the exact causal window: swa_chunk uint8 [B,n_q,512] holds the E4M3
+    window entries of the call's own positions, the rings the 128 positions before them."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(swa_chunk, "swa_chunk", torch.uint8, 3)
+    B, n_q = q.shape[0], q.shape[1]
+    out_dtype = (OUT_F32 if out.dtype == torch.float32 else OUT_BF16) | (OUT_DEROTATE if derotate else 0)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib.csa2_sparse_attn_prefill(_ptr(q), _ptr(topk), _ptr(seq_len), B, n_q, _ptr(block_table),
+                                        block_table.shape[1], n_pages, _ptr(main_pages), _ptr(rings),
+                                        _ptr(ring_idx), rings.shape[0], _ptr(swa_chunk), softmax_scale, out_dtype,
+                                        _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream(stream)))
+
+
 # ---- dispatcher ---------------------------------------------------------------
 
 def layer_args(mode, *, B, n_q, max_ctx, seq_len, block_table, n_pages, main_pages, idx_pages, rings,
                ring_idx, q, out, ws, q_idx_codes=None, q_idx_scales=None, w=None, pool=None, topk=None,
-               lse=None, softmax_scale=1.0 / math.sqrt(LATENT_DIM), derotate=False) -> LayerArgs:
+               lse=None, softmax_scale=1.0 / math.sqrt(LATENT_DIM), derotate=False, swa_chunk=None) -> LayerArgs:
     a = LayerArgs()
     a.mode, a.B, a.n_q, a.max_ctx = mode, B, n_q, max_ctx
     a.seq_len, a.block_table, a.max_pages, a.n_pages = _ptr(seq_len), _ptr(block_table), block_table.shape[1], n_pages
@@ -279,6 +320,7 @@ def layer_args(mode, *, B, n_q, max_ctx, seq_len, block_table, n_pages, main_pag
     a.out_dtype = (OUT_F32 if out.dtype == torch.float32 else OUT_BF16) | (OUT_DEROTATE if derotate else 0)
     a.out, a.lse = _ptr(out), _ptr(lse)
     a.ws, a.ws_bytes = _ptr(ws), ws.numel() * ws.element_size()
+    a.swa_chunk = _ptr(swa_chunk)
     return a
 
 

@@ -85,11 +85,17 @@ __global__ void __launch_bounds__(256) append_swa_kernel(const uint16_t* __restr
   const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (tok >= T) return;
-  const int r = ring_idx[tok];
-  const int64_t p = pos[tok];
-  if (r < 0 || r >= n_rings || p < 0) {
-    if (lane == 0) report(CSA2_ERR_DEVICE_BOUNDS, 111);
-    return;
+  // ring_idx == NULL: entry tok goes to row tok of a plain [T, 512] array
+  // (a prefill chunk's own window entries).
+  int64_t row = tok;
+  if (ring_idx) {
+    const int r = ring_idx[tok];
+    const int64_t p = pos[tok];
+    if (r < 0 || r >= n_rings || p < 0) {
+      if (lane == 0) report(CSA2_ERR_DEVICE_BOUNDS, 111);
+      return;
+    }
+    row = static_cast<int64_t>(r) * 128 + (p & 127);
   }
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * 512) + 2 * lane;
   float v[16];
@@ -100,8 +106,33 @@ __global__ void __launch_bounds__(256) append_swa_kernel(const uint16_t* __restr
   for (int i = 0; i < 4; ++i)
     w[i] = static_cast<uint32_t>(e4m3x2_from_f32(v[4 * i], v[4 * i + 1])) |
            (static_cast<uint32_t>(e4m3x2_from_f32(v[4 * i + 2], v[4 * i + 3])) << 16);
-  uint8_t* dst = rings + (static_cast<int64_t>(r) * 128 + (p & 127)) * 512 + 16 * lane;
+  uint8_t* dst = rings + row * 512 + 16 * lane;
   *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Ring refill: entries [B][n][512] (E4M3) hold positions seq_len[b] - n ..
+// seq_len[b] - 1; the last min(n, 128) of them go to slot position % 128 of
+// their sequence's ring. One warp per entry, 16 bytes per lane.
+__global__ void __launch_bounds__(256) ring_refill_kernel(const uint8_t* __restrict__ entries,
+                                                          const int64_t* __restrict__ seq_len, int n,
+                                                          const int32_t* __restrict__ ring_idx,
+                                                          int64_t n_rings, uint8_t* __restrict__ rings) {
+  griddep_wait();
+  griddep_launch();
+  const int b = blockIdx.y;
+  const int m = n < 128 ? n : 128;
+  const int k = blockIdx.x * 8 + (threadIdx.x >> 5);  // k-th of the last m entries
+  const int lane = threadIdx.x & 31;
+  if (k >= m) return;
+  const int i = n - m + k;
+  const int64_t p = seq_len[b] - n + i;
+  const int r = ring_idx[b];
+  if (r < 0 || r >= n_rings || p < 0) {
+    if (lane == 0) report(CSA2_ERR_DEVICE_BOUNDS, 112);
+    return;
+  }
+  const uint4 v = reinterpret_cast<const uint4*>(entries + (static_cast<int64_t>(b) * n + i) * 512)[lane];
+  reinterpret_cast<uint4*>(rings + (static_cast<int64_t>(r) * 128 + (p & 127)) * 512)[lane] = v;
 }
 
 __global__ void quant_mxfp4_kernel(const uint16_t* __restrict__ x, int64_t nblocks,
@@ -174,6 +205,14 @@ cudaError_t launch_append_swa(const void* x, const int32_t* ring_idx, const int6
   if (T == 0) return cudaSuccess;
   return launch_pdl(append_swa_kernel, dim3((T + 7) / 8), dim3(256), 0, stream, 0,
                     static_cast<const uint16_t*>(x), ring_idx, pos, T, n_rings, rings);
+}
+
+cudaError_t launch_ring_refill(const uint8_t* entries, const int64_t* seq_len, int B, int n,
+                               const int32_t* ring_idx, int64_t n_rings, uint8_t* rings, cudaStream_t stream) {
+  if (B == 0 || n == 0) return cudaSuccess;
+  const int m = n < 128 ? n : 128;
+  return launch_pdl(ring_refill_kernel, dim3((m + 7) / 8, B), dim3(256), 0, stream, 0, entries, seq_len, n,
+                    ring_idx, n_rings, rings);
 }
 
 cudaError_t launch_quant_mxfp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales,

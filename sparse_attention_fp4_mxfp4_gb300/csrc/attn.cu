@@ -50,6 +50,10 @@ constexpr int kSmemBytes = 1024 + kMiscOff + 4096;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.f;  // headroom (log2 units) before the stabiliser is raised
 constexpr int kBarGd = 1, kBarSxOr = 2, kBarSx = 3;  // named barriers
+constexpr int64_t kChunkSrc = int64_t(1) << 62;     // key offset tag: the call's own window entries
+// Tokens from which a query's chunks are never split over several CTAs (so no
+// partial-output workspace is needed), whatever the SM count.
+constexpr int64_t kNoSplitQueries = 256;
 
 struct AttnParams {
   const uint16_t* q;
@@ -63,6 +67,10 @@ struct AttnParams {
   const uint8_t* rings;
   const int32_t* ring_idx;
   int64_t n_rings;
+  // Prefill: FP8 window entries of the call's own positions N-n_q .. N-1,
+  // [B][n_q][512]; the rings then hold the positions before them. NULL:
+  // decode, every window entry comes from the ring.
+  const uint8_t* swa_chunk;
   float scale_log2;   // softmax_scale * log2(e)
   int nsplit;         // CTAs per query (1..5)
   int out_dtype;
@@ -177,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
             else off = static_cast<int64_t>(page) * (128 * 288) + (p & 127) * 288;
           }
         }
-      } else {
+      } else if (!P.swa_chunk) {
         const int32_t ri = P.ring_idx[b];
         const int64_t base = N - 128;  // the ring holds positions N-128 .. N-1
         int64_t d = (static_cast<int64_t>(gt) - base) % 128;
@@ -190,6 +198,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
           if (gt == 0) report(CSA2_ERR_DEVICE_BOUNDS, 403);
         } else if (p >= lo && p <= t) {
           off = (static_cast<int64_t>(ri) * 128 + gt) * 512;
+        }
+      } else {
+        // Prefill: key slot gt holds position t - 127 + gt, from the call's
+        // own entries when it is one of the new positions, else from the ring
+        // (which still holds the 128 positions before them).
+        const int64_t p = t - 127 + gt, first_new = N - P.n_q;
+        if (p >= 0) {
+          if (p >= first_new) {
+            off = kChunkSrc | ((static_cast<int64_t>(b) * P.n_q + (p - first_new)) * 512);
+          } else {
+            const int32_t ri = P.ring_idx[b];
+            if (ri < 0 || ri >= P.n_rings) report(CSA2_ERR_DEVICE_BOUNDS, 404);
+            else off = (static_cast<int64_t>(ri) * 128 + (p & 127)) * 512;
+          }
         }
       }
       dst[gt] = off;
@@ -214,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
           scl[hf] = *reinterpret_cast<const uint2*>(e + 256 + hf * 16 + sub * 8);
         }
       } else {
-        const uint8_t* e = P.rings + off;
+        const uint8_t* e = (off & kChunkSrc) ? P.swa_chunk + (off & ~kChunkSrc) : P.rings + off;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
@@ -572,6 +594,7 @@ cudaError_t status_attn(cudaStream_t stream, int* code, int* where, bool clear) 
 }
 
 size_t attn_workspace_bytes(int64_t queries) {
+  if (queries >= kNoSplitQueries) return 0;
   const size_t part = static_cast<size_t>(queries) * kChunks * 64 * 512 * sizeof(float);
   const size_t stats = static_cast<size_t>(queries) * kChunks * 64 * sizeof(float2);
   return ((part + 255) & ~size_t(255)) + ((stats + 255) & ~size_t(255));
@@ -580,8 +603,8 @@ size_t attn_workspace_bytes(int64_t queries) {
 cudaError_t launch_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len, int B,
                                int n_q, const int32_t* block_table, int max_pages,
                                int64_t n_pages, const uint8_t* main_pages, const uint8_t* rings,
-                               const int32_t* ring_idx, int64_t n_rings, float softmax_scale,
-                               int out_dtype, void* out, float* lse, void* ws,
+                               const int32_t* ring_idx, int64_t n_rings, const uint8_t* swa_chunk,
+                               float softmax_scale, int out_dtype, void* out, float* lse, void* ws,
                                cudaStream_t stream) {
   const int64_t Q = static_cast<int64_t>(B) * n_q;
   if (Q == 0) return cudaSuccess;
@@ -606,9 +629,11 @@ cudaError_t launch_sparse_attn(const void* q, const int32_t* topk, const int64_t
   p.rings = rings;
   p.ring_idx = ring_idx;
   p.n_rings = n_rings;
+  p.swa_chunk = swa_chunk;
   p.scale_log2 = softmax_scale * kLog2e;
   // Split a query's chunks over several CTAs only while that is what fills the GPU.
-  p.nsplit = static_cast<int>(std::min<int64_t>(kChunks, std::max<int64_t>(1, attn_num_sms() / Q)));
+  p.nsplit = Q >= kNoSplitQueries
+                 ? 1 : static_cast<int>(std::min<int64_t>(kChunks, std::max<int64_t>(1, attn_num_sms() / Q)));
   p.out_dtype = out_dtype;
   p.out = out;
   p.lse = lse;

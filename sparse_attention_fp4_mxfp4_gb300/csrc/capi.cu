@@ -47,11 +47,14 @@ size_t blockmax_ws(int64_t Q, int64_t max_ctx) {
     if (!aligned16(p)) return fail(CSA2_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
   } while (0)
 
-int check_batch(int B, int n_q) {
+// max_nq: CSA2_MAX_NQ for the decode attention, CSA2_MAX_PREFILL_NQ elsewhere.
+int check_batch(int B, int n_q, int max_nq = CSA2_MAX_PREFILL_NQ) {
   if (B < 0) return fail(CSA2_ERR_INVALID_ARG, "B = %d < 0", B);
-  if (B > 65535) return fail(CSA2_ERR_UNSUPPORTED, "B = %d > 65535", B);
+  if (B > CSA2_MAX_TOKENS) return fail(CSA2_ERR_UNSUPPORTED, "B = %d > %d", B, CSA2_MAX_TOKENS);
   if (n_q < 1) return fail(CSA2_ERR_INVALID_ARG, "n_q = %d < 1", n_q);
-  if (n_q > CSA2_MAX_NQ) return fail(CSA2_ERR_UNSUPPORTED, "n_q = %d > %d", n_q, CSA2_MAX_NQ);
+  if (n_q > max_nq) return fail(CSA2_ERR_UNSUPPORTED, "n_q = %d > %d", n_q, max_nq);
+  if (static_cast<int64_t>(B) * n_q > CSA2_MAX_TOKENS)
+    return fail(CSA2_ERR_UNSUPPORTED, "B * n_q = %lld > %d", static_cast<long long>(B) * n_q, CSA2_MAX_TOKENS);
   return CSA2_OK;
 }
 
@@ -151,6 +154,29 @@ int csa2_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, 
   if (n_rings < 1) return fail(CSA2_ERR_INVALID_ARG, "n_rings < 1");
   cudaError_t e = csa2::launch_append_swa(x, ring_idx, pos, T, n_rings, rings, S(stream));
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "append_swa launch");
+}
+
+int csa2_quant_fp8_entries(const void* x, int T, uint8_t* out, void* stream) {
+  if (T < 0) return fail(CSA2_ERR_INVALID_ARG, "T = %d < 0", T);
+  if (T == 0) return CSA2_OK;
+  CHECK_A16(x, "x");
+  CHECK_A16(out, "out");
+  cudaError_t e = csa2::launch_append_swa(x, nullptr, nullptr, T, 0, out, S(stream));
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "quant_fp8_entries launch");
+}
+
+int csa2_ring_refill(const uint8_t* entries, const int64_t* seq_len, int B, int n,
+                     const int32_t* ring_idx, int64_t n_rings, uint8_t* rings, void* stream) {
+  if (B < 0 || B > CSA2_MAX_TOKENS) return fail(CSA2_ERR_INVALID_ARG, "B = %d out of range", B);
+  if (n < 0) return fail(CSA2_ERR_INVALID_ARG, "n = %d < 0", n);
+  if (B == 0 || n == 0) return CSA2_OK;
+  CHECK_A16(entries, "entries");
+  CHECK_PTR(seq_len, "seq_len");
+  CHECK_PTR(ring_idx, "ring_idx");
+  CHECK_A16(rings, "rings");
+  if (n_rings < 1) return fail(CSA2_ERR_INVALID_ARG, "n_rings < 1");
+  cudaError_t e = csa2::launch_ring_refill(entries, seq_len, B, n, ring_idx, n_rings, rings, S(stream));
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "ring_refill launch");
 }
 
 int csa2_quant_mxfp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales, void* stream) {
@@ -271,13 +297,14 @@ int csa2_indexer_full(const uint8_t* q_codes, const uint8_t* q_scales, const flo
                               ws_bytes - blockmax_ws(Q, max_ctx), stream);
 }
 
-int csa2_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len, int B, int n_q,
-                     const int32_t* block_table, int max_pages, int64_t n_pages,
-                     const uint8_t* main_pages, const uint8_t* rings, const int32_t* ring_idx,
-                     int64_t n_rings, float softmax_scale, int out_dtype, void* out, float* lse,
-                     void* ws, size_t ws_bytes, void* stream) {
-  if (int st = check_batch(B, n_q)) return st;
+static int sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len, int B, int n_q,
+                       const int32_t* block_table, int max_pages, int64_t n_pages,
+                       const uint8_t* main_pages, const uint8_t* rings, const int32_t* ring_idx,
+                       int64_t n_rings, const uint8_t* swa_chunk, float softmax_scale, int out_dtype,
+                       void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  if (int st = check_batch(B, n_q, swa_chunk ? CSA2_MAX_PREFILL_NQ : CSA2_MAX_NQ)) return st;
   if (B == 0) return CSA2_OK;
+  if (swa_chunk && !aligned16(swa_chunk)) return fail(CSA2_ERR_INVALID_ARG, "swa_chunk is not 16-byte aligned");
   CHECK_A16(q, "q");
   CHECK_PTR(topk, "topk");
   CHECK_PTR(seq_len, "seq_len");
@@ -293,12 +320,34 @@ int csa2_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len,
   if (!(softmax_scale > 0.f) || softmax_scale > 1e30f) return fail(CSA2_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
   const int64_t Q = static_cast<int64_t>(B) * n_q;
   const size_t need = csa2::attn_workspace_bytes(Q);
-  if (!ws || ws_bytes < need) return fail(CSA2_ERR_WORKSPACE, "sparse_attn needs %zu workspace bytes", need);
-  if (!aligned16(ws)) return fail(CSA2_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  if (need > 0) {
+    if (!ws || ws_bytes < need) return fail(CSA2_ERR_WORKSPACE, "sparse_attn needs %zu workspace bytes", need);
+    if (!aligned16(ws)) return fail(CSA2_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  }
   cudaError_t e = csa2::launch_sparse_attn(q, topk, seq_len, B, n_q, block_table, max_pages, n_pages,
-                                           main_pages, rings, ring_idx, n_rings, softmax_scale, out_dtype,
-                                           out, lse, ws, S(stream));
+                                           main_pages, rings, ring_idx, n_rings, swa_chunk, softmax_scale,
+                                           out_dtype, out, lse, ws, S(stream));
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "sparse_attn launch");
+}
+
+int csa2_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len, int B, int n_q,
+                     const int32_t* block_table, int max_pages, int64_t n_pages,
+                     const uint8_t* main_pages, const uint8_t* rings, const int32_t* ring_idx,
+                     int64_t n_rings, float softmax_scale, int out_dtype, void* out, float* lse,
+                     void* ws, size_t ws_bytes, void* stream) {
+  return sparse_attn(q, topk, seq_len, B, n_q, block_table, max_pages, n_pages, main_pages, rings, ring_idx,
+                     n_rings, nullptr, softmax_scale, out_dtype, out, lse, ws, ws_bytes, stream);
+}
+
+int csa2_sparse_attn_prefill(const void* q, const int32_t* topk, const int64_t* seq_len, int B,
+                             int n_q, const int32_t* block_table, int max_pages, int64_t n_pages,
+                             const uint8_t* main_pages, const uint8_t* rings,
+                             const int32_t* ring_idx, int64_t n_rings, const uint8_t* swa_chunk,
+                             float softmax_scale, int out_dtype, void* out, float* lse, void* ws,
+                             size_t ws_bytes, void* stream) {
+  CHECK_A16(swa_chunk, "swa_chunk");
+  return sparse_attn(q, topk, seq_len, B, n_q, block_table, max_pages, n_pages, main_pages, rings, ring_idx,
+                     n_rings, swa_chunk, softmax_scale, out_dtype, out, lse, ws, ws_bytes, stream);
 }
 
 static int run_layer(const csa2_layer_args* a, int32_t* pool, int32_t* topk, void* stream) {
@@ -325,9 +374,9 @@ static int run_layer(const csa2_layer_args* a, int32_t* pool, int32_t* topk, voi
     default:
       return fail(CSA2_ERR_INVALID_ARG, "unknown mode %d", a->mode);
   }
-  return csa2_sparse_attn(a->q, topk, a->seq_len, a->B, a->n_q, a->block_table, a->max_pages, a->n_pages,
-                          a->main_pages, a->rings, a->ring_idx, a->n_rings, a->softmax_scale, a->out_dtype,
-                          a->out, a->lse, a->ws, a->ws_bytes, stream);
+  return sparse_attn(a->q, topk, a->seq_len, a->B, a->n_q, a->block_table, a->max_pages, a->n_pages,
+                     a->main_pages, a->rings, a->ring_idx, a->n_rings, a->swa_chunk, a->softmax_scale,
+                     a->out_dtype, a->out, a->lse, a->ws, a->ws_bytes, stream);
 }
 
 int csa2_decode_layer(const csa2_layer_args* layer, void* stream) {

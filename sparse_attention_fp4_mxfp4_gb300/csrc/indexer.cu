@@ -13,8 +13,12 @@
 //
 // One kernel serves both uses:
 //   * Full scan: a tile is one 128-entry page; the epilogue reduces scores to
-//     the maximum over 8-position blocks. All n_q query tokens of a sequence
-//     share the tile: N = 32 * n_q MMA columns.
+//     the maximum over 8-position blocks. The query tokens of a sequence are
+//     cut into groups of at most 8 (one group at decode, many in a prefill
+//     chunk); a group's tokens share the tile: N = 32 * tokens MMA columns.
+//     A group walks the pages up to its last token's position, and CTAs of
+//     different groups that read the same pages run side by side, so the
+//     repeated reads of a prefill chunk come from L2.
 //   * Pool rescore (Reindex, and the end of Full): a tile is 16 pool blocks of
 //     8 positions, gathered block by block; the epilogue writes every score.
 //
@@ -34,6 +38,7 @@ constexpr int kStages = 5;
 constexpr int kTileBytes = 16 * 576;     // one indexer page / 16 pool blocks
 constexpr int kThreads = 192;
 constexpr int kIdxPageBytes = 16 * 576;
+constexpr int kGroup = 8;  // query tokens per scan CTA (N = 256 MMA columns)
 
 struct ScanParams {
   const uint8_t* q_codes;
@@ -41,6 +46,7 @@ struct ScanParams {
   const float* w;
   const int64_t* seq_len;
   int B, n_q;
+  int n_grp;  // scan: query groups of at most kGroup tokens per sequence
   const int32_t* block_table;
   int max_pages;
   int64_t n_pages;
@@ -86,7 +92,10 @@ template <bool kPool>
 __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int n_q = kPool ? 1 : P.n_q;
+  // Scan: this CTA's query group, tokens j0 .. j0 + n_q - 1 of its sequence.
+  const int grp = kPool ? 0 : static_cast<int>(blockIdx.y % P.n_grp);
+  const int j0 = grp * kGroup;
+  const int n_q = kPool ? 1 : (P.n_q - j0 < kGroup ? P.n_q - j0 : kGroup);
   const int n_cols = 32 * n_q;
   const TmemPlan plan = tmem_plan(n_q);
   uint8_t* stages = smem;                                   // kStages x 9216 B
@@ -132,8 +141,9 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
     if (n_tiles < 0) n_tiles = 0;
     tile_stride = 1;
   } else {
-    b = blockIdx.y;
-    const int64_t pages = (P.seq_len[b] + 127) >> 7;
+    b = blockIdx.y / P.n_grp;
+    const int64_t t_last = P.seq_len[b] - P.n_q + j0 + n_q - 1;  // the group's last position
+    const int64_t pages = t_last >= 0 ? (t_last + 128) >> 7 : 0;
     first_tile = blockIdx.x;
     tile_stride = gridDim.x;
     n_tiles = pages > first_tile ? (pages - first_tile + tile_stride - 1) / tile_stride : 0;
@@ -150,13 +160,13 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
   if (tid < 128) {
     for (int task = tid; task < n_cols * 4; task += 128) {
       const int n = task >> 2, c = task & 3;
-      const int jj = kPool ? jq : n >> 5, h = n & 31;
+      const int jj = kPool ? jq : j0 + (n >> 5), h = n & 31;
       const int64_t qrow = (static_cast<int64_t>(b) * P.n_q + jj) * 32 + h;
       const uint4 codes = *reinterpret_cast<const uint4*>(P.q_codes + qrow * 64 + c * 16);
       *reinterpret_cast<uint4*>(qbuf + ((n >> 3) * 4 + c) * 128 + (n & 7) * 16) = codes;
     }
     for (int i = tid; i < n_cols; i += 128) {
-      const int jj = kPool ? jq : i >> 5;
+      const int jj = kPool ? jq : j0 + (i >> 5);
       wsm[i] = P.w[(static_cast<int64_t>(b) * P.n_q + jj) * 32 + (i & 31)];
     }
     if (kPool) {
@@ -199,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
   if (warp < 4) {
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     for (int jj = 0; jj < n_q; ++jj) {
-      const int jt = kPool ? jq : jj;
+      const int jt = kPool ? jq : j0 + jj;
       const int64_t qrow = (static_cast<int64_t>(b) * P.n_q + jt) * 32 + lane;
       const uint8_t* sp = P.q_scales + qrow * 8;  // only 2-byte alignment is promised
       const uint32_t lo = sp[0] | (sp[1] << 8) | (sp[2] << 16) | (static_cast<uint32_t>(sp[3]) << 24);
@@ -326,14 +336,14 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
         }
         const float s = (s0 + s1) + (s2 + s3);
         if (!kPool) {
-          const int64_t t_q = seq_n - P.n_q + jj;
+          const int64_t t_q = seq_n - P.n_q + j0 + jj;
           const int64_t p = tile * 128 + tid;
           float m = (row_ok && p <= t_q) ? s : -INFINITY;
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
           if ((tid & 7) == 0 && row_ok && p <= t_q)
-            P.block_max[(static_cast<int64_t>(b) * P.n_q + jj) * P.max_blocks + (p >> 3)] = m;
+            P.block_max[(static_cast<int64_t>(b) * P.n_q + j0 + jj) * P.max_blocks + (p >> 3)] = m;
         } else {
           const bool causal = (tid & 7) < slot_n[i * 16 + (tid >> 3)];
           const float v = (row_ok && causal) ? s : -INFINITY;
@@ -443,10 +453,13 @@ cudaError_t launch_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales,
   p.idx_pages = idx_pages;
   p.block_max = block_max;
   p.max_blocks = max_blocks;
+  p.n_grp = (n_q + kGroup - 1) / kGroup;
+  const int tile_q = std::min(n_q, kGroup);
+  const int64_t rows = static_cast<int64_t>(B) * p.n_grp;
   const int64_t pages = (max_ctx + 127) / 128;
-  const int64_t target = static_cast<int64_t>(ctas_per_sm(n_q, 0)) * num_sms();
-  const int64_t per_seq = std::max<int64_t>(1, std::min<int64_t>(pages, (target + B - 1) / B));
-  return launch<false>(p, dim3(static_cast<unsigned>(per_seq), B), n_q, stream);
+  const int64_t target = static_cast<int64_t>(ctas_per_sm(tile_q, 0)) * num_sms();
+  const int64_t per_seq = std::max<int64_t>(1, std::min<int64_t>(pages, (target + rows - 1) / rows));
+  return launch<false>(p, dim3(static_cast<unsigned>(per_seq), static_cast<unsigned>(rows)), tile_q, stream);
 }
 
 cudaError_t launch_pool_scores(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
@@ -469,6 +482,7 @@ cudaError_t launch_pool_scores(const uint8_t* q_codes, const uint8_t* q_scales, 
   p.idx_pages = idx_pages;
   p.pool = pool;
   p.scores = scores;
+  p.n_grp = 1;
   // The 128 tiles of a token are cut into equal runs so that all CTAs are
   // resident at once (one wave) where the batch allows it; a run's slot table
   // is sized to the run, so short runs leave room for more CTAs per SM.

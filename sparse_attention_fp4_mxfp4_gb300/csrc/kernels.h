@@ -22,8 +22,12 @@ cudaError_t launch_append_kv(const void* latent, const void* idx_key, const int3
                              const int64_t* pos, int T, const int32_t* block_table, int B,
                              int max_pages, int64_t n_pages, uint8_t* main_pages,
                              uint8_t* idx_pages, cudaStream_t stream);
+// ring_idx == NULL: E4M3 of T entries into rings viewed as [T, 512] (pos unused).
 cudaError_t launch_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, int T,
                               int64_t n_rings, uint8_t* rings, cudaStream_t stream);
+// The last min(n, 128) of n E4M3 entries per sequence into their ring slots.
+cudaError_t launch_ring_refill(const uint8_t* entries, const int64_t* seq_len, int B, int n,
+                               const int32_t* ring_idx, int64_t n_rings, uint8_t* rings, cudaStream_t stream);
 cudaError_t launch_quant_mxfp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales,
                                cudaStream_t stream);
 cudaError_t launch_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t n,
@@ -54,8 +58,8 @@ size_t attn_workspace_bytes(int64_t queries);
 cudaError_t launch_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len, int B,
                                int n_q, const int32_t* block_table, int max_pages,
                                int64_t n_pages, const uint8_t* main_pages, const uint8_t* rings,
-                               const int32_t* ring_idx, int64_t n_rings, float softmax_scale,
-                               int out_dtype, void* out, float* lse, void* ws,
+                               const int32_t* ring_idx, int64_t n_rings, const uint8_t* swa_chunk,
+                               float softmax_scale, int out_dtype, void* out, float* lse, void* ws,
                                cudaStream_t stream);
 
 }  // namespace csa2

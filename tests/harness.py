@@ -24,6 +24,13 @@ TOL_ATTN_F32 = 2e-3    # max over channels |o - r| / max |r|, per (query, head)
 # (reached just above a power of two), and |o| <= (1 + 2e-3) max |r|.
 TOL_ATTN_BF16 = TOL_ATTN_F32 + 2.0 ** -8 * (1 + TOL_ATTN_F32)
 TOPK_TIE_RTOL = 1e-5   # selections may differ only among scores this close to the k-th
+# Log-sum-exp (natural log), absolute: the kernel rounds every p = 2^(l - m) to
+# f16 and its normaliser sums exactly those rounded values, so the sum carries
+# a relative error of at most 2^-11 (half an f16 ulp; p >= 2^-14 stays normal
+# except for negligible keys, which add at most 640 * 2^-25), plus fp32
+# accumulation (the relative 1e-5 the tests add covers the logits' fp32 dot
+# products). With few keys the roundings do not average out.
+TOL_LSE = 2.0 ** -11 + 640 * 2.0 ** -25 + 1e-5
 
 
 def u16_to_bf16(a: np.ndarray, device) -> torch.Tensor:
@@ -106,8 +113,10 @@ def build(wl: Workload, device="cuda", *, N=None, B=None, n_q=None, shuffle_seed
             seq = torch.full((n,), b, dtype=torch.int32, device=device)
             pos = torch.arange(p0, p0 + n, dtype=torch.int64, device=device)
             csa2.csa2_append_kv(lat, key, seq, pos, cache.block_table, cache.main_pages, cache.idx_pages)
-    # Window entries of the positions already in the cache, one ring per (layer, sequence).
-    lo = max(0, N - 128)
+    # Window entries of the 128 positions before the step's tokens, one ring per
+    # (layer, sequence): the ring state a prefill chunk starts from; a decode
+    # step's appends then leave positions N-128 .. N-1.
+    lo = max(0, pre - 128)
     for li in range(n_layers):
         for b in range(Bq):
             if pre > lo:
@@ -179,9 +188,15 @@ class Runner:
     step's appends (A1, A2), then every layer in order. A FULL layer quantises
     its indexer query, scans, selects the pool and the top-512; a REINDEX
     layer quantises its query and rescores its pool; every layer then runs
-    sparse attention with the latest top-k, its own query and its own ring."""
+    sparse attention with the latest top-k, its own query and its own ring.
 
-    def __init__(self, S: Setup, out_dtype=torch.bfloat16):
+    prefill=True runs the step's n_q tokens as one prefill chunk instead: each
+    layer's window entries of the chunk are encoded to E4M3 into a chunk
+    buffer (not the ring), the attention takes every token's exact causal
+    window from that buffer and the ring, and each layer's ring is refilled
+    with the chunk's last 128 entries after its attention."""
+
+    def __init__(self, S: Setup, out_dtype=torch.bfloat16, prefill=False):
         import sparse_attention_fp4_mxfp4_gb300 as csa2
         self.csa2 = csa2
         self.S = S
@@ -203,8 +218,10 @@ class Runner:
         # The attention launch splits a token's five key chunks over several
         # CTAs (plus a merge kernel) only while there are fewer tokens than SMs.
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        self.attn_launches = 1 if min(5, max(1, sms // Q)) == 1 else 2
+        self.attn_launches = 1 if Q >= 256 or min(5, max(1, sms // Q)) == 1 else 2
         self.side = None
+        self.prefill = prefill
+        self.chunk = [torch.empty(B, n_q, 512, dtype=torch.uint8, device=dev) for _ in S.layers] if prefill else None
 
     def step(self, mark=None):
         """The window-ring appends and the indexer-query quantisations do not
@@ -221,7 +238,10 @@ class Runner:
         s_q.wait_stream(main)
         with torch.cuda.stream(s_swa):
             for li in range(len(S.layers)):
-                csa2.csa2_append_swa(S.step_swa[li], S.step_ring_idx[li], S.step_pos, c.rings)
+                if self.prefill:
+                    csa2.csa2_quant_fp8_entries(S.step_swa[li], self.chunk[li])
+                else:
+                    csa2.csa2_append_swa(S.step_swa[li], S.step_ring_idx[li], S.step_pos, c.rings)
         with torch.cuda.stream(s_q):
             for L in S.layers:
                 if L.kind in ("full", "reindex"):
@@ -253,10 +273,18 @@ class Runner:
                 main.wait_stream(s_swa)
                 swa_joined = True
             mark("attn0")
-            csa2.csa2_sparse_attn(L.q, self.topk, S.seq_len, c.block_table, c.n_pages, c.main_pages, c.rings,
-                                  L.ring_idx, self.out[li], self.lse[li], self.ws)
+            if self.prefill:
+                csa2.csa2_sparse_attn_prefill(L.q, self.topk, S.seq_len, c.block_table, c.n_pages, c.main_pages,
+                                              c.rings, L.ring_idx, self.chunk[li], self.out[li], self.lse[li],
+                                              self.ws)
+            else:
+                csa2.csa2_sparse_attn(L.q, self.topk, S.seq_len, c.block_table, c.n_pages, c.main_pages, c.rings,
+                                      L.ring_idx, self.out[li], self.lse[li], self.ws)
             mark("attn1")
             n += self.attn_launches
+            if self.prefill:
+                csa2.csa2_ring_refill(self.chunk[li], S.seq_len, L.ring_idx, c.rings)
+                n += 1
         self.launches = n
 
 
@@ -282,14 +310,16 @@ def oracle_reindex(S: Setup, b: int, j: int, li: int, pool_row, keys=None):
     return oracle.reindex(L.q_idx_u16[b, j], L.w_np[b, j], keys, t, np.asarray(pool_row, np.int32))
 
 
-def oracle_attention(S: Setup, b: int, j: int, li: int, topk_row):
+def oracle_attention(S: Setup, b: int, j: int, li: int, topk_row, exact_window=False):
+    """exact_window: the prefill window (all of max(0, t-127) .. t), which is
+    the decode window of a context that ends at t."""
     import oracle
     seed = S.wl.seed
     t = S.t(j)
     sel = np.asarray(topk_row)
     sel = sel[sel >= 0].astype(np.int64)
     main = synth.latent_rows(seed, np.full(sel.size, b), sel)
-    win = oracle.window_positions(t, S.N, 128)
+    win = oracle.window_positions(t, t + 1 if exact_window else S.N, 128)
     wrows = synth.latent_rows(seed, np.full(win.size, b), win, tensor=synth.SWA + li)
     return oracle.sparse_attention(S.layers[li].q_u16[b, j], main, wrows, TAU)
 

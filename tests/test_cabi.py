@@ -55,8 +55,42 @@ def test_size_queries(lib):
     assert lib.csa2_workspace_bytes(3, 64, 1, 65536, ctypes.byref(n)) == 0
     assert n.value == 64 * 5 * 64 * 512 * 4 + 64 * 5 * 64 * 8
     assert lib.csa2_workspace_bytes(2, 64, 1, 131072, ctypes.byref(n)) == 0 and n.value == 64 * 16384 * 4
-    assert lib.csa2_workspace_bytes(3, 1, 9, 100, ctypes.byref(n)) == 2  # n_q > 8 unsupported
     assert lib.csa2_workspace_bytes(3, 1, 0, 100, ctypes.byref(n)) == 1
+    # Prefill shapes: up to 4096 tokens per sequence and 65535 per call; the
+    # attention needs no partial-output workspace from 256 tokens on.
+    assert lib.csa2_workspace_bytes(3, 1, 4096, 100, ctypes.byref(n)) == 0 and n.value == 0
+    assert lib.csa2_workspace_bytes(3, 1, 255, 100, ctypes.byref(n)) == 0
+    assert n.value == 255 * 5 * 64 * 512 * 4 + 255 * 5 * 64 * 8
+    assert lib.csa2_workspace_bytes(2, 2, 1000, 100, ctypes.byref(n)) == 0 and n.value == 2000 * 16384 * 4
+    assert lib.csa2_workspace_bytes(3, 1, 4097, 100, ctypes.byref(n)) == 2
+    assert lib.csa2_workspace_bytes(3, 17, 4000, 100, ctypes.byref(n)) == 2  # 68000 tokens
+
+
+def test_prefill_and_refill_host_checks(lib):
+    p, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.csa2_last_error.restype = ctypes.c_char_p
+    lib.csa2_sparse_attn.argtypes = [p, p, p, i32, i32, p, i32, i64, p, p, p, i64, f32, i32, p, p, p, sz, p]
+    lib.csa2_sparse_attn_prefill.argtypes = [p, p, p, i32, i32, p, i32, i64, p, p, p, i64, p, f32, i32, p, p, p,
+                                             sz, p]
+    x = p(4096)  # an aligned non-null address; no call below reaches the device
+    # The decode attention keeps its 8-token limit (its window comes from the ring alone).
+    assert lib.csa2_sparse_attn(x, x, x, 1, 9, x, 1, 1, x, x, x, 1, 0.05, 0, x, None, None, 0, None) == 2
+    assert lib.csa2_sparse_attn_prefill(x, x, x, 1, 9, x, 1, 1, x, x, x, 1, None, 0.05, 0, x, None, None, 0,
+                                        None) == 1
+    assert b"swa_chunk" in lib.csa2_last_error()
+    assert lib.csa2_sparse_attn_prefill(x, x, x, 1, 9, x, 1, 1, x, x, x, 1, p(4100), 0.05, 0, x, None, None, 0,
+                                        None) == 1
+    assert lib.csa2_sparse_attn_prefill(x, x, x, 1, 4097, x, 1, 1, x, x, x, 1, x, 0.05, 0, x, None, None, 0,
+                                        None) == 2
+    lib.csa2_ring_refill.argtypes = [p, p, i32, i32, p, i64, p, p]
+    assert lib.csa2_ring_refill(None, None, 1, 0, None, 1, None, None) == 0  # nothing to do
+    assert lib.csa2_ring_refill(None, x, 1, 4, x, 1, x, None) == 1
+    assert b"entries" in lib.csa2_last_error()
+    assert lib.csa2_ring_refill(x, x, 1, 4, x, 0, x, None) == 1
+    assert lib.csa2_ring_refill(x, x, 1, -1, x, 1, x, None) == 1
+    lib.csa2_quant_fp8_entries.argtypes = [p, i32, p, p]
+    assert lib.csa2_quant_fp8_entries(p(4104), 2, x, None) == 1
+    assert lib.csa2_quant_fp8_entries(None, 0, None, None) == 0
 
 
 def test_status_strings_and_null_checks(lib):
