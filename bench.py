@@ -9,7 +9,10 @@ rescore + top-512, and sparse attention over 512 FP4 entries + the 128-entry
 FP8 window (64 heads x 512, bf16 output).
 
 Default workload: 8 sequences x 1,048,576 context entries, 1 query token
-each (Full mode at 1M context). Other workloads: --workload 0..4.
+each (Full mode at 1M context). Other workloads: --workload 0..4, and
+--workload 5, a chunked-prefill step (4096 new tokens of one sequence at
+128K context through a Full layer, each token with its exact causal window;
+reported in tokens/s).
 
 Prints one JSON line (rank 0). `--impl reference` times the CPU oracle on
 the same workload instead (a bounded sample, scaled to queries/s).
@@ -34,14 +37,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode queries/s per CSA2 mode at context N; % of HBM roofline (1xGB300)"
+METRIC_PREFILL = "chunked-prefill tokens/s of a CSA2 Full layer at context N; % of the scan's ALU roofline (1xGB300)"
 
 # ncu DRAM traffic of the dominant kernel, per launch, with the hash of the
 # sources it was measured on (reported as null once those sources change).
 NCU_TRAFFIC = {
-    # profiles/indexer_scan_b4_n1m.txt: 303.26 MB read + 6.55 MB written for 4 x 1M
+    # profiles/indexer_scan_b4_n1m.txt: 303.69 MB read + 5.87 MB written for 4 x 1M
     # positions; traffic grows with the positions scanned, so x2 for 8 x 1M.
-    ("indexer_scan", 3): {"bytes_per_launch": 2 * (303.259904e6 + 6.548224e6),
-                          "files": ['indexer.cu', 'sm103.cuh'], "hash": "e4d217a66c448aa2"},
+    ("indexer_scan", 3): {"bytes_per_launch": 2 * (303.685376e6 + 5.872384e6),
+                          "files": ['indexer.cu', 'sm103.cuh'], "hash": "47893677ae65ae02"},
 }
 
 
@@ -149,6 +153,32 @@ def scan_bytes(wl) -> int:
     return wl.B * (72 * wl.N + wl.n_q * (32 * 72 + 32 * 4))
 
 
+def causal_positions(wl) -> int:
+    """Positions scored by the Full scan per step: sum over tokens of t + 1."""
+    t0 = wl.N - wl.n_q
+    return wl.B * (wl.n_q * (t0 + 1) + wl.n_q * (wl.n_q - 1) // 2)
+
+
+def scan_alu_ops(wl) -> int:
+    """fp32 ALU operations the Full scan's score needs per step: for each
+    causal (position, token) and each of 32 heads, a ReLU (max) and a
+    weighted accumulation (fma)."""
+    return causal_positions(wl) * 32 * 2
+
+
+def alu_peak(dev) -> float:
+    """fp32 lane operations per second: SMs x 128 lanes x the SM clock limit."""
+    props = torch.cuda.get_device_properties(dev)
+    mhz = None
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={dev.index or 0}", "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+        mhz = float(out.stdout.strip().splitlines()[0])
+    except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+        mhz = 2070.0
+    return props.multi_processor_count * 128 * mhz * 1e6
+
+
 def attn_bytes_per_query() -> int:
     # 512 FP4 entries x 288 B + 128 FP8 window entries x 512 B + q (64 x 512 bf16) + top-k.
     return 512 * 288 + 128 * 512 + 64 * 512 * 2 + 512 * 4
@@ -203,7 +233,7 @@ def run_ours(args, wl, rank, world, local):
         dist.init_process_group("nccl", device_id=dev)
     t_setup = time.time()
     S = H.build(wl, dev)
-    R = H.Runner(S)
+    R = H.Runner(S, prefill=wl.prefill)
     torch.cuda.synchronize()
     setup_s = time.time() - t_setup
     B, n_q, N = wl.B, wl.n_q, wl.N
@@ -293,13 +323,26 @@ def run_ours(args, wl, rank, world, local):
     rec = NCU_TRAFFIC.get((dom, wl.index))
     if rec and rec["hash"] == source_hash(rec["files"]):
         traffic = rec["bytes_per_launch"]
+    roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+            "algorithmic_bytes_per_launch": dom_bytes, "peak_source": peak_kind}
+    if wl.prefill:
+        # A prefill chunk re-reads the same pages for every group of 8 tokens
+        # (from L2): the scan is bound by the fp32 ALU work of its scores.
+        ops = scan_alu_ops(wl)
+        apk = alu_peak(dev)
+        ach = ops / (launch_ms * 1e-3) / 1e12 if launch_ms else None
+        roof = {"bound": "alu", "kernel": dom, "achieved": ach, "peak": apk / 1e12, "unit": "Top/s",
+                "frac": (ach * 1e12 / apk) if ach else None, "traffic": traffic,
+                "algorithmic_ops_per_launch": ops, "peak_source": "derived: SMs x 128 fp32 lanes x max SM clock",
+                "tensor_flops_per_launch": causal_positions(wl) * 32 * 128 * 2}
     total_q = sum_over_ranks(float(Q), world, dev)
     value = total_q / (ms_max * 1e-3)
     sb = step_bytes(wl)
     line = {
-        "metric": METRIC,
+        "metric": METRIC_PREFILL if wl.prefill else METRIC,
         "value": value,
-        "unit": "queries/s",
+        "unit": "tokens/s" if wl.prefill else "queries/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -310,7 +353,7 @@ def run_ours(args, wl, rank, world, local):
         "dtype": "fp4(e2m1)+e4m3 storage, f16 tensor-core operands, fp32 accumulate/softmax, bf16 out",
         "data": "synthetic (seeded generator; RMSNormed post-RoPE latents, N(0,1) indexer keys/queries)",
         "config": {"workload": wl.name, "mode": wl.mode, "layers": list(kinds), "batch": B, "context": N,
-                   "query_tokens": n_q, "queries_per_step": Q,
+                   "query_tokens": n_q, "queries_per_step": Q, "prefill": wl.prefill,
                    "l2": "inputs larger than L2 (store of %.1f GB; the step reads %.0f MB)" % (
                        S.cache.nbytes() / 1e9, step_bytes(wl) / 1e6),
                    "parallelism": f"replicas x{world} (independent sequences)", "setup_s": round(setup_s, 1),
@@ -319,9 +362,7 @@ def run_ours(args, wl, rank, world, local):
         "hbm_fraction_step": (sb / (ms_max * 1e-3) / 1e9) / peak,
         "stage_ms": stage_ms,
         "stage_roofline": stage_roofline(wl, kinds, stage_ms, peak),
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": (achieved / peak) if achieved else None, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": dom_bytes, "peak_source": peak_kind},
+        "roofline": roof,
         "clocks": clk,
         "gpu_launches": R.launches * args.steps,
         "e2e": e2e,
@@ -357,7 +398,8 @@ def run_e2e(args, wl, S, R, dev):
             ring_idx=L.ring_idx, q=dev_in[f"q{li}"], out=R.out[li], ws=R.ws, lse=R.lse[li],
             q_idx_codes=L.q_codes, q_idx_scales=L.q_scales, w=dev_in.get(f"w{li}"),
             pool=R.pool if L.kind == "full" else L.pool if L.kind == "reindex" else None,
-            topk=R.topk if L.kind != "reuse" or li == 0 else None))
+            topk=R.topk if L.kind != "reuse" or li == 0 else None,
+            swa_chunk=R.chunk[li] if wl.prefill else None))
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(o.numel() * o.element_size() for o in outs_h) + sum(x.numel() * 4 for x in lses_h)
 
@@ -367,10 +409,16 @@ def run_e2e(args, wl, S, R, dev):
         csa2.csa2_append_kv(dev_in["latent"], dev_in["key"], S.step_seq, S.step_pos, c.block_table,
                             c.main_pages, c.idx_pages)
         for li, L in enumerate(S.layers):
-            csa2.csa2_append_swa(dev_in[f"swa{li}"], S.step_ring_idx[li], S.step_pos, c.rings)
+            if wl.prefill:
+                csa2.csa2_quant_fp8_entries(dev_in[f"swa{li}"], R.chunk[li])
+            else:
+                csa2.csa2_append_swa(dev_in[f"swa{li}"], S.step_ring_idx[li], S.step_pos, c.rings)
             if L.q_idx is not None:
                 csa2.csa2_quant_mxfp4(dev_in[f"qi{li}"], L.q_codes, L.q_scales)
         csa2.csa2_decode_group(args_list)
+        if wl.prefill:
+            for li, L in enumerate(S.layers):
+                csa2.csa2_ring_refill(R.chunk[li], S.seq_len, L.ring_idx, c.rings)
         for li in range(len(S.layers)):
             outs_h[li].copy_(R.out[li], non_blocking=True)
             lses_h[li].copy_(R.lse[li], non_blocking=True)
@@ -387,7 +435,8 @@ def run_e2e(args, wl, S, R, dev):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    return {"value": wl.B * wl.n_q / (ms * 1e-3), "unit": "queries/s", "ms_per_step": ms, "steps": steps,
+    return {"value": wl.B * wl.n_q / (ms * 1e-3), "unit": "tokens/s" if wl.prefill else "queries/s",
+            "ms_per_step": ms, "steps": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
@@ -434,7 +483,8 @@ def oracle_query(wl, b=0, j=0, n_scan=None):
     sel = np.asarray(sel)
     sel = sel[sel >= 0].astype(np.int64)
     main = synth.latent_rows(seed, np.full(sel.size, b), sel)
-    win = oracle.window_positions(t, N, 128)
+    # A prefill token's window is exact: the decode window of a context ending at t.
+    win = oracle.window_positions(t, t + 1 if wl.prefill else N, 128)
     wrows = synth.latent_rows(seed, np.full(win.size, b), win, tensor=synth.SWA + li)
     t0 = time.perf_counter()
     oracle.sparse_attention(q, main, wrows, 1.0 / math.sqrt(512))
@@ -453,7 +503,8 @@ def cpu_baseline(wl, budget_s=12.0):
         _, s, desc = oracle_query(wl, b=b, j=j)
         spent += s
         done += 1
-    return {"value": done / spent, "unit": "queries/s", "cores": oracle.THREADS, "kind": "oracle",
+    unit = "tokens/s" if wl.prefill else "queries/s"
+    return {"value": done / spent, "unit": unit, "cores": oracle.THREADS, "kind": "oracle",
             "sample": f"{done} queries of the workload in (sequence, token) order, each: " + desc,
             "oracle_s": round(spent, 2), "wall_s": round(time.perf_counter() - wall, 1)}
 
@@ -481,14 +532,16 @@ def run_reference(args, wl, rank, world):
         scaled.append(s)
     sec = sum(scaled) / len(scaled)
     v = 1.0 / sec
+    unit = "tokens/s" if wl.prefill else "queries/s"
     return {
-        "impl": "reference", "metric": METRIC, "value": v, "unit": "queries/s", "n_gpus": world,
+        "impl": "reference", "metric": METRIC_PREFILL if wl.prefill else METRIC, "value": v, "unit": unit,
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded generator)",
         "config": {"workload": wl.name, "mode": wl.mode, "batch": wl.B, "context": wl.N, "query_tokens": wl.n_q},
-        "cpu_baseline": {"value": v, "unit": "queries/s", "cores": oracle.THREADS, "kind": "oracle",
+        "cpu_baseline": {"value": v, "unit": unit, "cores": oracle.THREADS, "kind": "oracle",
                          "sample": desc + " (one query per step)"},
-        "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
@@ -505,15 +558,17 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--B", type=int, default=None, help="override the batch (profiling captures only)")
     ap.add_argument("--N", type=int, default=None, help="override the context (profiling captures only)")
+    ap.add_argument("--nq", type=int, default=None, help="override the query tokens (profiling captures only)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     from synth.workloads import WORKLOADS
     wl = WORKLOADS[args.workload]
-    if args.B or args.N:
+    if args.B or args.N or args.nq:
         from synth.workloads import Workload
-        wl = Workload(wl.index, wl.name + f"_B{args.B or wl.B}_N{args.N or wl.N}", wl.mode, B=args.B or wl.B,
-                      N=args.N or wl.N, n_q=wl.n_q, layers=wl.layers)
+        wl = Workload(wl.index, wl.name + f"_B{args.B or wl.B}_N{args.N or wl.N}_q{args.nq or wl.n_q}", wl.mode,
+                      B=args.B or wl.B, N=args.N or wl.N, n_q=args.nq or wl.n_q, layers=wl.layers,
+                      prefill=wl.prefill)
     rank, world, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, wl, rank, world)

@@ -14,18 +14,21 @@
 // One kernel serves both uses:
 //   * Full scan: a tile is one 128-entry page; the epilogue reduces scores to
 //     the maximum over 8-position blocks. The query tokens of a sequence are
-//     cut into groups of at most 8 (one group at decode, many in a prefill
-//     chunk); a group's tokens share the tile: N = 32 * tokens MMA columns.
-//     A group walks the pages up to its last token's position, and CTAs of
-//     different groups that read the same pages run side by side, so the
-//     repeated reads of a prefill chunk come from L2.
+//     cut into groups (one group of up to 8 at decode; groups of 7 in a
+//     prefill chunk); a group's tokens share the tile: N = 32 * tokens MMA
+//     columns. A group walks the pages up to its last token's position, and
+//     CTAs of different groups that read the same pages run side by side, so
+//     the repeated reads of a prefill chunk come from L2.
 //   * Pool rescore (Reindex, and the end of Full): a tile is 16 pool blocks of
 //     8 positions, gathered block by block; the epilogue writes every score.
 //
-// Per CTA: warp 4 streams tiles into a ring of shared-memory stages with bulk
-// copies; warps 0-3 move each row's 8 scale bytes into TMEM and run the
-// epilogue of the previous tile; warp 5 issues the two K = 64 MMAs of a tile
-// (M = 128 positions) straight from the stage.
+// Per CTA: warp E streams tiles into a ring of shared-memory stages with bulk
+// copies; warps 0-3 move each row's 8 scale bytes into TMEM; warps 0..E-1 run
+// the epilogue (warp w reads TMEM lane quarter w % 4, i.e. rows 32 (w % 4) ..
+// +31, for the tokens j = w / 4 (mod E / 4)); warp E + 1 issues the two
+// K = 64 MMAs of a tile (M = 128 positions) straight from the stage. E = 4 at
+// decode and in the pool rescore; E = 16 for a prefill chunk, whose 7 tokens
+// per tile make the epilogue's fp32 work the bound.
 #include <algorithm>
 
 #include "kernels.h"
@@ -36,9 +39,13 @@ namespace {
 
 constexpr int kStages = 5;
 constexpr int kTileBytes = 16 * 576;     // one indexer page / 16 pool blocks
-constexpr int kThreads = 192;
 constexpr int kIdxPageBytes = 16 * 576;
-constexpr int kGroup = 8;  // query tokens per scan CTA (N = 256 MMA columns)
+constexpr int kGroup = 8;      // decode: query tokens per scan CTA (N <= 256 MMA columns)
+constexpr int kWideGroup = 7;  // prefill: tokens per scan CTA (two N = 224 accumulators fit TMEM)
+constexpr int kWideSub = 4;    // prefill: epilogue warps per TMEM lane quarter
+
+// Epilogue warps 4 * kSub, then the producer and the MMA warp.
+__host__ __device__ constexpr int threads_for(int kSub) { return 32 * (4 * kSub + 2); }
 
 struct ScanParams {
   const uint8_t* q_codes;
@@ -46,7 +53,8 @@ struct ScanParams {
   const float* w;
   const int64_t* seq_len;
   int B, n_q;
-  int n_grp;  // scan: query groups of at most kGroup tokens per sequence
+  int n_grp;     // scan: query groups per sequence
+  int grp_size;  // scan: tokens per group (the last group may hold fewer)
   const int32_t* block_table;
   int max_pages;
   int64_t n_pages;
@@ -69,7 +77,7 @@ struct TmemPlan {
 
 __host__ __device__ constexpr TmemPlan tmem_plan(int n_q) {
   const uint32_t n = 32u * n_q;
-  const uint32_t nacc = n <= 128 ? 2u : 1u;
+  const uint32_t nacc = 2u * n + 32u <= 512u ? 2u : 1u;
   const uint32_t sf = (nacc * n + 31u) & ~31u;
   uint32_t cols = 32;
   while (cols < sf + 32u) cols <<= 1;
@@ -88,14 +96,27 @@ __host__ __device__ constexpr int smem_bytes_for(int n_q, int pool_tiles) {
          pool_table_bytes(pool_tiles);
 }
 
-template <bool kPool>
-__global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P) {
+// fp32 fused multiply-add of two lanes at once (each lane an IEEE fma.rn).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+template <bool kPool, int kSub>
+__global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_kernel(const ScanParams P) {
+  static_assert(!kPool || kSub == 1, "the pool rescore has one token per CTA");
+  constexpr int kEpi = 4 * kSub;  // epilogue warps; producer = warp kEpi, MMA issuer = warp kEpi + 1
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // Scan: this CTA's query group, tokens j0 .. j0 + n_q - 1 of its sequence.
   const int grp = kPool ? 0 : static_cast<int>(blockIdx.y % P.n_grp);
-  const int j0 = grp * kGroup;
-  const int n_q = kPool ? 1 : (P.n_q - j0 < kGroup ? P.n_q - j0 : kGroup);
+  const int j0 = grp * P.grp_size;
+  const int n_q = kPool ? 1 : (P.n_q - j0 < P.grp_size ? P.n_q - j0 : P.grp_size);
   const int n_cols = 32 * n_q;
   const TmemPlan plan = tmem_plan(n_q);
   uint8_t* stages = smem;                                   // kStages x 9216 B
@@ -122,12 +143,12 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
     for (int i = 0; i < 2; ++i) {
       mbar_init(sfull0 + 8 * i, 128);
       mbar_init(dfull0 + 8 * i, 1);
-      mbar_init(dempty0 + 8 * i, 128);
+      mbar_init(dempty0 + 8 * i, 32 * kEpi);
     }
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), plan.ncols);
+  if (warp == kEpi + 1) tmem_alloc(smem_u32(tmem_slot), plan.ncols);
   griddep_wait();  // everything below may read what earlier kernels wrote
   griddep_launch();
   int b, jq = 0;  // sequence, query token (pool mode)
@@ -223,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
   __syncthreads();
   tc_fence_after();
 
-  if (warp == 4) {
+  if (warp == kEpi) {
     // ---- producer (whole warp: lookups in parallel, one bulk copy per lane) ----
     int32_t next_pages = -1;  // scan: page id of tile (i & ~31) + lane
     const int nt = static_cast<int>(n_tiles);
@@ -270,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
                    576, full0 + 8 * s);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kEpi + 1) {
     // ---- MMA issuer ----
     if (lane == 0) {
       const uint32_t idesc = idesc_mxf4nvf4(128, n_cols);
@@ -307,95 +328,127 @@ __global__ void __launch_bounds__(kThreads, 4) indexer_kernel(const ScanParams P
         mbar_wait(dfull0 + 8 * (two ? ((issued - 1) & 1) : 0), (two ? ((issued - 1) >> 1) : (issued - 1)) & 1, 213);
     }
   } else {
-    // ---- scales to TMEM + epilogue (warps 0-3, thread t <-> row t) ----
-    uint32_t valid_rows[2] = {0, 0};  // per 8-row group, tiles i and i-1
+    // ---- scales to TMEM (warps 0-3, thread t <-> row t) + epilogue ----
+    const int quarter = warp & 3, sub = warp >> 2;
+    const int row = quarter * 32 + lane;  // the tile row (TMEM lane) this thread owns
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t valid_rows[2] = {0, 0};  // kSub == 1: per 8-row group, tiles i and i-1 (from the stage)
+    int32_t next_pages = -1;          // kSub > 1: page ids of tiles (i & ~31) + lane
     const bool two = plan.nacc == 2;
+    // This warp's tokens of the group: j = sub, sub + kSub, ...
+    const int mine = sub < n_q ? (n_q - sub + kSub - 1) / kSub : 0;
     auto epilogue = [&](int i) -> bool {
       const int acc = two ? (i & 1) : 0;
+      bool row_ok;
+      if (kSub == 1) {
+        row_ok = (valid_rows[i & 1] >> (row >> 3)) & 1u;
+      } else {
+        // A wide CTA's epilogue warps run up to two tiles behind the
+        // producer's stage bookkeeping, so they look the page up themselves.
+        if ((i & 31) == 0) {
+          const int64_t tl = first_tile + (i + lane) * tile_stride;
+          next_pages = (i + lane < n_tiles && tl < P.max_pages)
+                           ? P.block_table[static_cast<int64_t>(b) * P.max_pages + tl] : -1;
+        }
+        const int32_t page = __shfl_sync(0xffffffffu, next_pages, i & 31);
+        row_ok = page >= 0 && page < P.n_pages;
+      }
       if (!mbar_wait(dfull0 + 8 * acc, (two ? (i >> 1) : i) & 1, 221, abort_flag)) return false;
       tc_fence_after();
       const int64_t tile = first_tile + i * tile_stride;
-      const bool row_ok = (valid_rows[i & 1] >> (tid >> 3)) & 1u;
-      for (int jj = 0; jj < n_q; ++jj) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * n_cols + jj * 32, r);
-        tmem_wait_ld();
-        if (jj == n_q - 1) {
-          tc_fence_before();
-          mbar_arrive(dempty0 + 8 * acc);
-        }
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      // The score of this thread's row for token jj from its 32 head dot products.
+      auto finish = [&](const uint32_t (&r)[32], int jj) {
+        // Heads h = 0, 1, 2, 3 (mod 4) in four fp32 sums, two per packed fma.
+        float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
         const float4* wj = reinterpret_cast<const float4*>(wsm + jj * 32);  // 16-byte aligned
 #pragma unroll
         for (int h = 0; h < 32; h += 4) {
           const float4 wv = wj[h >> 2];
-          s0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.f), s0);
-          s1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
-          s2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
-          s3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
+          a01 = ffma2(make_float2(fmaxf(__uint_as_float(r[h]), 0.f), fmaxf(__uint_as_float(r[h + 1]), 0.f)),
+                      make_float2(wv.x, wv.y), a01);
+          a23 = ffma2(make_float2(fmaxf(__uint_as_float(r[h + 2]), 0.f), fmaxf(__uint_as_float(r[h + 3]), 0.f)),
+                      make_float2(wv.z, wv.w), a23);
         }
-        const float s = (s0 + s1) + (s2 + s3);
+        const float s = (a01.x + a01.y) + (a23.x + a23.y);
         if (!kPool) {
           const int64_t t_q = seq_n - P.n_q + j0 + jj;
-          const int64_t p = tile * 128 + tid;
+          const int64_t p = tile * 128 + row;
           float m = (row_ok && p <= t_q) ? s : -INFINITY;
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-          if ((tid & 7) == 0 && row_ok && p <= t_q)
+          if ((row & 7) == 0 && row_ok && p <= t_q)
             P.block_max[(static_cast<int64_t>(b) * P.n_q + j0 + jj) * P.max_blocks + (p >> 3)] = m;
         } else {
-          const bool causal = (tid & 7) < slot_n[i * 16 + (tid >> 3)];
+          const bool causal = (row & 7) < slot_n[i * 16 + (row >> 3)];
           const float v = (row_ok && causal) ? s : -INFINITY;
-          P.scores[(static_cast<int64_t>(b) * P.n_q + jq) * 16384 + tile * 128 + tid] = v;
+          P.scores[(static_cast<int64_t>(b) * P.n_q + jq) * 16384 + tile * 128 + row] = v;
         }
+      };
+      if (mine == 0) {
+        tc_fence_before();
+        mbar_arrive(dempty0 + 8 * acc);
+      }
+      for (int k = 0; k < mine; ++k) {
+        const int jj = sub + k * kSub;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + acc * n_cols + jj * 32, r);
+        tmem_wait_ld();
+        if (k == mine - 1) {
+          tc_fence_before();
+          mbar_arrive(dempty0 + 8 * acc);
+        }
+        finish(r, jj);
       }
       return true;
     };
     bool ok = true;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int nt = static_cast<int>(n_tiles);
-    int s = 0, u = 0;
-    for (int i = 0; i < nt && ok; ++i, s = (s + 1 == kStages) ? 0 : s + 1, u += (s == 0) ? 1 : 0) {
-      const int a = static_cast<int>(i & 1);
-      if (!mbar_wait(full0 + 8 * s, u & 1, 231, abort_flag)) { ok = false; break; }
-      valid_rows[a] = stage_mask[s];
-      // Row t's 8 scale bytes: blocks 0-3 feed the first K = 64 step, 4-7 the second.
-      const uint8_t* grp = stages + s * kTileBytes + (tid >> 3) * 576;
-      const uint2 sc = *reinterpret_cast<const uint2*>(grp + 512 + (tid & 7) * 8);
-      const uint32_t sfa = tmem + lane_base + plan.sfa + 8 * a;
-      tmem_st1(sfa + warp, sc.x);
-      tmem_st1(sfa + 4 + warp, sc.y);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(sfull0 + 8 * a);
-      if (i > 0) ok = epilogue(i - 1);
+    if (warp < 4) {
+      int s = 0, u = 0;
+      for (int i = 0; i < nt && ok; ++i, s = (s + 1 == kStages) ? 0 : s + 1, u += (s == 0) ? 1 : 0) {
+        const int a = static_cast<int>(i & 1);
+        if (!mbar_wait(full0 + 8 * s, u & 1, 231, abort_flag)) { ok = false; break; }
+        if (kSub == 1) valid_rows[a] = stage_mask[s];
+        // Row t's 8 scale bytes: blocks 0-3 feed the first K = 64 step, 4-7 the second.
+        const uint8_t* grp_bytes = stages + s * kTileBytes + (row >> 3) * 576;
+        const uint2 sc = *reinterpret_cast<const uint2*>(grp_bytes + 512 + (row & 7) * 8);
+        const uint32_t sfa = tmem + lane_base + plan.sfa + 8 * a;
+        tmem_st1(sfa + quarter, sc.x);
+        tmem_st1(sfa + 4 + quarter, sc.y);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(sfull0 + 8 * a);
+        if (i > 0) ok = epilogue(i - 1);
+      }
+      if (ok && nt > 0) ok = epilogue(nt - 1);
+    } else {
+      for (int i = 0; i < nt && ok; ++i) ok = epilogue(i);
     }
-    if (ok && n_tiles > 0) ok = epilogue(n_tiles - 1);
     if (!ok) *abort_flag = 1;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kEpi + 1) {
     tc_fence_after();
     tmem_dealloc(tmem, plan.ncols);
   }
 }
 
-template <bool kPool>
+template <bool kPool, int kSub>
 cudaError_t launch(const ScanParams& p, dim3 grid, int n_q, cudaStream_t stream) {
   const int smem = smem_bytes_for(kPool ? 1 : n_q, kPool ? p.tiles_per_cta : 0);
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(indexer_kernel<kPool>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes_for(kPool ? 1 : 8, kPool ? 128 : 0));
+    cudaError_t e = cudaFuncSetAttribute(indexer_kernel<kPool, kSub>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes_for(kPool ? 1 : kGroup, kPool ? 128 : 0));
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = true;
   }
-  return launch_pdl(indexer_kernel<kPool>, grid, dim3(kThreads), smem, stream, 0, p);
+  return launch_pdl(indexer_kernel<kPool, kSub>, grid, dim3(threads_for(kSub)), smem, stream, 0, p);
 }
 
 int num_sms() {
@@ -411,11 +464,12 @@ int num_sms() {
   return sms[dev];
 }
 
-// Resident CTAs per SM, bounded by shared memory and TMEM columns.
-int ctas_per_sm(int n_q, int pool_tiles) {
+// Resident CTAs per SM, bounded by shared memory, TMEM columns and threads.
+int ctas_per_sm(int n_q, int pool_tiles, int sub = 1) {
   const int by_smem = (228 * 1024) / (smem_bytes_for(n_q, pool_tiles) + 1024);
   const int by_tmem = 512 / static_cast<int>(tmem_plan(n_q).ncols);
-  return std::max(1, std::min(by_smem, by_tmem));
+  const int by_threads = 2048 / threads_for(sub);
+  return std::max(1, std::min(std::min(by_smem, by_tmem), by_threads));
 }
 
 }  // namespace
@@ -453,13 +507,18 @@ cudaError_t launch_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales,
   p.idx_pages = idx_pages;
   p.block_max = block_max;
   p.max_blocks = max_blocks;
-  p.n_grp = (n_q + kGroup - 1) / kGroup;
-  const int tile_q = std::min(n_q, kGroup);
+  // Decode: all tokens of a sequence in one group. A prefill chunk: groups of
+  // 7 tokens, each CTA with 16 epilogue warps.
+  const bool wide = n_q > kGroup;
+  p.grp_size = wide ? kWideGroup : kGroup;
+  p.n_grp = (n_q + p.grp_size - 1) / p.grp_size;
+  const int tile_q = std::min(n_q, p.grp_size);
   const int64_t rows = static_cast<int64_t>(B) * p.n_grp;
   const int64_t pages = (max_ctx + 127) / 128;
-  const int64_t target = static_cast<int64_t>(ctas_per_sm(tile_q, 0)) * num_sms();
+  const int64_t target = static_cast<int64_t>(ctas_per_sm(tile_q, 0, wide ? kWideSub : 1)) * num_sms();
   const int64_t per_seq = std::max<int64_t>(1, std::min<int64_t>(pages, (target + rows - 1) / rows));
-  return launch<false>(p, dim3(static_cast<unsigned>(per_seq), static_cast<unsigned>(rows)), tile_q, stream);
+  const dim3 grid(static_cast<unsigned>(per_seq), static_cast<unsigned>(rows));
+  return wide ? launch<false, kWideSub>(p, grid, tile_q, stream) : launch<false, 1>(p, grid, tile_q, stream);
 }
 
 cudaError_t launch_pool_scores(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
@@ -483,6 +542,7 @@ cudaError_t launch_pool_scores(const uint8_t* q_codes, const uint8_t* q_scales, 
   p.pool = pool;
   p.scores = scores;
   p.n_grp = 1;
+  p.grp_size = 1;
   // The 128 tiles of a token are cut into equal runs so that all CTAs are
   // resident at once (one wave) where the batch allows it; a run's slot table
   // is sized to the run, so short runs leave room for more CTAs per SM.
@@ -495,7 +555,7 @@ cudaError_t launch_pool_scores(const uint8_t* q_codes, const uint8_t* q_scales, 
     if (ctas_per_sm(1, per) >= cps) break;
   }
   p.tiles_per_cta = per;
-  return launch<true>(p, dim3(splits, static_cast<unsigned>(Q)), 1, stream);
+  return launch<true, 1>(p, dim3(splits, static_cast<unsigned>(Q)), 1, stream);
 }
 
 }  // namespace csa2

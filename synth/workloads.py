@@ -1,8 +1,11 @@
-"""The five decode workloads of the CSA2 path, as sizes and seeds.
+"""The five decode workloads of the CSA2 path and one chunked-prefill
+workload, as sizes and seeds.
 
 Each workload is seeded with 1000 + its index. Query token j of n_q sits at
 absolute position t = N - n_q + j, where N counts the entries in the cache
-after the step's new tokens have been appended.
+after the step's new tokens have been appended. A prefill workload's n_q
+tokens are one chunk of a prompt: each attends causally, with the exact
+128-position window.
 """
 from dataclasses import dataclass, field
 
@@ -16,6 +19,7 @@ class Workload:
     N: int              # context entries per sequence (after appending the step's tokens)
     n_q: int = 1        # query tokens per sequence
     layers: tuple = field(default=("full",))
+    prefill: bool = False
 
     @property
     def seed(self) -> int:
@@ -33,6 +37,7 @@ WORKLOADS = {
     3: Workload(3, "full_b8_n1m", "full", B=8, N=1048576),
     4: Workload(4, "group_reindex_3reuse_b32_n256k_q6", "group", B=32, N=262144, n_q=6,
                 layers=("reindex", "reuse", "reuse", "reuse")),
+    5: Workload(5, "prefill_full_b1_n128k_c4096", "full", B=1, N=131072, n_q=4096, prefill=True),
 }
 
 # Method constants (decoder CSA2 at m = 1).

@@ -99,7 +99,8 @@ def build(wl: Workload, device="cuda", *, N=None, B=None, n_q=None, shuffle_seed
     from sparse_attention_fp4_mxfp4_gb300.cache import PagedCache
 
     if N is not None or B is not None or n_q is not None:
-        wl = Workload(wl.index, wl.name, wl.mode, B=B or wl.B, N=N or wl.N, n_q=n_q or wl.n_q, layers=wl.layers)
+        wl = Workload(wl.index, wl.name, wl.mode, B=B or wl.B, N=N or wl.N, n_q=n_q or wl.n_q, layers=wl.layers,
+                      prefill=wl.prefill)
     N, Bq, nq, seed = wl.N, wl.B, wl.n_q, wl.seed
     n_layers = len(wl.layers)
     cache = PagedCache(Bq, N, n_rings=Bq * n_layers, device=device, shuffle_seed=shuffle_seed)

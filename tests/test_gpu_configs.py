@@ -7,6 +7,8 @@ times (tests.harness.Runner), on outputs the oracle can compute one by one:
   3  Full, 8 x 1M:           pool and top-512 of every sequence, attention of 2
   4  Reindex + 3 Reuse, 32 x 256K, 6 tokens: top-512 of 4 sampled (sequence,
      token) pairs and the attention of all four layers for them
+  5  Full prefill chunk, 1 x 128K, 4096 tokens: pool, top-512 and attention
+     (exact causal window) of 6 sampled tokens, and the refilled ring
 
 Selections: equal up to ties within 1e-5 relative of the oracle's k-th score.
 Attention: within 2e-3 + 2^-8 (1 + 2e-3) ~ 5.9e-3 max-relative per head row (bf16
@@ -30,7 +32,7 @@ DEV = "cuda"
 
 def _run(index):
     S = H.build(WORKLOADS[index], DEV)
-    R = H.Runner(S)
+    R = H.Runner(S, prefill=S.wl.prefill)
     R.step()
     torch.cuda.synchronize()
     assert csa2.csa2_check_device_status() == csa2.OK, csa2.device_status_message()
@@ -44,7 +46,7 @@ def _samples(S, n, seed):
 
 
 def _check_attn(S, R, b, j, li, topk_row):
-    ro, rl = H.oracle_attention(S, b, j, li, topk_row)
+    ro, rl = H.oracle_attention(S, b, j, li, topk_row, exact_window=S.wl.prefill)
     H.check_attention(R.out[li][b, j].float().cpu().numpy(), ro, H.TOL_ATTN_BF16)
     np.testing.assert_allclose(R.lse[li][b, j].cpu().numpy(), rl, rtol=1e-5, atol=H.TOL_LSE)
 
@@ -117,5 +119,23 @@ def test_workload4_group_b32_n256k_q6():
         H.check_selection(tk[b, j], ref["topk"], lambda p: slot[p], 512, f"group reindex {b},{j}")
         for li in range(4):
             _check_attn(S, R, b, j, li, tk[b, j])
+    del S, R
+    torch.cuda.empty_cache()
+
+
+def test_workload5_prefill_b1_n128k_c4096():
+    S, R = _run(5)
+    keys = H.oracle_keys(S, 0, S.N - 1)
+    for j in (0, 127, 128, 2047, 4094, 4095):
+        ref = H.oracle_full(S, 0, j, keys=keys)
+        pool = R.pool[0, j].cpu().numpy()
+        tk = R.topk[0, j].cpu().numpy()
+        H.check_selection(pool, ref["pool"], lambda i: ref["blockmax"][i], 2048, f"pool {j}")
+        H.check_selection(tk, ref["topk"], lambda i: ref["scores"][i], 512, f"topk {j}")
+        _check_attn(S, R, 0, j, 0, tk)
+    ring = S.cache.rings[0].cpu().numpy()
+    lo = S.N - 128
+    want = oracle.fp8_quant(synth.bf16_to_f32(synth.latent(S.wl.seed, 0, lo, 128, tensor=synth.SWA)))
+    assert np.array_equal(ring[np.arange(lo, S.N) % 128], want)
     del S, R
     torch.cuda.empty_cache()
