@@ -64,6 +64,7 @@ def lib():
         L.orc_window_positions.argtypes, L.orc_window_positions.restype = [i64, i64, i64, p], i64
         L.orc_sparse_attention.argtypes = [p, i32, i32, p, i64, p, i64, d, p, p]
         L.orc_output_derotate.argtypes = [p, i64, i32, i64]
+        L.orc_compress.argtypes = [p, p, i32, i32, i64, p]
         _lib = L
     return _lib
 
@@ -227,3 +228,23 @@ def output_derotate(rows, t):
     D = a.shape[-1]
     lib().orc_output_derotate(_p(a), a.size // D, D, int(t))
     return a
+
+
+# ---- compressed entries (encoder-side CSA2, m tokens per entry) ---------------
+
+def compress(x_bf16, z_bf16):
+    """x, z: uint16 (bf16 bits) [n, m, D] candidates and compression logits of
+    each entry's m tokens. Returns uint16 [n, D]: per channel the softmax over
+    the m tokens of z weighting x, in fp64, rounded once to bf16."""
+    x = _c(x_bf16, np.uint16)
+    z = _c(z_bf16, np.uint16)
+    assert x.shape == z.shape and x.ndim == 3
+    n, m, D = x.shape
+    out = np.empty((n, D), np.uint16)
+    lib().orc_compress(_p(x), _p(z), m, D, n, _p(out))
+    return out
+
+
+def entry_limit(t, m):
+    """Complete entries visible to a token at position t: floor((t + 1) / m)."""
+    return (t + 1) // m

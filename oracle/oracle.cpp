@@ -42,6 +42,11 @@
 //     entries followed by the FP8 window entries, duplicates kept.
 //   * Window of query t when the ring holds the last W positions of a
 //     sequence of N entries: positions max(0, t - W + 1, N - W) .. t.
+//   * Compressed entries at ratio m (encoder-side CSA2, m = 2): entry e covers
+//     tokens m*e .. m*e + m - 1; per channel it is the softmax over those m
+//     tokens of their compression logits, weighting their candidate values
+//     (fp64, then rounded to bf16); a token at position t sees the complete
+//     entries 0 .. floor((t + 1) / m) - 1, and its window stays in tokens.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -200,6 +205,25 @@ int64_t topk_indices(const double* s, int64_t n, int64_t k, int64_t* out) {
   std::sort(idx.begin(), idx.begin() + m);
   for (int64_t i = 0; i < m; ++i) out[i] = idx[i];
   return m;
+}
+
+// fp64 -> bf16, round to nearest, ties to even, in one step (no intermediate
+// float). Finite inputs within the bf16 range (the compressor's convex
+// combinations of bf16 values always are).
+uint16_t bf16_round(double d) {
+  if (d == 0.0) return std::signbit(d) ? 0x8000u : 0u;
+  const bool neg = d < 0;
+  double a = neg ? -d : d;
+  int e = 0;
+  std::frexp(a, &e);  // a = f * 2^e, f in [0.5, 1)
+  // bf16 keeps 8 significant bits down to 2^-126, then a fixed quantum 2^-133.
+  int q_exp = e - 8;
+  if (q_exp < -133) q_exp = -133;
+  double r = std::nearbyint(std::ldexp(a, -q_exp));  // default mode: nearest, ties to even
+  const float v = static_cast<float>(std::ldexp(r, q_exp));  // exact: at most 8 significant bits
+  uint32_t u;
+  std::memcpy(&u, &v, 4);
+  return static_cast<uint16_t>((u >> 16) | (neg ? 0x8000u : 0u));
 }
 
 }  // namespace
@@ -405,6 +429,30 @@ void orc_sparse_attention(const uint16_t* q, int heads, int dim, const uint16_t*
     }
     for (int c = 0; c < dim; ++c) o[c] /= den;
     lse[h] = mx + std::log(den);
+  }
+}
+
+// Compressed entries ([RN] section 1 / [AB] section 3.1: the encoder's CSA2
+// layers compress m = 2 tokens per entry; "DeepSeek-V4 model structure (7)",
+// KV cache of hybrid attention: the compressor keeps an unfinished entry's
+// tail tokens and their compression weights as state). The pages give no
+// formula; per channel c of entry e:
+//   out_c = sum_i exp(z_ic - zmax_c) x_ic / sum_i exp(z_ic - zmax_c),
+// i over the entry's m tokens, in fp64, rounded once to bf16.
+//   x, z: bf16 [n, m, dim] candidates and logits; out: bf16 [n, dim].
+void orc_compress(const uint16_t* x, const uint16_t* z, int m, int dim, int64_t n, uint16_t* out) {
+  for (int64_t e = 0; e < n; ++e) {
+    for (int c = 0; c < dim; ++c) {
+      double zmax = -INFINITY;
+      for (int i = 0; i < m; ++i) zmax = std::max(zmax, static_cast<double>(bf16_value(z[(e * m + i) * dim + c])));
+      double num = 0.0, den = 0.0;
+      for (int i = 0; i < m; ++i) {
+        const double w = std::exp(static_cast<double>(bf16_value(z[(e * m + i) * dim + c])) - zmax);
+        num += w * static_cast<double>(bf16_value(x[(e * m + i) * dim + c]));
+        den += w;
+      }
+      out[e * dim + c] = bf16_round(num / den);
+    }
   }
 }
 

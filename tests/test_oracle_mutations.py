@@ -2,7 +2,7 @@
 
 Each case copies oracle.cpp, plants one mistake of the kind an implementation
 plausibly makes (a dropped term, a wrong sign, index or tie rule, a transposed
-nibble order), builds the copy on the CPU and runs the pin tests against it in
+nibble order, a softmax sign or normaliser), builds the copy on the CPU and runs the pin tests against it in
 a child process. Every mutant must fail at least one pin.
 """
 import os
@@ -29,6 +29,11 @@ MUTANTS = {
     "attention_no_scale": ("logit[i] = tau * d;", "logit[i] = d;"),
     "block_max_shifted": ("for (int64_t p = b * block; p < std::min<int64_t>(n, (b + 1) * block); ++p)",
                           "for (int64_t p = b * block + 1; p < std::min<int64_t>(n, (b + 1) * block); ++p)"),
+    "compress_logit_sign": ("const double w = std::exp(static_cast<double>(bf16_value(z[(e * m + i) * dim + c])) - zmax);",
+                            "const double w = std::exp(zmax - static_cast<double>(bf16_value(z[(e * m + i) * dim + c])));"),
+    "compress_unnormalised": ("out[e * dim + c] = bf16_round(num / den);", "out[e * dim + c] = bf16_round(num);"),
+    "compress_ties_away": ("double r = std::nearbyint(std::ldexp(a, -q_exp));",
+                           "double r = std::round(std::ldexp(a, -q_exp));"),
 }
 
 
@@ -46,6 +51,7 @@ def test_mutant_fails_a_pin(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_formats.py"),
                         os.path.join(ROOT, "tests", "test_oracle_indexer.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_attention.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_attention.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_compress.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
