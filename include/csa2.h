@@ -60,6 +60,13 @@
  *     window is the positions max(0, t - 127, seq_len[b] - 128) .. t still
  *     resident in the ring; in a prefill call (csa2_sparse_attn_prefill) it is
  *     exactly max(0, t - 127) .. t.
+ *   - Tokens per entry m (argument m of the indexer and attention calls): 1
+ *     for the decoder's CSA2 layers, where entry p is token p; 2 for the
+ *     encoder's ([RN] 1, [AB] 3.1), where entry e summarises tokens 2e and
+ *     2e + 1 (csa2_compress_append). Pages, block tables, top-k positions and
+ *     block ids then count entries; seq_len and t still count tokens: token t
+ *     sees the complete entries 0 .. floor((t + 1) / m) - 1, and its sliding
+ *     window stays in tokens.
  *   - Query tokens per sequence: the indexer calls and the prefill attention
  *     take n_q <= CSA2_MAX_PREFILL_NQ (the Full scan serves them in groups of
  *     8 tokens), the decode attention n_q <= CSA2_MAX_NQ; every call takes
@@ -158,6 +165,28 @@ int csa2_append_kv(const void* latent, const void* idx_key, const int32_t* seq_i
 int csa2_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, int T,
                     int64_t n_rings, uint8_t* rings, void* stream);
 
+/* Encoder-side append at m tokens per entry (m = 1 or 2; [RN] 1 / [AB] 3.1
+ * give m = 2 for the encoder's CSA2 layers; "DeepSeek-V4 model structure
+ * (7)", KV cache of hybrid attention: an unfinished entry's tail tokens and
+ * their compression weights are per-sequence state). T new tokens: kv, kv_gate
+ * bf16 [T, 512] (candidate latent and its compression logits), idx_key,
+ * idx_gate bf16 [T, 128] (the same for the indexer key), seq_idx int32 [T],
+ * pos int64 [T] token positions. The rows of one sequence must be consecutive
+ * positions in order. The token at position p with p % m == m - 1 completes
+ * entry e = p / m: per channel, out_c = sum_i exp(z_ic - max z) x_ic /
+ * sum_i exp(z_ic - max z) over tokens m*e .. p (fp64), rounded once to bf16,
+ * then stored like csa2_append_kv at entry e (page block_table[b, e / 128],
+ * slot e % 128). The tokens of the entry that precede this call come from
+ * tail: bf16 [B, m - 1, 1280] (per token: kv 512, kv_gate 512, idx_key 128,
+ * idx_gate 128; slot = position % m), owned by the caller, one per (layer,
+ * sequence group); tokens whose entry stays unfinished after the call are
+ * written there. m = 1 stores every token as is (tail unused, may be NULL).
+ * Two kernels run in order on the stream (entries, then tails). */
+int csa2_compress_append(const void* kv, const void* kv_gate, const void* idx_key, const void* idx_gate,
+                         const int32_t* seq_idx, const int64_t* pos, int T, int m, void* tail,
+                         const int32_t* block_table, int B, int max_pages, int64_t n_pages,
+                         uint8_t* main_pages, uint8_t* idx_pages, void* stream);
+
 /* The same E4M3 encoding of T window entries x: bf16 [T, 512] into out: u8
  * [T, 512] (16-byte aligned), row for row. A prefill chunk's own window
  * entries are encoded this way for csa2_sparse_attn_prefill before the ring
@@ -193,20 +222,21 @@ int csa2_quant_fp8(const float* x, int64_t n, uint8_t* out, void* stream);
  *   q_codes: [B, n_q, 32, 64] bytes, q_scales: [B, n_q, 32, 8] (MXFP4 of the
  *   indexer query, as written by csa2_quant_mxfp4 on a [B, n_q, 32, 128]
  *   tensor); w: fp32 [B, n_q, 32]; seq_len: int64 [B].
- *   block_max: fp32 [B, n_q, max_blocks], max_blocks >= ceil(max_ctx / 8);
- *   entries at or past ceil((t + 1) / 8) are left untouched.
- * max_ctx is a host-side upper bound of seq_len (sizes the grid). */
+ *   block_max: fp32 [B, n_q, max_blocks], max_blocks >= ceil(max_ctx / m / 8);
+ *   entries at or past ceil(floor((t + 1) / m) / 8) are left untouched.
+ * max_ctx is a host-side upper bound of seq_len (sizes the grid); m: tokens
+ * per entry (1 or 2; positions p are entries then). */
 int csa2_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
                       const int64_t* seq_len, int B, int n_q, int64_t max_ctx,
                       const int32_t* block_table, int max_pages, int64_t n_pages,
-                      const uint8_t* idx_pages, float* block_max, int64_t max_blocks,
+                      const uint8_t* idx_pages, float* block_max, int64_t max_blocks, int m,
                       void* stream);
 
 /* Top 2048 blocks of each query token by block maximum (higher first, then
  * lower block id); all causal blocks when there are at most 2048.
  *   pool: int32 [B, n_q, 2048], block ids ascending, -1 padded. */
 int csa2_block_topk(const float* block_max, const int64_t* seq_len, int B, int n_q,
-                    int64_t max_blocks, int32_t* pool, void* stream);
+                    int64_t max_blocks, int32_t* pool, int m, void* stream);
 
 /* Reindex: scores only the positions 8b..8b+7 (<= t) of each pool block b
  * with this layer's indexer query and takes the top 512 (higher score first,
@@ -217,7 +247,7 @@ int csa2_block_topk(const float* block_max, const int64_t* seq_len, int B, int n
 int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
                          const int64_t* seq_len, int B, int n_q, const int32_t* block_table,
                          int max_pages, int64_t n_pages, const uint8_t* idx_pages,
-                         const int32_t* pool, int32_t* topk, void* ws, size_t ws_bytes,
+                         const int32_t* pool, int32_t* topk, void* ws, size_t ws_bytes, int m,
                          void* stream);
 
 /* Same computation and outputs as csa2_indexer_reindex, for callers that cannot
@@ -248,7 +278,7 @@ int csa2_indexer_full(const uint8_t* q_codes, const uint8_t* q_scales, const flo
                       const int64_t* seq_len, int B, int n_q, int64_t max_ctx,
                       const int32_t* block_table, int max_pages, int64_t n_pages,
                       const uint8_t* idx_pages, int32_t* pool, int32_t* topk, void* ws,
-                      size_t ws_bytes, void* stream);
+                      size_t ws_bytes, int m, void* stream);
 
 /* ---- sparse attention (Reuse mode; [RN] 2.2, [AB] 3.3 / 3.6, [SY]) ---------- */
 /* o_h = softmax(scale * q_h K^T) V with K = V = the dequantised keys: the main
@@ -264,7 +294,7 @@ int csa2_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len,
                      const int32_t* block_table, int max_pages, int64_t n_pages,
                      const uint8_t* main_pages, const uint8_t* rings, const int32_t* ring_idx,
                      int64_t n_rings, float softmax_scale, int out_dtype, void* out, float* lse,
-                     void* ws, size_t ws_bytes, void* stream);
+                     void* ws, size_t ws_bytes, int m, void* stream);
 
 /* Prefill (chunked prefill) of n_q <= CSA2_MAX_PREFILL_NQ new tokens per
  * sequence ([RN] 2.2, [AB] 3.3: the same attention over a causal run of query
@@ -280,7 +310,7 @@ int csa2_sparse_attn_prefill(const void* q, const int32_t* topk, const int64_t* 
                              const uint8_t* main_pages, const uint8_t* rings,
                              const int32_t* ring_idx, int64_t n_rings, const uint8_t* swa_chunk,
                              float softmax_scale, int out_dtype, void* out, float* lse, void* ws,
-                             size_t ws_bytes, void* stream);
+                             size_t ws_bytes, int m, void* stream);
 
 /* ---- mode dispatcher ([RN] 2.2, [AB] 3.3) ----------------------------------- */
 typedef struct csa2_layer_args {
@@ -311,6 +341,7 @@ typedef struct csa2_layer_args {
   const uint8_t* swa_chunk; /* NULL: decode (n_q <= CSA2_MAX_NQ, window from the ring).
                                Else prefill: the chunk's E4M3 window entries
                                [B, n_q, 512], attention as csa2_sparse_attn_prefill */
+  int tokens_per_entry;     /* m: 0 or 1 = decoder layer, 2 = encoder layer */
 } csa2_layer_args;
 
 /* One layer: FULL = indexer_full then sparse_attn; REINDEX = indexer_reindex

@@ -33,7 +33,7 @@ OP_INDEXER_FULL, OP_INDEXER_REINDEX, OP_SPARSE_ATTN, OP_DECODE_LAYER = 1, 2, 3, 
 # Exported entry points of include/csa2.h.
 EXPORTS = (
     "csa2_status_string", "csa2_last_error", "csa2_version", "csa2_page_bytes", "csa2_ring_bytes",
-    "csa2_workspace_bytes", "csa2_append_kv", "csa2_append_swa", "csa2_quant_fp8_entries",
+    "csa2_workspace_bytes", "csa2_append_kv", "csa2_compress_append", "csa2_append_swa", "csa2_quant_fp8_entries",
     "csa2_ring_refill", "csa2_quant_mxfp4",
     "csa2_dequant_mxfp4", "csa2_quant_fp8", "csa2_indexer_scan", "csa2_block_topk",
     "csa2_indexer_reindex", "csa2_indexer_reindex_noalloc", "csa2_indexer_full", "csa2_sparse_attn", "csa2_sparse_attn_prefill", "csa2_decode_layer",
@@ -58,7 +58,7 @@ class LayerArgs(ctypes.Structure):
         ("w", ctypes.c_void_p), ("q", ctypes.c_void_p), ("pool", ctypes.c_void_p), ("topk", ctypes.c_void_p),
         ("softmax_scale", ctypes.c_float), ("out_dtype", ctypes.c_int), ("out", ctypes.c_void_p),
         ("lse", ctypes.c_void_p), ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
-        ("swa_chunk", ctypes.c_void_p),
+        ("swa_chunk", ctypes.c_void_p), ("tokens_per_entry", ctypes.c_int),
     ]
 
 
@@ -76,20 +76,21 @@ def _load():
         "csa2_ring_bytes": ([psz], i32),
         "csa2_workspace_bytes": ([i32, i32, i32, i64, psz], i32),
         "csa2_append_kv": ([p, p, p, p, i32, p, i32, i32, i64, p, p, p], i32),
+        "csa2_compress_append": ([p, p, p, p, p, p, i32, i32, p, p, i32, i32, i64, p, p, p], i32),
         "csa2_append_swa": ([p, p, p, i32, i64, p, p], i32),
         "csa2_quant_fp8_entries": ([p, i32, p, p], i32),
         "csa2_ring_refill": ([p, p, i32, i32, p, i64, p, p], i32),
         "csa2_quant_mxfp4": ([p, i64, p, p, p], i32),
         "csa2_dequant_mxfp4": ([p, p, i64, p, p], i32),
         "csa2_quant_fp8": ([p, i64, p, p], i32),
-        "csa2_indexer_scan": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, i64, p], i32),
-        "csa2_block_topk": ([p, p, i32, i32, i64, p, p], i32),
-        "csa2_indexer_reindex": ([p, p, p, p, i32, i32, p, i32, i64, p, p, p, p, sz, p], i32),
+        "csa2_indexer_scan": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, i64, i32, p], i32),
+        "csa2_block_topk": ([p, p, i32, i32, i64, p, i32, p], i32),
+        "csa2_indexer_reindex": ([p, p, p, p, i32, i32, p, i32, i64, p, p, p, p, sz, i32, p], i32),
         "csa2_indexer_reindex_noalloc": ([p, p, p, p, i32, i32, p, i32, i64, p, p, p, p], i32),
-        "csa2_indexer_full": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, p, p, sz, p], i32),
-        "csa2_sparse_attn": ([p, p, p, i32, i32, p, i32, i64, p, p, p, i64, f32, i32, p, p, p, sz, p], i32),
-        "csa2_sparse_attn_prefill": ([p, p, p, i32, i32, p, i32, i64, p, p, p, i64, p, f32, i32, p, p, p, sz, p],
-                                     i32),
+        "csa2_indexer_full": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, p, p, sz, i32, p], i32),
+        "csa2_sparse_attn": ([p, p, p, i32, i32, p, i32, i64, p, p, p, i64, f32, i32, p, p, p, sz, i32, p], i32),
+        "csa2_sparse_attn_prefill": ([p, p, p, i32, i32, p, i32, i64, p, p, p, i64, p, f32, i32, p, p, p, sz, i32,
+                                      p], i32),
         "csa2_decode_layer": ([ctypes.POINTER(LayerArgs), p], i32),
         "csa2_decode_group": ([ctypes.POINTER(LayerArgs), i32, p], i32),
         "csa2_check_device_status": ([p, ctypes.POINTER(ctypes.c_int)], i32),
@@ -169,6 +170,21 @@ def csa2_append_kv(latent, idx_key, seq_idx, pos, block_table, main_pages, idx_p
                               _ptr(main_pages), _ptr(idx_pages), _stream(stream)))
 
 
+def csa2_compress_append(kv, kv_gate, idx_key, idx_gate, seq_idx, pos, m, tail, block_table, main_pages, idx_pages,
+                         stream=None):
+    """Encoder-side append at m tokens per entry: kv, kv_gate bf16 [T,512], idx_key, idx_gate bf16 [T,128],
+    seq_idx int32 [T], pos int64 [T] (each sequence's rows consecutive positions), tail bf16 [B,m-1,1280]
+    (None for m = 1). Entries go to the pages at entry e = pos // m."""
+    for t, n in ((kv, "kv"), (kv_gate, "kv_gate"), (idx_key, "idx_key"), (idx_gate, "idx_gate")):
+        _need(t, n, torch.bfloat16, 2)
+    _need(seq_idx, "seq_idx", torch.int32, 1)
+    _need(pos, "pos", torch.int64, 1)
+    T = kv.shape[0]
+    _check(lib.csa2_compress_append(_ptr(kv), _ptr(kv_gate), _ptr(idx_key), _ptr(idx_gate), _ptr(seq_idx), _ptr(pos),
+                                    T, m, _ptr(tail), _ptr(block_table), block_table.shape[0], block_table.shape[1],
+                                    main_pages.shape[0], _ptr(main_pages), _ptr(idx_pages), _stream(stream)))
+
+
 def csa2_append_swa(x, ring_idx, pos, rings, stream=None):
     """x bf16 [T,512], ring_idx int32 [T], pos int64 [T], rings uint8 [R,128,512]."""
     _need(x, "x", torch.bfloat16, 2)
@@ -231,27 +247,27 @@ def csa2_quant_fp8(x, out=None, stream=None):
 # ---- indexer ------------------------------------------------------------------
 
 def csa2_indexer_scan(q_codes, q_scales, w, seq_len, max_ctx, block_table, n_pages, idx_pages,
-                      block_max, stream=None):
+                      block_max, stream=None, m=1):
     """q_codes uint8 [B,n_q,32,64], q_scales uint8 [B,n_q,32,8], w fp32 [B,n_q,32],
     seq_len int64 [B] -> block_max fp32 [B,n_q,max_blocks]."""
     B, n_q = w.shape[0], w.shape[1]
     _check(lib.csa2_indexer_scan(_ptr(q_codes), _ptr(q_scales), _ptr(w), _ptr(seq_len), B, n_q, max_ctx,
                                  _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx_pages),
-                                 _ptr(block_max), block_max.shape[-1], _stream(stream)))
+                                 _ptr(block_max), block_max.shape[-1], m, _stream(stream)))
 
 
-def csa2_block_topk(block_max, seq_len, pool, stream=None):
+def csa2_block_topk(block_max, seq_len, pool, stream=None, m=1):
     B, n_q = block_max.shape[0], block_max.shape[1]
-    _check(lib.csa2_block_topk(_ptr(block_max), _ptr(seq_len), B, n_q, block_max.shape[-1], _ptr(pool),
+    _check(lib.csa2_block_topk(_ptr(block_max), _ptr(seq_len), B, n_q, block_max.shape[-1], _ptr(pool), m,
                                _stream(stream)))
 
 
 def csa2_indexer_reindex(q_codes, q_scales, w, seq_len, block_table, n_pages, idx_pages, pool, topk, ws,
-                         stream=None):
+                         stream=None, m=1):
     B, n_q = w.shape[0], w.shape[1]
     _check(lib.csa2_indexer_reindex(_ptr(q_codes), _ptr(q_scales), _ptr(w), _ptr(seq_len), B, n_q,
                                     _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx_pages),
-                                    _ptr(pool), _ptr(topk), _ptr(ws), ws.numel() * ws.element_size(),
+                                    _ptr(pool), _ptr(topk), _ptr(ws), ws.numel() * ws.element_size(), m,
                                     _stream(stream)))
 
 
@@ -266,18 +282,18 @@ def csa2_indexer_reindex_noalloc(q_codes, q_scales, w, seq_len, block_table, n_p
 
 
 def csa2_indexer_full(q_codes, q_scales, w, seq_len, max_ctx, block_table, n_pages, idx_pages, pool, topk,
-                      ws, stream=None):
+                      ws, stream=None, m=1):
     B, n_q = w.shape[0], w.shape[1]
     _check(lib.csa2_indexer_full(_ptr(q_codes), _ptr(q_scales), _ptr(w), _ptr(seq_len), B, n_q, max_ctx,
                                  _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx_pages),
-                                 _ptr(pool), _ptr(topk), _ptr(ws), ws.numel() * ws.element_size(),
+                                 _ptr(pool), _ptr(topk), _ptr(ws), ws.numel() * ws.element_size(), m,
                                  _stream(stream)))
 
 
 # ---- attention ----------------------------------------------------------------
 
 def csa2_sparse_attn(q, topk, seq_len, block_table, n_pages, main_pages, rings, ring_idx, out, lse, ws,
-                     softmax_scale=1.0 / math.sqrt(LATENT_DIM), stream=None, derotate=False):
+                     softmax_scale=1.0 / math.sqrt(LATENT_DIM), stream=None, derotate=False, m=1):
     """q bf16 [B,n_q,64,512], topk int32 [B,n_q,512] -> out [B,n_q,64,512] (fp32 or bf16), lse fp32 [B,n_q,64].
     derotate: rotate the output's last 64 channels back by the token position (CSA2_OUT_DEROTATE)."""
     _need(q, "q", torch.bfloat16, 4)
@@ -286,11 +302,12 @@ def csa2_sparse_attn(q, topk, seq_len, block_table, n_pages, main_pages, rings, 
     _check(lib.csa2_sparse_attn(_ptr(q), _ptr(topk), _ptr(seq_len), B, n_q, _ptr(block_table),
                                 block_table.shape[1], n_pages, _ptr(main_pages), _ptr(rings), _ptr(ring_idx),
                                 rings.shape[0], softmax_scale, out_dtype, _ptr(out), _ptr(lse), _ptr(ws),
-                                ws.numel() * ws.element_size(), _stream(stream)))
+                                ws.numel() * ws.element_size(), m, _stream(stream)))
 
 
 def csa2_sparse_attn_prefill(q, topk, seq_len, block_table, n_pages, main_pages, rings, ring_idx, swa_chunk, out,
-                             lse, ws=None, softmax_scale=1.0 / math.sqrt(LATENT_DIM), stream=None, derotate=False):
+                             lse, ws=None, softmax_scale=1.0 / math.sqrt(LATENT_DIM), stream=None, derotate=False,
+                             m=1):
     """As csa2_sparse_attn, with the exact causal window: swa_chunk uint8 [B,n_q,512] holds the E4M3
     window entries of the call's own positions, the rings the 128 positions before them."""
     _need(q, "q", torch.bfloat16, 4)
@@ -301,14 +318,15 @@ def csa2_sparse_attn_prefill(q, topk, seq_len, block_table, n_pages, main_pages,
     _check(lib.csa2_sparse_attn_prefill(_ptr(q), _ptr(topk), _ptr(seq_len), B, n_q, _ptr(block_table),
                                         block_table.shape[1], n_pages, _ptr(main_pages), _ptr(rings),
                                         _ptr(ring_idx), rings.shape[0], _ptr(swa_chunk), softmax_scale, out_dtype,
-                                        _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream(stream)))
+                                        _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, m, _stream(stream)))
 
 
 # ---- dispatcher ---------------------------------------------------------------
 
 def layer_args(mode, *, B, n_q, max_ctx, seq_len, block_table, n_pages, main_pages, idx_pages, rings,
                ring_idx, q, out, ws, q_idx_codes=None, q_idx_scales=None, w=None, pool=None, topk=None,
-               lse=None, softmax_scale=1.0 / math.sqrt(LATENT_DIM), derotate=False, swa_chunk=None) -> LayerArgs:
+               lse=None, softmax_scale=1.0 / math.sqrt(LATENT_DIM), derotate=False, swa_chunk=None,
+               m=1) -> LayerArgs:
     a = LayerArgs()
     a.mode, a.B, a.n_q, a.max_ctx = mode, B, n_q, max_ctx
     a.seq_len, a.block_table, a.max_pages, a.n_pages = _ptr(seq_len), _ptr(block_table), block_table.shape[1], n_pages
@@ -321,6 +339,7 @@ def layer_args(mode, *, B, n_q, max_ctx, seq_len, block_table, n_pages, main_pag
     a.out, a.lse = _ptr(out), _ptr(lse)
     a.ws, a.ws_bytes = _ptr(ws), ws.numel() * ws.element_size()
     a.swa_chunk = _ptr(swa_chunk)
+    a.tokens_per_entry = m
     return a
 
 

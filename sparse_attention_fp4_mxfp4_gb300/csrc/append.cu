@@ -14,6 +14,180 @@ namespace {
 
 constexpr int kMainPageBytes = 128 * 288;
 constexpr int kIdxPageBytes = 16 * 576;
+constexpr int kTailRow = 512 + 512 + 128 + 128;  // bf16 per pending token: kv, kv logits, key, key logits
+
+// One 16-channel block of an entry into its page: the main latent block of
+// lane `lane` and, for lanes 0-7, the indexer-key block.
+__device__ __forceinline__ void store_entry(uint8_t* __restrict__ main_pages, uint8_t* __restrict__ idx_pages,
+                                            int32_t page, int slot, int lane, const float (&lat)[16],
+                                            const float (&key)[16]) {
+  uint8_t sc;
+  uint32_t lo, hi;
+  mxfp4_block(lat, sc, lo, hi);
+  uint8_t* e = main_pages + static_cast<int64_t>(page) * kMainPageBytes + slot * 288;
+  *reinterpret_cast<uint2*>(e + 8 * lane) = make_uint2(lo, hi);
+  e[256 + lane] = sc;
+  if (lane < 8) {
+    mxfp4_block(key, sc, lo, hi);
+    const int row = slot & 7;
+    uint8_t* g = idx_pages + static_cast<int64_t>(page) * kIdxPageBytes + (slot >> 3) * 576;
+    *reinterpret_cast<uint2*>(g + (lane >> 1) * 128 + row * 16 + (lane & 1) * 8) = make_uint2(lo, hi);
+    g[512 + row * 8 + lane] = sc;
+  }
+}
+
+// fp64 -> bf16, nearest with ties to even, from the double's bits in one step.
+__device__ __forceinline__ uint16_t bf16_from_f64(double d) {
+  const uint64_t u = static_cast<uint64_t>(__double_as_longlong(d));
+  const uint32_t sign = static_cast<uint32_t>(u >> 63) << 15;
+  const int ex = static_cast<int>((u >> 52) & 0x7FF);
+  if (ex == 0) return static_cast<uint16_t>(sign);  // zero or far below bf16's range
+  const uint64_t m = (u & ((uint64_t(1) << 52) - 1)) | (uint64_t(1) << 52);  // 53 significant bits
+  int e8 = ex - 1023 + 127;
+  // Normal bf16 keeps 8 significant bits; below 2^-126 the quantum is 2^-133.
+  const int drop = e8 >= 1 ? 45 : 45 + (1 - e8);
+  if (drop > 54) return static_cast<uint16_t>(sign);
+  uint64_t q = m >> drop;
+  const uint64_t rem = m & ((uint64_t(1) << drop) - 1), half = uint64_t(1) << (drop - 1);
+  if (rem > half || (rem == half && (q & 1))) ++q;
+  if (e8 < 1) return static_cast<uint16_t>(sign | static_cast<uint32_t>(q));  // q = 128 is the smallest normal
+  if (q == (uint64_t(1) << 8)) {
+    q >>= 1;
+    ++e8;
+  }
+  if (e8 >= 255) return static_cast<uint16_t>(sign | 0x7F80u);
+  return static_cast<uint16_t>(sign | (static_cast<uint32_t>(e8) << 7) | static_cast<uint32_t>(q & 0x7F));
+}
+
+// Entry of ratio m: per channel, the softmax of the m tokens' logits weights
+// their candidates (fp64), rounded once to bf16, returned as fp32.
+template <int kM>
+__device__ __forceinline__ void compress16(const float (&x)[kM][16], const float (&z)[kM][16], float (&out)[16]) {
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    double zmax = z[0][c];
+#pragma unroll
+    for (int i = 1; i < kM; ++i) zmax = fmax(zmax, static_cast<double>(z[i][c]));
+    double num = 0.0, den = 0.0;
+#pragma unroll
+    for (int i = 0; i < kM; ++i) {
+      const double w = exp(static_cast<double>(z[i][c]) - zmax);
+      num += w * static_cast<double>(x[i][c]);
+      den += w;
+    }
+    out[c] = __uint_as_float(static_cast<uint32_t>(bf16_from_f64(num / den)) << 16);
+  }
+}
+
+// Encoder-side append at ratio kM: the warp of a token at position p with
+// p % kM == kM - 1 builds entry p / kM from its kM tokens (earlier ones from
+// this call when they are the rows just before it, else from the sequence's
+// tail state) and stores it; other tokens do nothing here.
+template <int kM>
+__global__ void __launch_bounds__(256) compress_append_kernel(
+    const uint16_t* __restrict__ kv, const uint16_t* __restrict__ kv_gate, const uint16_t* __restrict__ idx_key,
+    const uint16_t* __restrict__ idx_gate, const int32_t* __restrict__ seq_idx, const int64_t* __restrict__ pos,
+    int T, const uint16_t* __restrict__ tail, const int32_t* __restrict__ block_table, int B, int max_pages,
+    int64_t n_pages, uint8_t* __restrict__ main_pages, uint8_t* __restrict__ idx_pages) {
+  griddep_wait();
+  griddep_launch();
+  const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (tok >= T) return;
+  const int b = seq_idx[tok];
+  const int64_t p = pos[tok];
+  if (b < 0 || b >= B || p < 0) {
+    if (lane == 0) report(CSA2_ERR_DEVICE_BOUNDS, 121);
+    return;
+  }
+  if (p % kM != kM - 1) return;
+  const int64_t e = p / kM;
+  if ((e >> 7) >= max_pages) {
+    if (lane == 0) report(CSA2_ERR_DEVICE_BOUNDS, 122);
+    return;
+  }
+  const int32_t page = block_table[static_cast<int64_t>(b) * max_pages + (e >> 7)];
+  if (page < 0 || page >= n_pages) {
+    if (lane == 0) report(CSA2_ERR_DEVICE_BOUNDS, 123);
+    return;
+  }
+  float x[kM][16], z[kM][16], kx[kM][16], kz[kM][16];
+#pragma unroll
+  for (int i = 0; i < kM; ++i) {
+    // Token m*e + i: row tok - (kM - 1 - i) of this call, or tail slot i.
+    const int r = tok - (kM - 1 - i);
+    const bool in_call = i == kM - 1 || (r >= 0 && seq_idx[r] == b && pos[r] == p - (kM - 1 - i));
+    const uint16_t *xs, *zs, *ks, *kzs;
+    if (in_call) {
+      xs = kv + static_cast<int64_t>(r) * 512;
+      zs = kv_gate + static_cast<int64_t>(r) * 512;
+      ks = idx_key + static_cast<int64_t>(r) * 128;
+      kzs = idx_gate + static_cast<int64_t>(r) * 128;
+    } else {
+      const uint16_t* row = tail + (static_cast<int64_t>(b) * (kM - 1) + i) * kTailRow;
+      xs = row;
+      zs = row + 512;
+      ks = row + 1024;
+      kzs = row + 1152;
+    }
+    const uint4* xv = reinterpret_cast<const uint4*>(xs) + 2 * lane;
+    const uint4* zv = reinterpret_cast<const uint4*>(zs) + 2 * lane;
+    bf16x8_to_f32(xv[0], x[i]);
+    bf16x8_to_f32(xv[1], x[i] + 8);
+    bf16x8_to_f32(zv[0], z[i]);
+    bf16x8_to_f32(zv[1], z[i] + 8);
+    if (lane < 8) {
+      const uint4* kv4 = reinterpret_cast<const uint4*>(ks) + 2 * lane;
+      const uint4* kz4 = reinterpret_cast<const uint4*>(kzs) + 2 * lane;
+      bf16x8_to_f32(kv4[0], kx[i]);
+      bf16x8_to_f32(kv4[1], kx[i] + 8);
+      bf16x8_to_f32(kz4[0], kz[i]);
+      bf16x8_to_f32(kz4[1], kz[i] + 8);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) kx[i][c] = kz[i][c] = 0.f;
+    }
+  }
+  float lat[16], key[16];
+  compress16<kM>(x, z, lat);
+  compress16<kM>(kx, kz, key);
+  store_entry(main_pages, idx_pages, page, static_cast<int>(e & 127), lane, lat, key);
+}
+
+// After compress_append_kernel: a token whose entry is not completed within
+// this call (its completing token is not among the rows after it) goes to
+// tail slot p % kM of its sequence.
+template <int kM>
+__global__ void __launch_bounds__(256) compress_tail_kernel(
+    const uint16_t* __restrict__ kv, const uint16_t* __restrict__ kv_gate, const uint16_t* __restrict__ idx_key,
+    const uint16_t* __restrict__ idx_gate, const int32_t* __restrict__ seq_idx, const int64_t* __restrict__ pos,
+    int T, int B, uint16_t* __restrict__ tail) {
+  griddep_wait();
+  griddep_launch();
+  const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (tok >= T) return;
+  const int b = seq_idx[tok];
+  const int64_t p = pos[tok];
+  if (b < 0 || b >= B || p < 0 || p % kM == kM - 1) return;
+  const int d = static_cast<int>(kM - 1 - p % kM);
+  const int r = tok + d;
+  if (r < T && seq_idx[r] == b && pos[r] == p + d) return;  // completed in this call
+  uint16_t* row = tail + (static_cast<int64_t>(b) * (kM - 1) + p % kM) * kTailRow;
+  // 1280 bf16 = 160 x 16 B: lane copies chunks lane, lane + 32, ...
+  for (int c = lane; c < kTailRow / 8; c += 32) {
+    const uint16_t* src;
+    int off;
+    if (c < 64) { src = kv; off = c; }
+    else if (c < 128) { src = kv_gate; off = c - 64; }
+    else if (c < 144) { src = idx_key; off = c - 128; }
+    else { src = idx_gate; off = c - 144; }
+    const int width = c < 128 ? 512 : 128;
+    reinterpret_cast<uint4*>(row)[c] =
+        reinterpret_cast<const uint4*>(src + static_cast<int64_t>(tok) * width)[off];
+  }
+}
+
 
 __global__ void __launch_bounds__(256) append_kv_kernel(
     const uint16_t* __restrict__ latent, const uint16_t* __restrict__ idx_key,
@@ -213,6 +387,37 @@ cudaError_t launch_ring_refill(const uint8_t* entries, const int64_t* seq_len, i
   const int m = n < 128 ? n : 128;
   return launch_pdl(ring_refill_kernel, dim3((m + 7) / 8, B), dim3(256), 0, stream, 0, entries, seq_len, n,
                     ring_idx, n_rings, rings);
+}
+
+template <int kM>
+cudaError_t launch_compress_m(const void* kv, const void* kv_gate, const void* idx_key, const void* idx_gate,
+                              const int32_t* seq_idx, const int64_t* pos, int T, void* tail,
+                              const int32_t* block_table, int B, int max_pages, int64_t n_pages,
+                              uint8_t* main_pages, uint8_t* idx_pages, cudaStream_t stream) {
+  const dim3 grid((T + 7) / 8);
+  cudaError_t e = launch_pdl(compress_append_kernel<kM>, grid, dim3(256), 0, stream, 0,
+                             static_cast<const uint16_t*>(kv), static_cast<const uint16_t*>(kv_gate),
+                             static_cast<const uint16_t*>(idx_key), static_cast<const uint16_t*>(idx_gate), seq_idx,
+                             pos, T, static_cast<const uint16_t*>(tail), block_table, B, max_pages, n_pages,
+                             main_pages, idx_pages);
+  if (e != cudaSuccess || kM == 1) return e;
+  return launch_pdl(compress_tail_kernel<kM>, grid, dim3(256), 0, stream, 0, static_cast<const uint16_t*>(kv),
+                    static_cast<const uint16_t*>(kv_gate), static_cast<const uint16_t*>(idx_key),
+                    static_cast<const uint16_t*>(idx_gate), seq_idx, pos, T, B, static_cast<uint16_t*>(tail));
+}
+
+cudaError_t launch_compress_append(const void* kv, const void* kv_gate, const void* idx_key, const void* idx_gate,
+                                   const int32_t* seq_idx, const int64_t* pos, int T, int m, void* tail,
+                                   const int32_t* block_table, int B, int max_pages, int64_t n_pages,
+                                   uint8_t* main_pages, uint8_t* idx_pages, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  switch (m) {
+    case 1: return launch_compress_m<1>(kv, kv_gate, idx_key, idx_gate, seq_idx, pos, T, tail, block_table, B,
+                                        max_pages, n_pages, main_pages, idx_pages, stream);
+    case 2: return launch_compress_m<2>(kv, kv_gate, idx_key, idx_gate, seq_idx, pos, T, tail, block_table, B,
+                                        max_pages, n_pages, main_pages, idx_pages, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_quant_mxfp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales,

@@ -58,6 +58,11 @@ int check_batch(int B, int n_q, int max_nq = CSA2_MAX_PREFILL_NQ) {
   return CSA2_OK;
 }
 
+int check_ratio(int m) {
+  if (m != 1 && m != 2) return fail(CSA2_ERR_UNSUPPORTED, "tokens per entry m = %d (1 or 2 supported)", m);
+  return CSA2_OK;
+}
+
 int check_pages(const int32_t* block_table, int max_pages, int64_t n_pages) {
   CHECK_PTR(block_table, "block_table");
   if (max_pages < 1) return fail(CSA2_ERR_INVALID_ARG, "max_pages = %d < 1", max_pages);
@@ -156,6 +161,29 @@ int csa2_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, 
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "append_swa launch");
 }
 
+int csa2_compress_append(const void* kv, const void* kv_gate, const void* idx_key, const void* idx_gate,
+                         const int32_t* seq_idx, const int64_t* pos, int T, int m, void* tail,
+                         const int32_t* block_table, int B, int max_pages, int64_t n_pages,
+                         uint8_t* main_pages, uint8_t* idx_pages, void* stream) {
+  if (T < 0) return fail(CSA2_ERR_INVALID_ARG, "T = %d < 0", T);
+  if (int st = check_ratio(m)) return st;
+  if (T == 0) return CSA2_OK;
+  CHECK_A16(kv, "kv");
+  CHECK_A16(kv_gate, "kv_gate");
+  CHECK_A16(idx_key, "idx_key");
+  CHECK_A16(idx_gate, "idx_gate");
+  CHECK_PTR(seq_idx, "seq_idx");
+  CHECK_PTR(pos, "pos");
+  if (m > 1) CHECK_A16(tail, "tail");
+  CHECK_A16(main_pages, "main_pages");
+  CHECK_A16(idx_pages, "idx_pages");
+  if (B < 1) return fail(CSA2_ERR_INVALID_ARG, "B = %d < 1", B);
+  if (int st = check_pages(block_table, max_pages, n_pages)) return st;
+  cudaError_t e = csa2::launch_compress_append(kv, kv_gate, idx_key, idx_gate, seq_idx, pos, T, m, tail, block_table,
+                                               B, max_pages, n_pages, main_pages, idx_pages, S(stream));
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "compress_append launch");
+}
+
 int csa2_quant_fp8_entries(const void* x, int T, uint8_t* out, void* stream) {
   if (T < 0) return fail(CSA2_ERR_INVALID_ARG, "T = %d < 0", T);
   if (T == 0) return CSA2_OK;
@@ -225,38 +253,41 @@ static int check_indexer_inputs(const uint8_t* q_codes, const uint8_t* q_scales,
 int csa2_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
                       const int64_t* seq_len, int B, int n_q, int64_t max_ctx,
                       const int32_t* block_table, int max_pages, int64_t n_pages,
-                      const uint8_t* idx_pages, float* block_max, int64_t max_blocks,
+                      const uint8_t* idx_pages, float* block_max, int64_t max_blocks, int m,
                       void* stream) {
   if (int st = check_batch(B, n_q)) return st;
+  if (int st = check_ratio(m)) return st;
   if (B == 0) return CSA2_OK;
   if (int st = check_indexer_inputs(q_codes, q_scales, w, seq_len, idx_pages)) return st;
   if (int st = check_pages(block_table, max_pages, n_pages)) return st;
   CHECK_PTR(block_max, "block_max");
   if (max_ctx < 1) return fail(CSA2_ERR_INVALID_ARG, "max_ctx < 1");
-  if (max_blocks < (max_ctx + 7) / 8) return fail(CSA2_ERR_INVALID_ARG, "max_blocks < ceil(max_ctx / 8)");
+  if (max_blocks < (max_ctx / m + 7) / 8) return fail(CSA2_ERR_INVALID_ARG, "max_blocks < ceil(max_ctx / m / 8)");
   cudaError_t e = csa2::launch_indexer_scan(q_codes, q_scales, w, seq_len, B, n_q, max_ctx, block_table,
-                                            max_pages, n_pages, idx_pages, block_max, max_blocks, S(stream));
+                                            max_pages, n_pages, idx_pages, block_max, max_blocks, S(stream), m);
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "indexer_scan launch");
 }
 
 int csa2_block_topk(const float* block_max, const int64_t* seq_len, int B, int n_q,
-                    int64_t max_blocks, int32_t* pool, void* stream) {
+                    int64_t max_blocks, int32_t* pool, int m, void* stream) {
   if (int st = check_batch(B, n_q)) return st;
+  if (int st = check_ratio(m)) return st;
   if (B == 0) return CSA2_OK;
   CHECK_PTR(block_max, "block_max");
   CHECK_PTR(seq_len, "seq_len");
   CHECK_PTR(pool, "pool");
   if (max_blocks < 1) return fail(CSA2_ERR_INVALID_ARG, "max_blocks < 1");
-  cudaError_t e = csa2::launch_block_topk(block_max, seq_len, B, n_q, max_blocks, pool, S(stream));
+  cudaError_t e = csa2::launch_block_topk(block_max, seq_len, B, n_q, max_blocks, pool, S(stream), m);
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "block_topk launch");
 }
 
 int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
                          const int64_t* seq_len, int B, int n_q, const int32_t* block_table,
                          int max_pages, int64_t n_pages, const uint8_t* idx_pages,
-                         const int32_t* pool, int32_t* topk, void* ws, size_t ws_bytes,
+                         const int32_t* pool, int32_t* topk, void* ws, size_t ws_bytes, int m,
                          void* stream) {
   if (int st = check_batch(B, n_q)) return st;
+  if (int st = check_ratio(m)) return st;
   if (B == 0) return CSA2_OK;
   if (int st = check_indexer_inputs(q_codes, q_scales, w, seq_len, idx_pages)) return st;
   if (int st = check_pages(block_table, max_pages, n_pages)) return st;
@@ -267,7 +298,7 @@ int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const 
   if (!aligned16(ws)) return fail(CSA2_ERR_INVALID_ARG, "ws is not 16-byte aligned");
   float* scores = static_cast<float*>(ws);
   cudaError_t e = csa2::launch_pool_scores(q_codes, q_scales, w, seq_len, B, n_q, block_table, max_pages,
-                                           n_pages, idx_pages, pool, scores, S(stream));
+                                           n_pages, idx_pages, pool, scores, S(stream), m);
   if (e != cudaSuccess) return cuda_fail(e, "pool rescore launch");
   e = csa2::launch_pool_topk(scores, seq_len, B, n_q, pool, topk, S(stream));
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "pool top-k launch");
@@ -277,8 +308,9 @@ int csa2_indexer_full(const uint8_t* q_codes, const uint8_t* q_scales, const flo
                       const int64_t* seq_len, int B, int n_q, int64_t max_ctx,
                       const int32_t* block_table, int max_pages, int64_t n_pages,
                       const uint8_t* idx_pages, int32_t* pool, int32_t* topk, void* ws,
-                      size_t ws_bytes, void* stream) {
+                      size_t ws_bytes, int m, void* stream) {
   if (int st = check_batch(B, n_q)) return st;
+  if (int st = check_ratio(m)) return st;
   if (B == 0) return CSA2_OK;
   if (max_ctx < 1) return fail(CSA2_ERR_INVALID_ARG, "max_ctx < 1");
   const int64_t Q = static_cast<int64_t>(B) * n_q;
@@ -287,22 +319,23 @@ int csa2_indexer_full(const uint8_t* q_codes, const uint8_t* q_scales, const flo
   if (!aligned16(ws)) return fail(CSA2_ERR_INVALID_ARG, "ws is not 16-byte aligned");
   CHECK_PTR(pool, "pool");
   float* bm = static_cast<float*>(ws);
-  const int64_t max_blocks = (max_ctx + 7) / 8;
+  const int64_t max_blocks = (max_ctx / m + 7) / 8;
   if (int st = csa2_indexer_scan(q_codes, q_scales, w, seq_len, B, n_q, max_ctx, block_table, max_pages,
-                                 n_pages, idx_pages, bm, max_blocks, stream))
+                                 n_pages, idx_pages, bm, max_blocks, m, stream))
     return st;
-  if (int st = csa2_block_topk(bm, seq_len, B, n_q, max_blocks, pool, stream)) return st;
+  if (int st = csa2_block_topk(bm, seq_len, B, n_q, max_blocks, pool, m, stream)) return st;
   return csa2_indexer_reindex(q_codes, q_scales, w, seq_len, B, n_q, block_table, max_pages, n_pages,
                               idx_pages, pool, topk, static_cast<uint8_t*>(ws) + blockmax_ws(Q, max_ctx),
-                              ws_bytes - blockmax_ws(Q, max_ctx), stream);
+                              ws_bytes - blockmax_ws(Q, max_ctx), m, stream);
 }
 
 static int sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len, int B, int n_q,
                        const int32_t* block_table, int max_pages, int64_t n_pages,
                        const uint8_t* main_pages, const uint8_t* rings, const int32_t* ring_idx,
                        int64_t n_rings, const uint8_t* swa_chunk, float softmax_scale, int out_dtype,
-                       void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+                       void* out, float* lse, void* ws, size_t ws_bytes, int m, void* stream) {
   if (int st = check_batch(B, n_q, swa_chunk ? CSA2_MAX_PREFILL_NQ : CSA2_MAX_NQ)) return st;
+  if (int st = check_ratio(m)) return st;
   if (B == 0) return CSA2_OK;
   if (swa_chunk && !aligned16(swa_chunk)) return fail(CSA2_ERR_INVALID_ARG, "swa_chunk is not 16-byte aligned");
   CHECK_A16(q, "q");
@@ -326,7 +359,7 @@ static int sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_le
   }
   cudaError_t e = csa2::launch_sparse_attn(q, topk, seq_len, B, n_q, block_table, max_pages, n_pages,
                                            main_pages, rings, ring_idx, n_rings, swa_chunk, softmax_scale,
-                                           out_dtype, out, lse, ws, S(stream));
+                                           out_dtype, out, lse, ws, S(stream), m);
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "sparse_attn launch");
 }
 
@@ -334,9 +367,9 @@ int csa2_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len,
                      const int32_t* block_table, int max_pages, int64_t n_pages,
                      const uint8_t* main_pages, const uint8_t* rings, const int32_t* ring_idx,
                      int64_t n_rings, float softmax_scale, int out_dtype, void* out, float* lse,
-                     void* ws, size_t ws_bytes, void* stream) {
+                     void* ws, size_t ws_bytes, int m, void* stream) {
   return sparse_attn(q, topk, seq_len, B, n_q, block_table, max_pages, n_pages, main_pages, rings, ring_idx,
-                     n_rings, nullptr, softmax_scale, out_dtype, out, lse, ws, ws_bytes, stream);
+                     n_rings, nullptr, softmax_scale, out_dtype, out, lse, ws, ws_bytes, m, stream);
 }
 
 int csa2_sparse_attn_prefill(const void* q, const int32_t* topk, const int64_t* seq_len, int B,
@@ -344,20 +377,21 @@ int csa2_sparse_attn_prefill(const void* q, const int32_t* topk, const int64_t* 
                              const uint8_t* main_pages, const uint8_t* rings,
                              const int32_t* ring_idx, int64_t n_rings, const uint8_t* swa_chunk,
                              float softmax_scale, int out_dtype, void* out, float* lse, void* ws,
-                             size_t ws_bytes, void* stream) {
+                             size_t ws_bytes, int m, void* stream) {
   CHECK_A16(swa_chunk, "swa_chunk");
   return sparse_attn(q, topk, seq_len, B, n_q, block_table, max_pages, n_pages, main_pages, rings, ring_idx,
-                     n_rings, swa_chunk, softmax_scale, out_dtype, out, lse, ws, ws_bytes, stream);
+                     n_rings, swa_chunk, softmax_scale, out_dtype, out, lse, ws, ws_bytes, m, stream);
 }
 
 static int run_layer(const csa2_layer_args* a, int32_t* pool, int32_t* topk, void* stream) {
+  const int m = a->tokens_per_entry == 0 ? 1 : a->tokens_per_entry;
   switch (a->mode) {
     case CSA2_MODE_FULL:
       CHECK_PTR(pool, "pool (FULL)");
       CHECK_PTR(topk, "topk (FULL)");
       if (int st = csa2_indexer_full(a->q_idx_codes, a->q_idx_scales, a->w, a->seq_len, a->B, a->n_q,
                                      a->max_ctx, a->block_table, a->max_pages, a->n_pages, a->idx_pages,
-                                     pool, topk, a->ws, a->ws_bytes, stream))
+                                     pool, topk, a->ws, a->ws_bytes, m, stream))
         return st;
       break;
     case CSA2_MODE_REINDEX:
@@ -365,7 +399,7 @@ static int run_layer(const csa2_layer_args* a, int32_t* pool, int32_t* topk, voi
       CHECK_PTR(topk, "topk (REINDEX)");
       if (int st = csa2_indexer_reindex(a->q_idx_codes, a->q_idx_scales, a->w, a->seq_len, a->B, a->n_q,
                                         a->block_table, a->max_pages, a->n_pages, a->idx_pages, pool, topk,
-                                        a->ws, a->ws_bytes, stream))
+                                        a->ws, a->ws_bytes, m, stream))
         return st;
       break;
     case CSA2_MODE_REUSE:
@@ -376,7 +410,7 @@ static int run_layer(const csa2_layer_args* a, int32_t* pool, int32_t* topk, voi
   }
   return sparse_attn(a->q, topk, a->seq_len, a->B, a->n_q, a->block_table, a->max_pages, a->n_pages,
                      a->main_pages, a->rings, a->ring_idx, a->n_rings, a->swa_chunk, a->softmax_scale,
-                     a->out_dtype, a->out, a->lse, a->ws, a->ws_bytes, stream);
+                     a->out_dtype, a->out, a->lse, a->ws, a->ws_bytes, m, stream);
 }
 
 int csa2_decode_layer(const csa2_layer_args* layer, void* stream) {

@@ -22,6 +22,13 @@ cudaError_t launch_append_kv(const void* latent, const void* idx_key, const int3
                              const int64_t* pos, int T, const int32_t* block_table, int B,
                              int max_pages, int64_t n_pages, uint8_t* main_pages,
                              uint8_t* idx_pages, cudaStream_t stream);
+// Encoder-side append at ratio m (1 or 2): entries from groups of m tokens
+// (softmax of their logits per channel), MXFP4 into entry pages; pending
+// tokens into tail [B][m-1][1280] bf16.
+cudaError_t launch_compress_append(const void* kv, const void* kv_gate, const void* idx_key, const void* idx_gate,
+                                   const int32_t* seq_idx, const int64_t* pos, int T, int m, void* tail,
+                                   const int32_t* block_table, int B, int max_pages, int64_t n_pages,
+                                   uint8_t* main_pages, uint8_t* idx_pages, cudaStream_t stream);
 // ring_idx == NULL: E4M3 of T entries into rings viewed as [T, 512] (pos unused).
 cudaError_t launch_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, int T,
                               int64_t n_rings, uint8_t* rings, cudaStream_t stream);
@@ -39,17 +46,17 @@ cudaError_t launch_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales,
                                 const int64_t* seq_len, int B, int n_q, int64_t max_ctx,
                                 const int32_t* block_table, int max_pages, int64_t n_pages,
                                 const uint8_t* idx_pages, float* block_max, int64_t max_blocks,
-                                cudaStream_t stream);
+                                cudaStream_t stream, int m = 1);
 // Pool rescore -> per-slot scores [B*n_q, 2048*8] (-inf for empty / future slots).
 cudaError_t launch_pool_scores(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
                                const int64_t* seq_len, int B, int n_q,
                                const int32_t* block_table, int max_pages, int64_t n_pages,
                                const uint8_t* idx_pages, const int32_t* pool, float* scores,
-                               cudaStream_t stream);
+                               cudaStream_t stream, int m = 1);
 
 // Top-k selections (one CTA per query token).
 cudaError_t launch_block_topk(const float* block_max, const int64_t* seq_len, int B, int n_q,
-                              int64_t max_blocks, int32_t* pool, cudaStream_t stream);
+                              int64_t max_blocks, int32_t* pool, cudaStream_t stream, int m = 1);
 cudaError_t launch_pool_topk(const float* scores, const int64_t* seq_len, int B, int n_q,
                              const int32_t* pool, int32_t* topk, cudaStream_t stream);
 
@@ -60,6 +67,6 @@ cudaError_t launch_sparse_attn(const void* q, const int32_t* topk, const int64_t
                                int64_t n_pages, const uint8_t* main_pages, const uint8_t* rings,
                                const int32_t* ring_idx, int64_t n_rings, const uint8_t* swa_chunk,
                                float softmax_scale, int out_dtype, void* out, float* lse, void* ws,
-                               cudaStream_t stream);
+                               cudaStream_t stream, int m = 1);
 
 }  // namespace csa2

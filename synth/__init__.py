@@ -19,6 +19,8 @@ _LIB = os.path.join(_HERE, "_synth.so")
 # Tensor ids of the counter streams (per-layer tensors add the layer index).
 LATENT = 1      # main-KV latent entries, (seq, pos) -> 512 bf16
 IDXKEY = 2      # indexer keys, (seq, pos) -> 128 bf16
+KVGATE = 3      # compression logits of the latent candidates (m > 1), (seq, pos) -> 512 bf16
+IDXGATE = 4     # compression logits of the indexer-key candidates (m > 1), (seq, pos) -> 128 bf16
 Q = 16          # attention queries, (seq, t) -> 64 x 512 bf16        (+ layer)
 IDXQ = 32       # indexer queries, (seq, t) -> 32 x 128 bf16          (+ layer)
 W = 48          # indexer head weights, (seq, t) -> 32 fp32 U(0,1)    (+ layer)

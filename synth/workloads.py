@@ -20,6 +20,7 @@ class Workload:
     n_q: int = 1        # query tokens per sequence
     layers: tuple = field(default=("full",))
     prefill: bool = False
+    m: int = 1          # tokens per entry: 1 decoder layers, 2 encoder layers
 
     @property
     def seed(self) -> int:

@@ -70,6 +70,9 @@ class Setup:
     step_pos: torch.Tensor | None = None
     step_swa: list = field(default_factory=list)     # per layer bf16 [B*n_q, 512]
     step_ring_idx: list = field(default_factory=list)
+    step_kv_gate: torch.Tensor | None = None         # m > 1: compression logits of the step's tokens
+    step_idx_gate: torch.Tensor | None = None
+    tail: torch.Tensor | None = None                 # m > 1: bf16 [B, m-1, 1280] compressor state
 
     @property
     def B(self):
@@ -78,6 +81,10 @@ class Setup:
     @property
     def n_q(self):
         return self.wl.n_q
+
+    @property
+    def m(self):
+        return self.wl.m
 
     def t(self, j: int) -> int:
         return self.N - self.n_q + j
@@ -100,11 +107,14 @@ def build(wl: Workload, device="cuda", *, N=None, B=None, n_q=None, shuffle_seed
 
     if N is not None or B is not None or n_q is not None:
         wl = Workload(wl.index, wl.name, wl.mode, B=B or wl.B, N=N or wl.N, n_q=n_q or wl.n_q, layers=wl.layers,
-                      prefill=wl.prefill)
-    N, Bq, nq, seed = wl.N, wl.B, wl.n_q, wl.seed
+                      prefill=wl.prefill, m=wl.m)
+    N, Bq, nq, seed, m = wl.N, wl.B, wl.n_q, wl.seed, wl.m
     n_layers = len(wl.layers)
-    cache = PagedCache(Bq, N, n_rings=Bq * n_layers, device=device, shuffle_seed=shuffle_seed)
+    # The store holds entries: one per token (m = 1) or per m tokens.
+    cache = PagedCache(Bq, (N + m - 1) // m, n_rings=Bq * n_layers, device=device, shuffle_seed=shuffle_seed)
     S = Setup(wl=wl, N=N, cache=cache, seq_len=torch.full((Bq,), N, dtype=torch.int64, device=device))
+    if m > 1:
+        S.tail = torch.zeros(Bq, m - 1, 1280, dtype=torch.bfloat16, device=device)
     pre = N - nq
     for b in range(Bq):
         for p0 in range(0, pre, chunk):
@@ -113,7 +123,13 @@ def build(wl: Workload, device="cuda", *, N=None, B=None, n_q=None, shuffle_seed
             key = u16_to_bf16(synth.normal(seed, synth.IDXKEY, b, p0, n, 128), device)
             seq = torch.full((n,), b, dtype=torch.int32, device=device)
             pos = torch.arange(p0, p0 + n, dtype=torch.int64, device=device)
-            csa2.csa2_append_kv(lat, key, seq, pos, cache.block_table, cache.main_pages, cache.idx_pages)
+            if m == 1:
+                csa2.csa2_append_kv(lat, key, seq, pos, cache.block_table, cache.main_pages, cache.idx_pages)
+            else:
+                lg = u16_to_bf16(synth.normal(seed, synth.KVGATE, b, p0, n, 512), device)
+                kg = u16_to_bf16(synth.normal(seed, synth.IDXGATE, b, p0, n, 128), device)
+                csa2.csa2_compress_append(lat, lg, key, kg, seq, pos, m, S.tail, cache.block_table, cache.main_pages,
+                                          cache.idx_pages)
     # Window entries of the 128 positions before the step's tokens, one ring per
     # (layer, sequence): the ring state a prefill chunk starts from; a decode
     # step's appends then leave positions N-128 .. N-1.
@@ -130,6 +146,11 @@ def build(wl: Workload, device="cuda", *, N=None, B=None, n_q=None, shuffle_seed
     key = np.concatenate([synth.normal(seed, synth.IDXKEY, b, pre, nq, 128) for b in range(Bq)])
     S.step_latent = u16_to_bf16(lat, device)
     S.step_idx_key = u16_to_bf16(key, device)
+    if m > 1:
+        S.step_kv_gate = u16_to_bf16(np.concatenate([synth.normal(seed, synth.KVGATE, b, pre, nq, 512)
+                                                     for b in range(Bq)]), device)
+        S.step_idx_gate = u16_to_bf16(np.concatenate([synth.normal(seed, synth.IDXGATE, b, pre, nq, 128)
+                                                      for b in range(Bq)]), device)
     S.step_seq = torch.arange(Bq, dtype=torch.int32, device=device).repeat_interleave(nq)
     S.step_pos = torch.arange(pre, N, dtype=torch.int64, device=device).repeat(Bq)
     for li in range(n_layers):
@@ -155,8 +176,10 @@ def build(wl: Workload, device="cuda", *, N=None, B=None, n_q=None, shuffle_seed
             for b in range(Bq):
                 for j in range(nq):
                     t = N - nq + j
-                    s = synth.sample_sorted(seed, synth.POOL + li, b, t, n_blocks(t), 2048)
-                    pools[b, j, : s.size] = s
+                    te = (t + 1) // m - 1  # the token's last visible entry
+                    if te >= 0:
+                        s = synth.sample_sorted(seed, synth.POOL + li, b, t, n_blocks(te), 2048)
+                        pools[b, j, : s.size] = s
             L.pool = torch.from_numpy(pools).to(device)
         S.layers.append(L)
     if wl.layers[0] == "reuse":
@@ -164,8 +187,10 @@ def build(wl: Workload, device="cuda", *, N=None, B=None, n_q=None, shuffle_seed
         for b in range(Bq):
             for j in range(nq):
                 t = N - nq + j
-                s = synth.sample_sorted(seed, synth.TOPK, b, t, t + 1, 512)
-                tk[b, j, : s.size] = s
+                te = (t + 1) // m - 1
+                if te >= 0:
+                    s = synth.sample_sorted(seed, synth.TOPK, b, t, te + 1, 512)
+                    tk[b, j, : s.size] = s
         S.topk = torch.from_numpy(tk).to(device)
     else:
         S.topk = torch.full((Bq, nq, 512), -1, dtype=torch.int32, device=device)
@@ -174,12 +199,26 @@ def build(wl: Workload, device="cuda", *, N=None, B=None, n_q=None, shuffle_seed
     return S
 
 
+def append_main(S: Setup, latent=None, idx_key=None, kv_gate=None, idx_gate=None):
+    """A1 of the step: the n_q new tokens of every sequence into the store
+    (compressed m tokens per entry when m > 1)."""
+    import sparse_attention_fp4_mxfp4_gb300 as csa2
+    c = S.cache
+    lat = S.step_latent if latent is None else latent
+    key = S.step_idx_key if idx_key is None else idx_key
+    if S.m == 1:
+        csa2.csa2_append_kv(lat, key, S.step_seq, S.step_pos, c.block_table, c.main_pages, c.idx_pages)
+    else:
+        csa2.csa2_compress_append(lat, S.step_kv_gate if kv_gate is None else kv_gate, key,
+                                  S.step_idx_gate if idx_gate is None else idx_gate, S.step_seq, S.step_pos, S.m,
+                                  S.tail, c.block_table, c.main_pages, c.idx_pages)
+
+
 def append_step(S: Setup):
     """A1 + A2 of one decode step: the n_q new entries of every sequence."""
     import sparse_attention_fp4_mxfp4_gb300 as csa2
     c = S.cache
-    csa2.csa2_append_kv(S.step_latent, S.step_idx_key, S.step_seq, S.step_pos, c.block_table, c.main_pages,
-                        c.idx_pages)
+    append_main(S)
     for li in range(len(S.layers)):
         csa2.csa2_append_swa(S.step_swa[li], S.step_ring_idx[li], S.step_pos, c.rings)
 
@@ -204,7 +243,7 @@ class Runner:
         dev = S.seq_len.device
         B, n_q, N = S.B, S.n_q, S.N
         Q = B * n_q
-        self.max_blocks = (N + 7) // 8
+        self.max_blocks = (N // S.m + 7) // 8
         self.ws = torch.empty(csa2.csa2_workspace_bytes(csa2.OP_DECODE_LAYER, B, n_q, N), dtype=torch.uint8,
                               device=dev)
         bm_bytes = Q * self.max_blocks * 4
@@ -248,26 +287,25 @@ class Runner:
                 if L.kind in ("full", "reindex"):
                     csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
                     n += 1
-        csa2.csa2_append_kv(S.step_latent, S.step_idx_key, S.step_seq, S.step_pos, c.block_table, c.main_pages,
-                            c.idx_pages)
-        n += 1 + len(S.layers)
+        append_main(S)
+        n += (1 if S.m == 1 else 2) + len(S.layers)
         main.wait_stream(s_q)
         swa_joined = False
         for li, L in enumerate(S.layers):
             if L.kind == "full":
                 mark("scan0")
                 csa2.csa2_indexer_scan(L.q_codes, L.q_scales, L.w, S.seq_len, S.N, c.block_table, c.n_pages,
-                                       c.idx_pages, self.bm)
+                                       c.idx_pages, self.bm, m=S.m)
                 mark("scan1")
                 mark("blocktopk0")
-                csa2.csa2_block_topk(self.bm, S.seq_len, self.pool)
+                csa2.csa2_block_topk(self.bm, S.seq_len, self.pool, m=S.m)
                 mark("blocktopk1")
                 n += 2
             if L.kind in ("full", "reindex"):
                 pool = self.pool if L.kind == "full" else L.pool
                 mark("rescore0")
                 csa2.csa2_indexer_reindex(L.q_codes, L.q_scales, L.w, S.seq_len, c.block_table, c.n_pages,
-                                          c.idx_pages, pool, self.topk, self.rws)
+                                          c.idx_pages, pool, self.topk, self.rws, m=S.m)
                 mark("rescore1")
                 n += 2
             if not swa_joined:
@@ -277,10 +315,10 @@ class Runner:
             if self.prefill:
                 csa2.csa2_sparse_attn_prefill(L.q, self.topk, S.seq_len, c.block_table, c.n_pages, c.main_pages,
                                               c.rings, L.ring_idx, self.chunk[li], self.out[li], self.lse[li],
-                                              self.ws)
+                                              self.ws, m=S.m)
             else:
                 csa2.csa2_sparse_attn(L.q, self.topk, S.seq_len, c.block_table, c.n_pages, c.main_pages, c.rings,
-                                      L.ring_idx, self.out[li], self.lse[li], self.ws)
+                                      L.ring_idx, self.out[li], self.lse[li], self.ws, m=S.m)
             mark("attn1")
             n += self.attn_launches
             if self.prefill:
@@ -291,8 +329,42 @@ class Runner:
 
 # ---- oracle references ------------------------------------------------------------
 
+def entries_seen(S: Setup, t: int) -> int:
+    """Complete entries visible to the token at position t."""
+    return (t + 1) // S.m
+
+
+def oracle_entry_rows(S: Setup, b: int, entries, key=False) -> np.ndarray:
+    """bf16 rows of the given entries: the tokens' own values (m = 1) or the
+    oracle's compression of each entry's m tokens."""
+    import oracle
+    seed, m = S.wl.seed, S.m
+    e = np.asarray(entries, np.int64)
+    if m == 1:
+        if key:
+            return synth.normal_rows(seed, synth.IDXKEY, np.full(e.size, b), e, 128)
+        return synth.latent_rows(seed, np.full(e.size, b), e)
+    toks = (e[:, None] * m + np.arange(m)).reshape(-1)
+    bs = np.full(toks.size, b)
+    if key:
+        x = synth.normal_rows(seed, synth.IDXKEY, bs, toks, 128)
+        z = synth.normal_rows(seed, synth.IDXGATE, bs, toks, 128)
+    else:
+        x = synth.latent_rows(seed, bs, toks)
+        z = synth.normal_rows(seed, synth.KVGATE, bs, toks, 512)
+    d = x.shape[-1]
+    return oracle.compress(x.reshape(e.size, m, d), z.reshape(e.size, m, d))
+
+
 def oracle_keys(S: Setup, b: int, t: int) -> np.ndarray:
-    return synth.normal(S.wl.seed, synth.IDXKEY, b, 0, t + 1, 128)
+    """Indexer keys (bf16) of every entry visible at token position t."""
+    if S.m == 1:
+        return synth.normal(S.wl.seed, synth.IDXKEY, b, 0, t + 1, 128)
+    import oracle
+    n = entries_seen(S, t)
+    x = synth.normal(S.wl.seed, synth.IDXKEY, b, 0, n * S.m, 128).reshape(n, S.m, 128)
+    z = synth.normal(S.wl.seed, synth.IDXGATE, b, 0, n * S.m, 128).reshape(n, S.m, 128)
+    return oracle.compress(x, z)
 
 
 def oracle_full(S: Setup, b: int, j: int, li: int = 0, keys=None):
@@ -300,7 +372,7 @@ def oracle_full(S: Setup, b: int, j: int, li: int = 0, keys=None):
     L = S.layers[li]
     t = S.t(j)
     keys = oracle_keys(S, b, t) if keys is None else keys
-    return oracle.full_indexer(L.q_idx_u16[b, j], L.w_np[b, j], keys, t)
+    return oracle.full_indexer(L.q_idx_u16[b, j], L.w_np[b, j], keys, entries_seen(S, t) - 1)
 
 
 def oracle_reindex(S: Setup, b: int, j: int, li: int, pool_row, keys=None):
@@ -308,7 +380,8 @@ def oracle_reindex(S: Setup, b: int, j: int, li: int, pool_row, keys=None):
     L = S.layers[li]
     t = S.t(j)
     keys = oracle_keys(S, b, t) if keys is None else keys
-    return oracle.reindex(L.q_idx_u16[b, j], L.w_np[b, j], keys, t, np.asarray(pool_row, np.int32))
+    return oracle.reindex(L.q_idx_u16[b, j], L.w_np[b, j], keys, entries_seen(S, t) - 1,
+                          np.asarray(pool_row, np.int32))
 
 
 def oracle_attention(S: Setup, b: int, j: int, li: int, topk_row, exact_window=False):
@@ -319,7 +392,7 @@ def oracle_attention(S: Setup, b: int, j: int, li: int, topk_row, exact_window=F
     t = S.t(j)
     sel = np.asarray(topk_row)
     sel = sel[sel >= 0].astype(np.int64)
-    main = synth.latent_rows(seed, np.full(sel.size, b), sel)
+    main = oracle_entry_rows(S, b, sel)
     win = oracle.window_positions(t, t + 1 if exact_window else S.N, 128)
     wrows = synth.latent_rows(seed, np.full(win.size, b), win, tensor=synth.SWA + li)
     return oracle.sparse_attention(S.layers[li].q_u16[b, j], main, wrows, TAU)

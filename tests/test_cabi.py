@@ -69,19 +69,20 @@ def test_size_queries(lib):
 def test_prefill_and_refill_host_checks(lib):
     p, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     lib.csa2_last_error.restype = ctypes.c_char_p
-    lib.csa2_sparse_attn.argtypes = [p, p, p, i32, i32, p, i32, i64, p, p, p, i64, f32, i32, p, p, p, sz, p]
+    lib.csa2_sparse_attn.argtypes = [p, p, p, i32, i32, p, i32, i64, p, p, p, i64, f32, i32, p, p, p, sz, i32, p]
     lib.csa2_sparse_attn_prefill.argtypes = [p, p, p, i32, i32, p, i32, i64, p, p, p, i64, p, f32, i32, p, p, p,
-                                             sz, p]
+                                             sz, i32, p]
     x = p(4096)  # an aligned non-null address; no call below reaches the device
     # The decode attention keeps its 8-token limit (its window comes from the ring alone).
-    assert lib.csa2_sparse_attn(x, x, x, 1, 9, x, 1, 1, x, x, x, 1, 0.05, 0, x, None, None, 0, None) == 2
+    assert lib.csa2_sparse_attn(x, x, x, 1, 9, x, 1, 1, x, x, x, 1, 0.05, 0, x, None, None, 0, 1, None) == 2
+    assert lib.csa2_sparse_attn(x, x, x, 1, 1, x, 1, 1, x, x, x, 1, 0.05, 0, x, None, None, 0, 3, None) == 2  # m = 3
     assert lib.csa2_sparse_attn_prefill(x, x, x, 1, 9, x, 1, 1, x, x, x, 1, None, 0.05, 0, x, None, None, 0,
-                                        None) == 1
+                                        1, None) == 1
     assert b"swa_chunk" in lib.csa2_last_error()
     assert lib.csa2_sparse_attn_prefill(x, x, x, 1, 9, x, 1, 1, x, x, x, 1, p(4100), 0.05, 0, x, None, None, 0,
-                                        None) == 1
+                                        1, None) == 1
     assert lib.csa2_sparse_attn_prefill(x, x, x, 1, 4097, x, 1, 1, x, x, x, 1, x, 0.05, 0, x, None, None, 0,
-                                        None) == 2
+                                        1, None) == 2
     lib.csa2_ring_refill.argtypes = [p, p, i32, i32, p, i64, p, p]
     assert lib.csa2_ring_refill(None, None, 1, 0, None, 1, None, None) == 0  # nothing to do
     assert lib.csa2_ring_refill(None, x, 1, 4, x, 1, x, None) == 1
