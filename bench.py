@@ -148,15 +148,16 @@ def barrier(world):
 # ---- algorithmic bytes (reads the method must do) --------------------------------------
 
 def scan_bytes(wl) -> int:
-    """Full scan: 72 B per causal position per sequence (all n_q tokens share
-    the read) + the FP4 indexer query and head weights of each token."""
-    return wl.B * (72 * wl.N + wl.n_q * (32 * 72 + 32 * 4))
+    """Full scan: 72 B per causal entry per sequence (all n_q tokens share
+    the read; an entry is a token, or m tokens on the encoder side) + the FP4
+    indexer query and head weights of each token."""
+    return wl.B * (72 * (wl.N // wl.m) + wl.n_q * (32 * 72 + 32 * 4))
 
 
 def causal_positions(wl) -> int:
-    """Positions scored by the Full scan per step: sum over tokens of t + 1."""
-    t0 = wl.N - wl.n_q
-    return wl.B * (wl.n_q * (t0 + 1) + wl.n_q * (wl.n_q - 1) // 2)
+    """Entries scored by the Full scan per step: sum over tokens of the
+    entries each sees, floor((t + 1) / m)."""
+    return wl.B * sum((wl.N - wl.n_q + j + 1) // wl.m for j in range(wl.n_q))
 
 
 def scan_alu_ops(wl) -> int:
@@ -192,7 +193,7 @@ def stage_roofline(wl, kinds, stage_ms, peak) -> dict:
     n_full, n_reidx = kinds.count("full"), kinds.count("reindex")
     stage_bytes = {
         "scan": n_full * scan_bytes(wl),
-        "blocktopk": n_full * q * 4 * ((wl.N + 7) // 8),
+        "blocktopk": n_full * q * 4 * ((wl.N // wl.m + 7) // 8),
         "rescore": (n_full + n_reidx) * q * (2048 * 576 + 32 * 72 + 32 * 4 + 2048 * 4),
         "attn": len(kinds) * q * attn_bytes_per_query(),
     }
@@ -353,7 +354,7 @@ def run_ours(args, wl, rank, world, local):
         "dtype": "fp4(e2m1)+e4m3 storage, f16 tensor-core operands, fp32 accumulate/softmax, bf16 out",
         "data": "synthetic (seeded generator; RMSNormed post-RoPE latents, N(0,1) indexer keys/queries)",
         "config": {"workload": wl.name, "mode": wl.mode, "layers": list(kinds), "batch": B, "context": N,
-                   "query_tokens": n_q, "queries_per_step": Q, "prefill": wl.prefill,
+                   "query_tokens": n_q, "queries_per_step": Q, "prefill": wl.prefill, "tokens_per_entry": wl.m,
                    "l2": "inputs larger than L2 (store of %.1f GB; the step reads %.0f MB)" % (
                        S.cache.nbytes() / 1e9, step_bytes(wl) / 1e6),
                    "parallelism": f"replicas x{world} (independent sequences)", "setup_s": round(setup_s, 1),
@@ -377,8 +378,11 @@ def run_e2e(args, wl, S, R, dev):
     its new entries and every layer's queries from pinned host memory, runs
     the layers with csa2_decode_group and reads every layer's output back."""
     import sparse_attention_fp4_mxfp4_gb300 as csa2
+    from tests import harness as H
     c = S.cache
     host = {"latent": S.step_latent, "key": S.step_idx_key}
+    if wl.m > 1:
+        host["kv_gate"], host["idx_gate"] = S.step_kv_gate, S.step_idx_gate
     for li, L in enumerate(S.layers):
         host[f"swa{li}"] = S.step_swa[li]
         host[f"q{li}"] = L.q
@@ -399,15 +403,14 @@ def run_e2e(args, wl, S, R, dev):
             q_idx_codes=L.q_codes, q_idx_scales=L.q_scales, w=dev_in.get(f"w{li}"),
             pool=R.pool if L.kind == "full" else L.pool if L.kind == "reindex" else None,
             topk=R.topk if L.kind != "reuse" or li == 0 else None,
-            swa_chunk=R.chunk[li] if wl.prefill else None))
+            swa_chunk=R.chunk[li] if wl.prefill else None, m=wl.m))
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(o.numel() * o.element_size() for o in outs_h) + sum(x.numel() * 4 for x in lses_h)
 
     def step():
         for k, v in host.items():
             dev_in[k].copy_(v, non_blocking=True)
-        csa2.csa2_append_kv(dev_in["latent"], dev_in["key"], S.step_seq, S.step_pos, c.block_table,
-                            c.main_pages, c.idx_pages)
+        H.append_main(S, dev_in["latent"], dev_in["key"], dev_in.get("kv_gate"), dev_in.get("idx_gate"))
         for li, L in enumerate(S.layers):
             if wl.prefill:
                 csa2.csa2_quant_fp8_entries(dev_in[f"swa{li}"], R.chunk[li])
@@ -454,20 +457,30 @@ def oracle_query(wl, b=0, j=0, n_scan=None):
     li = 0
     q = synth.normal(seed, synth.Q + li, b, N - n_q + j, 1, 64 * 512).reshape(64, 512)
     desc = ""
-    if wl.mode in ("full", "reindex"):
+    first = wl.layers[0]  # the layer whose query is timed (a group's first layer)
+    if first in ("full", "reindex"):
         qi = synth.normal(seed, synth.IDXQ + li, b, t, 1, 32 * 128).reshape(32, 128)
         w = synth.uniform(seed, synth.W + li, b, t, 1, 32)[0]
-    if wl.mode == "full":
-        n = t + 1 if n_scan is None else min(t + 1, n_scan)
-        keys = synth.normal(seed, synth.IDXKEY, b, 0, n, 128)
+    m = wl.m
+    n_ent = (t + 1) // m  # entries the token sees
+    if first == "full":
+        n = n_ent if n_scan is None else min(n_ent, n_scan)
         t0 = time.perf_counter()
+        if m == 1:
+            keys = synth.normal(seed, synth.IDXKEY, b, 0, n, 128)
+        else:  # the oracle compresses each entry's m tokens first
+            x = synth.normal(seed, synth.IDXKEY, b, 0, n * m, 128).reshape(n, m, 128)
+            z = synth.normal(seed, synth.IDXGATE, b, 0, n * m, 128).reshape(n, m, 128)
+            keys = oracle.compress(x, z)
         r = oracle.full_indexer(qi, w, keys, n - 1, want_scores=False)
         t_idx = time.perf_counter() - t0
-        scale = (t + 1) / n
+        scale = n_ent / n
         sel = r["topk"]
-        desc = f"Full-mode query: oracle scan of {n} of {t + 1} positions" + (
-            f", scan time scaled x{scale:.1f}" if scale > 1 else "")
-    elif wl.mode == "reindex":
+        desc = f"Full-mode query: oracle scan of {n} of {n_ent} entries" + (
+            f", scan time scaled x{scale:.1f}" if scale > 1 else "") + (
+            f" ({m} tokens per entry, compressed by the oracle)" if m > 1 else "")
+    elif first == "reindex":
+        assert m == 1, "the reference timing of a Reindex layer is written for one token per entry"
         keys = synth.normal(seed, synth.IDXKEY, b, 0, t + 1, 128)
         pool = synth.sample_sorted(seed, synth.POOL + li, b, t, n_blocks(t), 2048)
         t0 = time.perf_counter()
@@ -477,12 +490,18 @@ def oracle_query(wl, b=0, j=0, n_scan=None):
         sel = r["topk"]
         desc = "Reindex-mode query"
     else:
-        sel = synth.sample_sorted(seed, synth.TOPK, b, t, t + 1, 512)
+        sel = synth.sample_sorted(seed, synth.TOPK, b, t, n_ent, 512)
         t_idx, scale = 0.0, 1.0
         desc = "Reuse-mode query"
     sel = np.asarray(sel)
     sel = sel[sel >= 0].astype(np.int64)
-    main = synth.latent_rows(seed, np.full(sel.size, b), sel)
+    if m == 1:
+        main = synth.latent_rows(seed, np.full(sel.size, b), sel)
+    else:
+        toks = (sel[:, None] * m + np.arange(m)).reshape(-1)
+        x = synth.latent_rows(seed, np.full(toks.size, b), toks).reshape(sel.size, m, 512)
+        z = synth.normal_rows(seed, synth.KVGATE, np.full(toks.size, b), toks, 512).reshape(sel.size, m, 512)
+        main = oracle.compress(x, z)
     # A prefill token's window is exact: the decode window of a context ending at t.
     win = oracle.window_positions(t, t + 1 if wl.prefill else N, 128)
     wrows = synth.latent_rows(seed, np.full(win.size, b), win, tensor=synth.SWA + li)
@@ -517,12 +536,12 @@ def run_reference(args, wl, rank, world):
     n_total = args.steps + args.warmup
     # Bound the whole run to about two minutes: the scan sample per step shrinks with the step count.
     n_scan = None
-    if wl.mode == "full":
-        probe_n = min(wl.N, 65536)
+    if wl.layers[0] == "full":
+        probe_n = min(wl.N // wl.m, 65536)
         t0 = time.perf_counter()
         oracle_query(wl, n_scan=probe_n)
         per_pos = (time.perf_counter() - t0) / probe_n
-        n_scan = int(max(4096, min(wl.N, 100.0 / max(1, n_total) / max(per_pos, 1e-9))))
+        n_scan = int(max(4096, min(wl.N // wl.m, 100.0 / max(1, n_total) / max(per_pos, 1e-9))))
     for _ in range(args.warmup):
         oracle_query(wl, n_scan=n_scan)
     scaled = []

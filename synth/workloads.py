@@ -1,5 +1,6 @@
-"""The five decode workloads of the CSA2 path and one chunked-prefill
-workload, as sizes and seeds.
+"""The five decode workloads of the CSA2 path, one chunked-prefill workload
+and one encoder-side group (2 tokens per entry: a Full layer and five Reuse
+layers), as sizes and seeds.
 
 Each workload is seeded with 1000 + its index. Query token j of n_q sits at
 absolute position t = N - n_q + j, where N counts the entries in the cache
@@ -39,6 +40,8 @@ WORKLOADS = {
     4: Workload(4, "group_reindex_3reuse_b32_n256k_q6", "group", B=32, N=262144, n_q=6,
                 layers=("reindex", "reuse", "reuse", "reuse")),
     5: Workload(5, "prefill_full_b1_n128k_c4096", "full", B=1, N=131072, n_q=4096, prefill=True),
+    6: Workload(6, "encoder_full_5reuse_m2_b8_n1m", "group", B=8, N=1048576,
+                layers=("full", "reuse", "reuse", "reuse", "reuse", "reuse"), m=2),
 }
 
 # Method constants (decoder CSA2 at m = 1).

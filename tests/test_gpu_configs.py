@@ -9,6 +9,8 @@ times (tests.harness.Runner), on outputs the oracle can compute one by one:
      token) pairs and the attention of all four layers for them
   5  Full prefill chunk, 1 x 128K, 4096 tokens: pool, top-512 and attention
      (exact causal window) of 6 sampled tokens, and the refilled ring
+  6  Encoder group at 2 tokens per entry (Full + 5 Reuse), 8 x 1M tokens:
+     pool and top-512 of 2 sequences and the attention of all six layers
 
 Selections: equal up to ties within 1e-5 relative of the oracle's k-th score.
 Attention: within 2e-3 + 2^-8 (1 + 2e-3) ~ 5.9e-3 max-relative per head row (bf16
@@ -137,5 +139,15 @@ def test_workload5_prefill_b1_n128k_c4096():
     lo = S.N - 128
     want = oracle.fp8_quant(synth.bf16_to_f32(synth.latent(S.wl.seed, 0, lo, 128, tensor=synth.SWA)))
     assert np.array_equal(ring[np.arange(lo, S.N) % 128], want)
+    del S, R
+    torch.cuda.empty_cache()
+
+
+def test_workload6_encoder_m2_b8_n1m():
+    S, R = _run(6)
+    for b in (0, S.B - 1):
+        tk = _check_full(S, R, b, 0)
+        for li in range(len(S.layers)):
+            _check_attn(S, R, b, 0, li, tk)
     del S, R
     torch.cuda.empty_cache()
