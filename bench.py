@@ -389,27 +389,48 @@ def run_e2e(args, wl, S, R, dev):
         if L.q_idx is not None:
             host[f"qi{li}"] = L.q_idx
             host[f"w{li}"] = L.w
-    host = {k: v.cpu().pin_memory() for k, v in host.items()}
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in R.out]
-    lses_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in R.lse]
+    # All of a step's inputs travel in one pinned buffer and one copy, all of
+    # its outputs (every layer's out and lse) in one copy back.
+    def pack(tensors):
+        offs, total = {}, 0
+        for k, t in tensors.items():
+            offs[k] = total
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, total
+
+    def view(buf, off, like):
+        n = like.numel() * like.element_size()
+        return buf[off:off + n].view(like.dtype).view(like.shape)
+
+    in_offs, in_bytes = pack(host)
+    host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    for k, t in host.items():
+        view(host_in, in_offs[k], t).copy_(t.cpu())
+    dev_in_buf = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+    dev_in = {k: view(dev_in_buf, in_offs[k], t) for k, t in host.items()}
+    outs_like = {f"o{li}": o for li, o in enumerate(R.out)}
+    outs_like.update({f"l{li}": x for li, x in enumerate(R.lse)})
+    out_offs, out_bytes = pack(outs_like)
+    dev_out_buf = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+    host_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+    outs_d = [view(dev_out_buf, out_offs[f"o{li}"], o) for li, o in enumerate(R.out)]
+    lses_d = [view(dev_out_buf, out_offs[f"l{li}"], x) for li, x in enumerate(R.lse)]
     mode = {"full": csa2.MODE_FULL, "reindex": csa2.MODE_REINDEX, "reuse": csa2.MODE_REUSE}
     args_list = []
     for li, L in enumerate(S.layers):
         args_list.append(csa2.layer_args(
             mode[L.kind], B=wl.B, n_q=wl.n_q, max_ctx=wl.N, seq_len=S.seq_len, block_table=c.block_table,
             n_pages=c.n_pages, main_pages=c.main_pages, idx_pages=c.idx_pages, rings=c.rings,
-            ring_idx=L.ring_idx, q=dev_in[f"q{li}"], out=R.out[li], ws=R.ws, lse=R.lse[li],
+            ring_idx=L.ring_idx, q=dev_in[f"q{li}"], out=outs_d[li], ws=R.ws, lse=lses_d[li],
             q_idx_codes=L.q_codes, q_idx_scales=L.q_scales, w=dev_in.get(f"w{li}"),
             pool=R.pool if L.kind == "full" else L.pool if L.kind == "reindex" else None,
             topk=R.topk if L.kind != "reuse" or li == 0 else None,
             swa_chunk=R.chunk[li] if wl.prefill else None, m=wl.m))
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(o.numel() * o.element_size() for o in outs_h) + sum(x.numel() * 4 for x in lses_h)
+    d2h = sum(o.numel() * o.element_size() for o in R.out) + sum(x.numel() * 4 for x in R.lse)
 
     def step():
-        for k, v in host.items():
-            dev_in[k].copy_(v, non_blocking=True)
+        dev_in_buf.copy_(host_in, non_blocking=True)
         H.append_main(S, dev_in["latent"], dev_in["key"], dev_in.get("kv_gate"), dev_in.get("idx_gate"))
         for li, L in enumerate(S.layers):
             if wl.prefill:
@@ -422,9 +443,7 @@ def run_e2e(args, wl, S, R, dev):
         if wl.prefill:
             for li, L in enumerate(S.layers):
                 csa2.csa2_ring_refill(R.chunk[li], S.seq_len, L.ring_idx, c.rings)
-        for li in range(len(S.layers)):
-            outs_h[li].copy_(R.out[li], non_blocking=True)
-            lses_h[li].copy_(R.lse[li], non_blocking=True)
+        host_out.copy_(dev_out_buf, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
         step()

@@ -71,7 +71,7 @@ struct AttnParams {
   // [B][n_q][512]; the rings then hold the positions before them. NULL:
   // decode, every window entry comes from the ring.
   const uint8_t* swa_chunk;
-  int m;              // tokens per entry: top-k entries of token t are < (t + 1) / m
+  int m_shift;        // log2 of the tokens per entry: top-k entries of token t are < (t + 1) >> m_shift
   float scale_log2;   // softmax_scale * log2(e)
   int nsplit;         // CTAs per query (1..5)
   int out_dtype;
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
       if (c < 4) {
         const int32_t p = P.topk[static_cast<int64_t>(q) * 512 + c * 128 + gt];
         if (p >= 0) {
-          if (p > (t + 1) / P.m - 1 || (p >> 7) >= P.max_pages) {
+          if (p > ((t + 1) >> P.m_shift) - 1 || (p >> 7) >= P.max_pages) {
             report(CSA2_ERR_DEVICE_BOUNDS, 401);
           } else {
             const int32_t page = P.block_table[static_cast<int64_t>(b) * P.max_pages + (p >> 7)];
@@ -631,7 +631,7 @@ cudaError_t launch_sparse_attn(const void* q, const int32_t* topk, const int64_t
   p.ring_idx = ring_idx;
   p.n_rings = n_rings;
   p.swa_chunk = swa_chunk;
-  p.m = m;
+  p.m_shift = m == 2 ? 1 : 0;
   p.scale_log2 = softmax_scale * kLog2e;
   // Split a query's chunks over several CTAs only while that is what fills the GPU.
   p.nsplit = Q >= kNoSplitQueries

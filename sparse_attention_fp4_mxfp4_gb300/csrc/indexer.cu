@@ -53,7 +53,7 @@ struct ScanParams {
   const float* w;
   const int64_t* seq_len;
   int B, n_q;
-  int m;         // tokens per entry (1 decoder, 2 encoder): token t sees entries < (t + 1) / m
+  int m_shift;   // log2 of the tokens per entry (0 decoder, 1 encoder): token t sees entries < (t + 1) >> m_shift
   int n_grp;     // scan: query groups per sequence
   int grp_size;  // scan: tokens per group (the last group may hold fewer)
   const int32_t* block_table;
@@ -165,14 +165,14 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
   } else {
     b = blockIdx.y / P.n_grp;
     // The group's last token and the last entry it sees.
-    const int64_t e_last = (P.seq_len[b] - P.n_q + j0 + n_q) / P.m - 1;
+    const int64_t e_last = ((P.seq_len[b] - P.n_q + j0 + n_q) >> P.m_shift) - 1;
     const int64_t pages = e_last >= 0 ? (e_last + 128) >> 7 : 0;
     first_tile = blockIdx.x;
     tile_stride = gridDim.x;
     n_tiles = pages > first_tile ? (pages - first_tile + tile_stride - 1) / tile_stride : 0;
   }
   const int64_t seq_n = P.seq_len[b];
-  if (!kPool && (seq_n / P.m + 7) / 8 > P.max_blocks) {
+  if (!kPool && ((seq_n >> P.m_shift) + 7) / 8 > P.max_blocks) {
     if (threadIdx.x == 0) report(CSA2_ERR_DEVICE_BOUNDS, 204);
     n_tiles = 0;
   }
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
       // Resolve every pool slot of this CTA's tiles up front (all lookups of a
       // thread in flight together), so the producer issues copies without
       // waiting on global memory.
-      const int64_t t_q = (seq_n - P.n_q + jq + 1) / P.m - 1;  // the token's last visible entry
+      const int64_t t_q = ((seq_n - P.n_q + jq + 1) >> P.m_shift) - 1;  // the token's last visible entry
       const int32_t* prow = P.pool + (static_cast<int64_t>(b) * P.n_q + jq) * 2048 + first_tile * 16;
       for (int e = tid; e < n_tiles * 16; e += 128) {
         const int32_t blk = prow[e];
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
         }
         const float s = (a01.x + a01.y) + (a23.x + a23.y);
         if (!kPool) {
-          const int64_t t_q = (seq_n - P.n_q + j0 + jj + 1) / P.m - 1;  // the token's last visible entry
+          const int64_t t_q = ((seq_n - P.n_q + j0 + jj + 1) >> P.m_shift) - 1;  // the token's last visible entry
           const int64_t p = tile * 128 + row;
           float m = (row_ok && p <= t_q) ? s : -INFINITY;
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
@@ -509,7 +509,7 @@ cudaError_t launch_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales,
   p.idx_pages = idx_pages;
   p.block_max = block_max;
   p.max_blocks = max_blocks;
-  p.m = m;
+  p.m_shift = m == 2 ? 1 : 0;
   // Decode: all tokens of a sequence in one group. A prefill chunk: groups of
   // 7 tokens, each CTA with 16 epilogue warps.
   const bool wide = n_q > kGroup;
@@ -546,7 +546,7 @@ cudaError_t launch_pool_scores(const uint8_t* q_codes, const uint8_t* q_scales, 
   p.scores = scores;
   p.n_grp = 1;
   p.grp_size = 1;
-  p.m = m;
+  p.m_shift = m == 2 ? 1 : 0;
   // The 128 tiles of a token are cut into equal runs so that all CTAs are
   // resident at once (one wave) where the batch allows it; a run's slot table
   // is sized to the run, so short runs leave room for more CTAs per SM.

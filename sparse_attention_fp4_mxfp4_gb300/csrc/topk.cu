@@ -71,7 +71,7 @@ __device__ __forceinline__ void warp_hist_add(uint32_t* hist, bool take, uint32_
 __global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __restrict__ keys,
                                                               int64_t row_stride,
                                                               const int64_t* __restrict__ seq_len,
-                                                              int n_q, int k, int ratio,
+                                                              int n_q, int k, int m_shift,
                                                               int32_t* __restrict__ out) {
   griddep_wait();
   griddep_launch();
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) radix_topk_kernel(const float* __res
   const int tid = threadIdx.x;
   const float* row = keys + static_cast<int64_t>(q) * row_stride;
   int32_t* orow = out + static_cast<int64_t>(q) * k;
-  const int64_t t = (seq_len[b] - n_q + j + 1) / ratio - 1;  // the token's last visible entry
+  const int64_t t = ((seq_len[b] - n_q + j + 1) >> m_shift) - 1;  // the token's last visible entry
   int64_t n = t >= 0 ? (t + 8) / 8 : 0;
   if (n > row_stride) {
     if (tid == 0) report(CSA2_ERR_DEVICE_BOUNDS, 301);
@@ -352,7 +352,7 @@ __device__ __forceinline__ uint32_t warp_sort_asc(uint32_t v, int lane) {
 __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* __restrict__ keys,
                                                                 int64_t row_stride,
                                                                 const int64_t* __restrict__ seq_len,
-                                                                int n_q, int k, int C, int ratio,
+                                                                int n_q, int k, int C, int m_shift,
                                                                 int32_t* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t cs_raw[];
   ClusterShared& cs = *reinterpret_cast<ClusterShared*>(cs_raw);
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
   const int q = blockIdx.y;
   const int b = q / n_q, j = q % n_q;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t t = (seq_len[b] - n_q + j + 1) / ratio - 1;  // the token's last visible entry
+  const int64_t t = ((seq_len[b] - n_q + j + 1) >> m_shift) - 1;  // the token's last visible entry
   int64_t n64 = t >= 0 ? (t + 8) / 8 : 0;
   if (n64 > row_stride || n64 > static_cast<int64_t>(C) * kChunk) {
     if (tid == 0 && r == 0) report(CSA2_ERR_DEVICE_BOUNDS, 311);
@@ -720,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
 constexpr size_t kClusterSmem = sizeof(ClusterShared);
 
 cudaError_t launch_cluster_topk(const float* keys, int64_t row_stride, const int64_t* seq_len, int Q,
-                                int n_q, int k, int C, int ratio, int32_t* out, cudaStream_t stream) {
+                                int n_q, int k, int C, int m_shift, int32_t* out, cudaStream_t stream) {
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -733,7 +733,7 @@ cudaError_t launch_cluster_topk(const float* keys, int64_t row_stride, const int
     if (dev < 64) configured[dev] = true;
   }
   return launch_pdl(cluster_topk_kernel, dim3(C, Q, 1), dim3(kThreads), kClusterSmem, stream,
-                    static_cast<unsigned>(C), keys, row_stride, seq_len, n_q, k, C, ratio, out);
+                    static_cast<unsigned>(C), keys, row_stride, seq_len, n_q, k, C, m_shift, out);
 }
 
 // ---- pool top-k: one CTA per token, the row in registers --------------------
@@ -950,12 +950,12 @@ cudaError_t launch_block_topk(const float* block_max, const int64_t* seq_len, in
   if (C > 16 || static_cast<int64_t>(Q) * C > 64) C = (max_blocks + kChunk - 1) / kChunk;
   if (C <= 16) {
     const cudaError_t e = launch_cluster_topk(block_max, max_blocks, seq_len, Q, n_q, 2048,
-                                              static_cast<int>(C < 1 ? 1 : C), m, pool, stream);
+                                              static_cast<int>(C < 1 ? 1 : C), m == 2 ? 1 : 0, pool, stream);
     if (e == cudaSuccess || C <= 8) return e;
     cudaGetLastError();  // a 16-CTA cluster may not fit this GPU: use the global-memory select
   }
   return launch_pdl(radix_topk_kernel, dim3(Q), dim3(kThreads), 0, stream, 0, block_max, max_blocks, seq_len, n_q,
-                    2048, m, pool);
+                    2048, m == 2 ? 1 : 0, pool);
 }
 
 cudaError_t launch_pool_topk(const float* scores, const int64_t* seq_len, int B, int n_q,
