@@ -406,31 +406,40 @@ def run_e2e(args, wl, S, R, dev):
     host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
     for k, t in host.items():
         view(host_in, in_offs[k], t).copy_(t.cpu())
-    dev_in_buf = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-    dev_in = {k: view(dev_in_buf, in_offs[k], t) for k, t in host.items()}
     outs_like = {f"o{li}": o for li, o in enumerate(R.out)}
     outs_like.update({f"l{li}": x for li, x in enumerate(R.lse)})
     out_offs, out_bytes = pack(outs_like)
-    dev_out_buf = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
-    host_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
-    outs_d = [view(dev_out_buf, out_offs[f"o{li}"], o) for li, o in enumerate(R.out)]
-    lses_d = [view(dev_out_buf, out_offs[f"l{li}"], x) for li, x in enumerate(R.lse)]
     mode = {"full": csa2.MODE_FULL, "reindex": csa2.MODE_REINDEX, "reuse": csa2.MODE_REUSE}
-    args_list = []
-    for li, L in enumerate(S.layers):
-        args_list.append(csa2.layer_args(
-            mode[L.kind], B=wl.B, n_q=wl.n_q, max_ctx=wl.N, seq_len=S.seq_len, block_table=c.block_table,
-            n_pages=c.n_pages, main_pages=c.main_pages, idx_pages=c.idx_pages, rings=c.rings,
-            ring_idx=L.ring_idx, q=dev_in[f"q{li}"], out=outs_d[li], ws=R.ws, lse=lses_d[li],
-            q_idx_codes=L.q_codes, q_idx_scales=L.q_scales, w=dev_in.get(f"w{li}"),
-            pool=R.pool if L.kind == "full" else L.pool if L.kind == "reindex" else None,
-            topk=R.topk if L.kind != "reuse" or li == 0 else None,
-            swa_chunk=R.chunk[li] if wl.prefill else None, m=wl.m))
+
+    # Two sets of staging buffers: step k reads set k % 2 while the inputs of
+    # step k + 1 arrive in the other set and the outputs of step k - 1 leave.
+    sets = []
+    for _ in range(2):
+        din = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+        dout = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+        hout = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+        dev_in = {k: view(din, in_offs[k], t) for k, t in host.items()}
+        outs_d = [view(dout, out_offs[f"o{li}"], o) for li, o in enumerate(R.out)]
+        lses_d = [view(dout, out_offs[f"l{li}"], x) for li, x in enumerate(R.lse)]
+        args_list = []
+        for li, L in enumerate(S.layers):
+            args_list.append(csa2.layer_args(
+                mode[L.kind], B=wl.B, n_q=wl.n_q, max_ctx=wl.N, seq_len=S.seq_len, block_table=c.block_table,
+                n_pages=c.n_pages, main_pages=c.main_pages, idx_pages=c.idx_pages, rings=c.rings,
+                ring_idx=L.ring_idx, q=dev_in[f"q{li}"], out=outs_d[li], ws=R.ws, lse=lses_d[li],
+                q_idx_codes=L.q_codes, q_idx_scales=L.q_scales, w=dev_in.get(f"w{li}"),
+                pool=R.pool if L.kind == "full" else L.pool if L.kind == "reindex" else None,
+                topk=R.topk if L.kind != "reuse" or li == 0 else None,
+                swa_chunk=R.chunk[li] if wl.prefill else None, m=wl.m))
+        ev = {k: torch.cuda.Event() for k in ("in_ready", "computed", "out_sent")}
+        sets.append(dict(din=din, dout=dout, hout=hout, dev_in=dev_in, args=args_list, ev=ev, used=False))
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(o.numel() * o.element_size() for o in R.out) + sum(x.numel() * 4 for x in R.lse)
+    main = torch.cuda.current_stream()
+    s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def step():
-        dev_in_buf.copy_(host_in, non_blocking=True)
+    def compute(st):
+        dev_in = st["dev_in"]
         H.append_main(S, dev_in["latent"], dev_in["key"], dev_in.get("kv_gate"), dev_in.get("idx_gate"))
         for li, L in enumerate(S.layers):
             if wl.prefill:
@@ -439,27 +448,67 @@ def run_e2e(args, wl, S, R, dev):
                 csa2.csa2_append_swa(dev_in[f"swa{li}"], S.step_ring_idx[li], S.step_pos, c.rings)
             if L.q_idx is not None:
                 csa2.csa2_quant_mxfp4(dev_in[f"qi{li}"], L.q_codes, L.q_scales)
-        csa2.csa2_decode_group(args_list)
+        csa2.csa2_decode_group(st["args"])
         if wl.prefill:
             for li, L in enumerate(S.layers):
                 csa2.csa2_ring_refill(R.chunk[li], S.seq_len, L.ring_idx, c.rings)
-        host_out.copy_(dev_out_buf, non_blocking=True)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
+    def step_serial(k):
+        """Copy in, compute, copy out, one after another on one stream."""
+        st = sets[0]
+        st["din"].copy_(host_in, non_blocking=True)
+        compute(st)
+        st["hout"].copy_(st["dout"], non_blocking=True)
+
+    def step_pipelined(k):
+        """Step k on staging set k % 2: its input copy waits until the step
+        that last read the set has computed, its compute waits for its input
+        and for the set's previous outputs to have left, its output copy waits
+        for its compute."""
+        st = sets[k % 2]
+        ev = st["ev"]
+        with torch.cuda.stream(s_h2d):
+            if st["used"]:
+                s_h2d.wait_event(ev["computed"])
+            st["din"].copy_(host_in, non_blocking=True)
+            ev["in_ready"].record(s_h2d)
+        main.wait_event(ev["in_ready"])
+        if st["used"]:
+            main.wait_event(ev["out_sent"])
+        compute(st)
+        ev["computed"].record(main)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev["computed"])
+            st["hout"].copy_(st["dout"], non_blocking=True)
+            ev["out_sent"].record(s_d2h)
+        st["used"] = True
+
     steps = max(1, min(args.steps, 500))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+
+    def timed(run):
+        for k in range(max(3, args.warmup)):
+            run(k)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        for k in range(steps):
+            run(k)
+        main.wait_stream(s_d2h)  # the last step's outputs are on the host
+        e1.record(main)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms_serial = timed(step_serial)
+    ms = timed(step_pipelined)
+    st = csa2.csa2_check_device_status()
+    if st != csa2.OK:
+        raise RuntimeError("device status after the end-to-end steps: " + csa2.device_status_message())
     return {"value": wl.B * wl.n_q / (ms * 1e-3), "unit": "tokens/s" if wl.prefill else "queries/s",
             "ms_per_step": ms, "steps": steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "launch": "calls launched per step; copies of steps k-1 and k+1 overlap the compute of step k "
+                      "(two staging sets, copy streams)",
+            "ms_per_step_serial": ms_serial, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
 # ---- the CPU oracle (baseline and reference arm) ------------------------------------------------
