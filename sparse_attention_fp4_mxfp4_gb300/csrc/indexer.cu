@@ -178,6 +178,17 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
   }
 
 
+  // The scan's producer needs neither the query nor TMEM: once the mbarriers
+  // are visible it starts streaming pages, while the other warps set the
+  // query up among themselves (named barrier 1). The pool rescore's producer
+  // needs the slot table, so there the whole CTA waits for the setup.
+  const bool early_producer = !kPool && warp == kEpi;
+  if (!kPool) __syncthreads();
+  auto setup_sync = [&]() {
+    if (kPool) __syncthreads();
+    else named_bar_sync(1, 32 * (kEpi + 1));
+  };
+
   // Query operand: packed E2M1 codes of the CTA's query tokens, rows
   // n = token * 32 + head, in core-matrix order [n / 8][chunk][n % 8][16 B].
   if (tid < 128) {
@@ -219,10 +230,13 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
     }
     fence_proxy_async();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  uint32_t tmem = 0;
+  if (!early_producer) {
+    tc_fence_before();
+    setup_sync();
+    tc_fence_after();
+    tmem = *tmem_slot;
+  }
 
   // Query scales: column n of B has its scales in lane n % 32 of column
   // sfb + 8 * step + n / 32, replicated in all four 32-lane quarters (each
@@ -242,9 +256,11 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
     }
     tmem_wait_st();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  if (!early_producer) {
+    tc_fence_before();
+    setup_sync();
+    tc_fence_after();
+  }
 
   if (warp == kEpi) {
     // ---- producer (whole warp: lookups in parallel, one bulk copy per lane) ----
