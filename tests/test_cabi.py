@@ -107,3 +107,26 @@ def test_status_strings_and_null_checks(lib):
     lib.csa2_quant_mxfp4.argtypes = [p, ctypes.c_int64, p, p, p]
     assert lib.csa2_quant_mxfp4(p(16), 17, p(16), p(16), None) == 1
     assert lib.csa2_decode_group(None, 1, None) == 1
+
+
+def test_tokens_per_entry_and_compressor_host_checks(lib):
+    p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.csa2_last_error.restype = ctypes.c_char_p
+    x = p(4096)  # an aligned non-null address; no call below reaches the device
+    lib.csa2_compress_append.argtypes = [p, p, p, p, p, p, i32, i32, p, p, i32, i32, i64, p, p, p]
+    assert lib.csa2_compress_append(None, None, None, None, None, None, 0, 2, None, None, 1, 1, 1, None, None,
+                                    None) == 0  # nothing to do
+    assert lib.csa2_compress_append(x, x, x, x, x, x, 4, 3, x, x, 1, 1, 1, x, x, None) == 2  # m = 3
+    assert b"m = 3" in lib.csa2_last_error()
+    assert lib.csa2_compress_append(x, x, x, x, x, x, 4, 2, None, x, 1, 1, 1, x, x, None) == 1
+    assert b"tail" in lib.csa2_last_error()
+    # m = 1 needs no tail
+    assert lib.csa2_compress_append(x, x, x, x, x, x, 4, 1, None, None, 1, 1, 1, x, x, None) == 1
+    assert b"block_table" in lib.csa2_last_error()
+    lib.csa2_indexer_scan.argtypes = [p, p, p, p, i32, i32, i64, p, i32, i64, p, p, i64, i32, p]
+    assert lib.csa2_indexer_scan(x, x, x, x, 1, 1, 100, x, 1, 1, x, x, 13, 4, None) == 2  # m = 4
+    # at m = 2 the block maxima cover ceil(max_ctx / 2 / 8) blocks
+    assert lib.csa2_indexer_scan(x, x, x, x, 1, 1, 1600, x, 1, 1, x, x, 99, 2, None) == 1
+    assert b"max_blocks" in lib.csa2_last_error()
+    lib.csa2_block_topk.argtypes = [p, p, i32, i32, i64, p, i32, p]
+    assert lib.csa2_block_topk(x, x, 1, 1, 10, x, 0, None) == 2
