@@ -299,8 +299,10 @@ struct ClusterShared {
   uint32_t cand[kBlkCandMax];   // CTA 0: the candidates of the whole row
   uint32_t wred[4][32];         // per warp: min, max, valid count, sample statistic
   uint32_t woff[32];            // per warp: offset of its candidates within the CTA
-  uint32_t cgt[kSlots][32];     // per (slot, warp): keys above T, then their prefix
-  uint32_t ceq[kSlots][32];     // per (slot, warp): keys equal to T, then their prefix
+  // Rows padded to 33 words: warp 0's prefix pass reads 16 consecutive entries
+  // per lane, which with 32-word rows would put every second lane in one bank.
+  uint32_t cgt[kSlots][33];     // per (slot, warp): keys above T, then their prefix
+  uint32_t ceq[kSlots][33];     // per (slot, warp): keys equal to T, then their prefix
   uint32_t warp_sums[32];
   uint32_t xchg[16];            // read by other CTAs: 0-3 min/max/valid/sample median,
                                 // 4 candidate count, 5 slice total, 6-7 gt/eq counts,
