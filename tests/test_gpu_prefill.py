@@ -194,3 +194,29 @@ def test_ring_refill_equals_the_appended_history():
     torch.cuda.synchronize()
     _status_ok()
     assert torch.equal(inc, reb)
+
+
+@pytest.mark.parametrize("N,n_q,B", [(20000, 100, 1), (3000, 140, 2)])
+def test_prefill_reindex_layer(N, n_q, B):
+    """A Reindex layer over a prefill chunk: every token rescores its own pool
+    (2048 blocks, fewer near the start) and attends with its exact window."""
+    wl = Workload(101, "t", "reindex", B=B, N=N, n_q=n_q, layers=("reindex",))
+    S = H.build(wl, DEV, shuffle_seed=41)
+    R = H.Runner(S, out_dtype=torch.float32, prefill=True)
+    R.step()
+    torch.cuda.synchronize()
+    gt = R.topk.cpu().numpy()
+    go, gl = R.out[0].cpu().numpy(), R.lse[0].cpu().numpy()
+    pools = S.layers[0].pool.cpu().numpy()
+    _status_ok()
+    for b in range(B):
+        keys = H.oracle_keys(S, b, N - 1)
+        for j in _tokens(n_q):
+            ref = H.oracle_reindex(S, b, j, 0, pools[b, j], keys=keys)
+            ps = ref["pos_scores"]
+            slot = {int(pools[b, j][i // 8]) * 8 + i % 8: ps[i] for i in range(ps.size) if pools[b, j][i // 8] >= 0}
+            H.check_selection(gt[b, j], ref["topk"], lambda p: slot[p], 512, f"reindex topk {j}")
+            ro, rl = H.oracle_attention(S, b, j, 0, gt[b, j], exact_window=True)
+            H.check_attention(go[b, j], ro, H.TOL_ATTN_F32)
+            np.testing.assert_allclose(gl[b, j], rl, rtol=1e-5, atol=H.TOL_LSE)
+        _check_ring_refilled(S, 0, b)
