@@ -178,16 +178,37 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
   }
 
 
-  // The scan's producer needs neither the query nor TMEM: once the mbarriers
-  // are visible it starts streaming pages, while the other warps set the
-  // query up among themselves (named barrier 1). The pool rescore's producer
-  // needs the slot table, so there the whole CTA waits for the setup.
-  const bool early_producer = !kPool && warp == kEpi;
-  if (!kPool) __syncthreads();
-  auto setup_sync = [&]() {
-    if (kPool) __syncthreads();
-    else named_bar_sync(1, 32 * (kEpi + 1));
+  // Pool rescore: the source (page * 16 + block in page, or kNoSlot) and the
+  // causal positions of pool slot e of this CTA's tiles.
+  auto resolve_slot = [&](int e) {
+    const int64_t t_q = ((seq_n - P.n_q + jq + 1) >> P.m_shift) - 1;  // the token's last visible entry
+    const int32_t blk = P.pool[(static_cast<int64_t>(b) * P.n_q + jq) * 2048 + first_tile * 16 + e];
+    uint32_t src = kNoSlot;
+    int nv = 0;
+    if (blk >= 0 && static_cast<int64_t>(blk) * 8 <= t_q) {
+      const int64_t lp = static_cast<int64_t>(blk) >> 4;
+      const int32_t page = lp < P.max_pages ? P.block_table[static_cast<int64_t>(b) * P.max_pages + lp] : -1;
+      if (page < 0 || page >= P.n_pages) {
+        report(CSA2_ERR_DEVICE_BOUNDS, 203);
+      } else {
+        src = static_cast<uint32_t>(page) * 16u + static_cast<uint32_t>(blk & 15);
+        const int64_t left = t_q - static_cast<int64_t>(blk) * 8 + 1;
+        nv = left < 8 ? static_cast<int>(left) : 8;
+      }
+    }
+    slot_src[e] = src;
+    slot_n[e] = static_cast<uint8_t>(nv);
   };
+  // The pool producer resolves the first two tiles' slots itself and starts;
+  // warps 0-3 resolve the rest and meet it at named barrier 2 before tile 2.
+  const bool pool_split = kPool && n_tiles > 2;
+
+  // The producer needs neither the query nor TMEM: once the mbarriers are
+  // visible it starts, while the other warps set the query up among
+  // themselves (named barrier 1).
+  const bool early_producer = warp == kEpi;
+  __syncthreads();
+  auto setup_sync = [&]() { named_bar_sync(1, 32 * (kEpi + 1)); };
 
   // Query operand: packed E2M1 codes of the CTA's query tokens, rows
   // n = token * 32 + head, in core-matrix order [n / 8][chunk][n % 8][16 B].
@@ -204,29 +225,8 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
       wsm[i] = P.w[(static_cast<int64_t>(b) * P.n_q + jj) * 32 + (i & 31)];
     }
     if (kPool) {
-      // Resolve every pool slot of this CTA's tiles up front (all lookups of a
-      // thread in flight together), so the producer issues copies without
-      // waiting on global memory.
-      const int64_t t_q = ((seq_n - P.n_q + jq + 1) >> P.m_shift) - 1;  // the token's last visible entry
-      const int32_t* prow = P.pool + (static_cast<int64_t>(b) * P.n_q + jq) * 2048 + first_tile * 16;
-      for (int e = tid; e < n_tiles * 16; e += 128) {
-        const int32_t blk = prow[e];
-        uint32_t src = kNoSlot;
-        int nv = 0;
-        if (blk >= 0 && static_cast<int64_t>(blk) * 8 <= t_q) {
-          const int64_t lp = static_cast<int64_t>(blk) >> 4;
-          const int32_t page = lp < P.max_pages ? P.block_table[static_cast<int64_t>(b) * P.max_pages + lp] : -1;
-          if (page < 0 || page >= P.n_pages) {
-            report(CSA2_ERR_DEVICE_BOUNDS, 203);
-          } else {
-            src = static_cast<uint32_t>(page) * 16u + static_cast<uint32_t>(blk & 15);
-            const int64_t left = t_q - static_cast<int64_t>(blk) * 8 + 1;
-            nv = left < 8 ? static_cast<int>(left) : 8;
-          }
-        }
-        slot_src[e] = src;
-        slot_n[e] = static_cast<uint8_t>(nv);
-      }
+      for (int e = 32 + tid; e < n_tiles * 16; e += 128) resolve_slot(e);
+      if (pool_split) named_bar_sync(2, 160);
     }
     fence_proxy_async();
   }
@@ -264,7 +264,14 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
 
   if (warp == kEpi) {
     // ---- producer (whole warp: lookups in parallel, one bulk copy per lane) ----
+    if (kPool) {
+      // The first two tiles' slots (one per lane); the consumers read the
+      // table after the stage barriers, which this warp arrives on afterwards.
+      if (lane < n_tiles * 16) resolve_slot(lane);
+      __syncwarp();
+    }
     int32_t next_pages = -1;  // scan: page id of tile (i & ~31) + lane
+    bool met = false;         // pool: named barrier 2 passed
     const int nt = static_cast<int>(n_tiles);
     int s = 0, u = 0;  // stage of tile i and the round of the ring it is in (i = u * kStages + s)
     for (int i = 0; i < nt; ++i, s = (s + 1 == kStages) ? 0 : s + 1, u += (s == 0) ? 1 : 0) {
@@ -275,6 +282,10 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
       }
       if (!__shfl_sync(0xffffffffu, go, 0)) break;
       const uint32_t dst = smem_u32(stages + s * kTileBytes);
+      if (pool_split && i == 2) {  // the other slots are resolved
+        named_bar_sync(2, 160);
+        met = true;
+      }
       if (!kPool) {
         if ((i & 31) == 0) {  // page ids of the next 32 tiles, one per lane
           const int64_t tl = first_tile + (i + lane) * tile_stride;
@@ -309,6 +320,7 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
                    576, full0 + 8 * s);
       }
     }
+    if (pool_split && !met) named_bar_sync(2, 160);  // stopped early: still meet warps 0-3
   } else if (warp == kEpi + 1) {
     // ---- MMA issuer ----
     if (lane == 0) {
