@@ -14,9 +14,9 @@
 // One kernel serves both uses:
 //   * Full scan: a tile is one 128-entry page; the epilogue reduces scores to
 //     the maximum over 8-position blocks. The query tokens of a sequence are
-//     cut into groups (one group of up to 8 at decode; groups of 7 in a
-//     prefill chunk); a group's tokens share the tile: N = 32 * tokens MMA
-//     columns. A group walks the pages up to its last token's position, and
+//     cut into groups (one group of one or two tokens; groups of 7 from three
+//     tokens on, draft tokens or a prefill chunk); a group's tokens share the
+//     tile: N = 32 * tokens MMA columns. A group walks the pages up to its last token's position, and
 //     CTAs of different groups that read the same pages run side by side, so
 //     the repeated reads of a prefill chunk come from L2.
 //   * Pool rescore (Reindex, and the end of Full): a tile is 16 pool blocks of
@@ -26,9 +26,9 @@
 // copies; warps 0-3 move each row's 8 scale bytes into TMEM; warps 0..E-1 run
 // the epilogue (warp w reads TMEM lane quarter w % 4, i.e. rows 32 (w % 4) ..
 // +31, for the tokens j = w / 4 (mod E / 4)); warp E + 1 issues the two
-// K = 64 MMAs of a tile (M = 128 positions) straight from the stage. E = 4 at
-// decode and in the pool rescore; E = 16 for a prefill chunk, whose 7 tokens
-// per tile make the epilogue's fp32 work the bound.
+// K = 64 MMAs of a tile (M = 128 positions) straight from the stage. E = 4 for
+// one or two tokens and in the pool rescore; E = 16 for groups of 7 tokens,
+// whose epilogue fp32 work is the bound.
 #include <algorithm>
 
 #include "kernels.h"
@@ -40,7 +40,7 @@ namespace {
 constexpr int kStages = 5;
 constexpr int kTileBytes = 16 * 576;     // one indexer page / 16 pool blocks
 constexpr int kIdxPageBytes = 16 * 576;
-constexpr int kGroup = 8;      // decode: query tokens per scan CTA (N <= 256 MMA columns)
+constexpr int kGroup = 8;      // one or two tokens: all in one CTA (the shared memory is sized for 8)
 constexpr int kWideGroup = 7;  // prefill: tokens per scan CTA (two N = 224 accumulators fit TMEM)
 constexpr int kWideSub = 4;    // prefill: epilogue warps per TMEM lane quarter
 
@@ -538,9 +538,11 @@ cudaError_t launch_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales,
   p.block_max = block_max;
   p.max_blocks = max_blocks;
   p.m_shift = m == 2 ? 1 : 0;
-  // Decode: all tokens of a sequence in one group. A prefill chunk: groups of
-  // 7 tokens, each CTA with 16 epilogue warps.
-  const bool wide = n_q > kGroup;
+  // One or two tokens per sequence: one group, 4 epilogue warps. Three or
+  // more (draft tokens at decode, a prefill chunk): groups of 7 tokens, each
+  // CTA with 16 epilogue warps (at 4 and 6 tokens per sequence and 256K
+  // context this halves the scan's time against one group with 4 warps).
+  const bool wide = n_q >= 3;
   p.grp_size = wide ? kWideGroup : kGroup;
   p.n_grp = (n_q + p.grp_size - 1) / p.grp_size;
   const int tile_q = std::min(n_q, p.grp_size);
