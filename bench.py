@@ -223,22 +223,33 @@ def step_bytes(wl) -> int:
 
 # ---- our arm ------------------------------------------------------------------------------------
 
-def run_ours(args, wl, rank, world, local):
-    import sparse_attention_fp4_mxfp4_gb300 as csa2
-    from tests import harness as H
+def dominant_stage(wl, kinds):
+    """The kernel whose HBM roofline the line reports: the scan when the step
+    has a Full layer, else the pool rescore of a Reindex layer, else the
+    attention; with its algorithmic bytes per launch and launches per step."""
+    q = wl.B * wl.n_q
+    if "full" in kinds:
+        return "indexer_scan", scan_bytes(wl), "scan", 1
+    if "reindex" in kinds:
+        return ("indexer_rescore", q * (2048 * 576 + 32 * 72 + 32 * 4 + 2048 * 4), "rescore",
+                kinds.count("reindex"))
+    return "sparse_attn", q * attn_bytes_per_query(), "attn", len(kinds)
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+
+def measure(args, wl, dev, world, clocks=None):
+    """Builds the workload, then times its step: the whole step as one CUDA
+    graph (the headline), the same steps launched eagerly with events around
+    every stage (per-kernel durations), and the end-to-end step through the
+    public calls with host buffers. Returns the raw measurements."""
+    import sparse_attention_fp4_mxfp4_gb300 as csa2
+    from sparse_attention_fp4_mxfp4_gb300.step import Runner
+    from sparse_attention_fp4_mxfp4_gb300.workload import build
+
     t_setup = time.time()
-    S = H.build(wl, dev)
-    R = H.Runner(S, prefill=wl.prefill)
+    S = build(wl, dev)
+    R = Runner(S, prefill=wl.prefill)
     torch.cuda.synchronize()
     setup_s = time.time() - t_setup
-    B, n_q, N = wl.B, wl.n_q, wl.N
-    Q = B * n_q
     stream = torch.cuda.current_stream()
     ev = {}
 
@@ -286,15 +297,14 @@ def run_ours(args, wl, rank, world, local):
         barrier(world)
         return e0.elapsed_time(e1) / steps
 
-    clocks = ClockSampler(local)
-    clocks.start()
+    if clocks is not None:
+        clocks.start()
     # Per-kernel durations: the same steps launched one by one with events
     # around every stage, back to back on the launching stream.
     stage_steps = args.steps if graph is None else max(3, min(args.steps, 500))
     ms_eager = timed(lambda: R.step(mark), stage_steps)
     ms = timed(graph.replay, args.steps) if graph is not None else ms_eager
-    clk = clocks.stop()
-    ms_max = max_over_ranks(ms, world, dev)
+    clk = clocks.stop() if clocks is not None else None
     stage_ms = {}
     for name in ("scan", "blocktopk", "rescore", "attn"):
         if name + "0" in ev:
@@ -303,20 +313,55 @@ def run_ours(args, wl, rank, world, local):
     st = csa2.csa2_check_device_status()
     if st != csa2.OK:
         raise RuntimeError("device status after timing: " + csa2.device_status_message())
+    e2e = None if args.no_e2e else run_e2e(args, wl, S, R, dev)
+    out = {"ms": ms, "ms_eager": ms_eager, "stage_steps": stage_steps, "stage_ms": stage_ms, "e2e": e2e,
+           "clocks": clk, "launches": R.launches, "setup_s": setup_s, "store_bytes": S.cache.nbytes(),
+           "kinds": [L.kind for L in S.layers], "graph": graph is not None}
+    del graph, R, S
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, wl, S, R, dev)
 
+# The decode modes the metric is quoted per, measured in the same run as the
+# headline (which is the Full mode at 8 x 1M).
+MODE_WORKLOADS = (1, 2, 4)
+
+
+def mode_summary(args, wl, m, peak) -> dict:
+    """One decode mode's device-timed queries/s, the HBM fraction of its
+    dominant stage and its end-to-end queries/s."""
+    kinds = m["kinds"]
+    dom, dom_bytes, dom_stage, per_step = dominant_stage(wl, kinds)
+    dms = m["stage_ms"].get(dom_stage)
+    frac = dom_bytes / (dms / per_step * 1e-3) / 1e9 / peak if dms else None
+    q = wl.B * wl.n_q
+    return {"workload": wl.name, "mode": wl.mode, "layers": kinds, "batch": wl.B, "context": wl.N,
+            "query_tokens": wl.n_q, "queries_per_step": q, "value": q / (m["ms"] * 1e-3), "unit": "queries/s",
+            "ms_per_step": m["ms"], "steps": args.steps, "warmup": args.warmup,
+            "hbm_fraction_step": (step_bytes(wl) / (m["ms"] * 1e-3) / 1e9) / peak,
+            "dominant": {"kernel": dom, "frac_of_measured_hbm": frac, "algorithmic_bytes_per_launch": dom_bytes},
+            "stage_ms": m["stage_ms"], "stage_roofline": stage_roofline(wl, kinds, m["stage_ms"], peak),
+            "e2e": None if m["e2e"] is None else {k: m["e2e"][k] for k in ("value", "unit", "ms_per_step")},
+            "clocks": m["clocks"], "gpu_launches": m["launches"] * args.steps}
+
+
+def run_ours(args, wl, rank, world, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    B, n_q, N = wl.B, wl.n_q, wl.N
+    Q = B * n_q
+    clocks = ClockSampler(local)
+    m = measure(args, wl, dev, world, clocks)
+    ms = m["ms"]
+    ms_max = max_over_ranks(ms, world, dev)
+    stage_ms = m["stage_ms"]
     peak, peak_kind = measured_peaks()
-    kinds = [L.kind for L in S.layers]
-    if "full" in kinds:
-        dom, dom_bytes, dom_stage, per_step = "indexer_scan", scan_bytes(wl), "scan", 1
-    elif "reindex" in kinds:
-        dom, dom_bytes, dom_stage, per_step = ("indexer_rescore", Q * (2048 * 576 + 32 * 72 + 32 * 4 + 2048 * 4),
-                                               "rescore", kinds.count("reindex"))
-    else:
-        dom, dom_bytes, dom_stage, per_step = "sparse_attn", Q * attn_bytes_per_query(), "attn", len(kinds)
+    kinds = m["kinds"]
+    dom, dom_bytes, dom_stage, per_step = dominant_stage(wl, kinds)
     dom_ms = stage_ms.get(dom_stage)
     launch_ms = dom_ms / per_step if dom_ms else None
     achieved = dom_bytes / (launch_ms * 1e-3) / 1e9 if launch_ms else None
@@ -356,18 +401,27 @@ def run_ours(args, wl, rank, world, local):
         "config": {"workload": wl.name, "mode": wl.mode, "layers": list(kinds), "batch": B, "context": N,
                    "query_tokens": n_q, "queries_per_step": Q, "prefill": wl.prefill, "tokens_per_entry": wl.m,
                    "l2": "inputs larger than L2 (store of %.1f GB; the step reads %.0f MB)" % (
-                       S.cache.nbytes() / 1e9, step_bytes(wl) / 1e6),
-                   "parallelism": f"replicas x{world} (independent sequences)", "setup_s": round(setup_s, 1),
-                   "launch": "CUDA graph of the whole step" if graph is not None else "eager launches",
-                   "ms_per_step_eager": ms_eager, "stage_steps": stage_steps},
+                       m["store_bytes"] / 1e9, sb / 1e6),
+                   "parallelism": f"replicas x{world} (independent sequences)", "setup_s": round(m["setup_s"], 1),
+                   "launch": "CUDA graph of the whole step" if m["graph"] else "eager launches",
+                   "ms_per_step_eager": m["ms_eager"], "stage_steps": m["stage_steps"]},
         "hbm_fraction_step": (sb / (ms_max * 1e-3) / 1e9) / peak,
         "stage_ms": stage_ms,
         "stage_roofline": stage_roofline(wl, kinds, stage_ms, peak),
         "roofline": roof,
-        "clocks": clk,
-        "gpu_launches": R.launches * args.steps,
-        "e2e": e2e,
+        "clocks": m["clocks"],
+        "gpu_launches": m["launches"] * args.steps,
+        "e2e": m["e2e"],
     }
+    # The other decode modes, same step and warm-up counts (replicas: every
+    # rank runs them; rank 0 reports its own).
+    if not args.no_modes and wl.index == 3 and not (args.B or args.N or args.nq):
+        from synth.workloads import WORKLOADS
+        modes = {}
+        for idx in MODE_WORKLOADS:
+            mwl = WORKLOADS[idx]
+            modes[mwl.mode] = mode_summary(args, mwl, measure(args, mwl, dev, world, ClockSampler(local)), peak)
+        line["modes"] = modes
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     return line
@@ -378,7 +432,7 @@ def run_e2e(args, wl, S, R, dev):
     its new entries and every layer's queries from pinned host memory, runs
     the layers with csa2_decode_group and reads every layer's output back."""
     import sparse_attention_fp4_mxfp4_gb300 as csa2
-    from tests import harness as H
+    from sparse_attention_fp4_mxfp4_gb300.workload import append_main
     c = S.cache
     host = {"latent": S.step_latent, "key": S.step_idx_key}
     if wl.m > 1:
@@ -440,7 +494,7 @@ def run_e2e(args, wl, S, R, dev):
 
     def compute(st):
         dev_in = st["dev_in"]
-        H.append_main(S, dev_in["latent"], dev_in["key"], dev_in.get("kv_gate"), dev_in.get("idx_gate"))
+        append_main(S, dev_in["latent"], dev_in["key"], dev_in.get("kv_gate"), dev_in.get("idx_gate"))
         for li, L in enumerate(S.layers):
             if wl.prefill:
                 csa2.csa2_quant_fp8_entries(dev_in[f"swa{li}"], R.chunk[li])
@@ -519,6 +573,22 @@ def run_e2e(args, wl, S, R, dev):
             st_["graph"] = g
         torch.cuda.synchronize()
         launch = "each step's calls replayed as a CUDA graph"
+    ms_calls_only = None
+    if sets[0].get("graph") is not None:
+        # The same graph of public calls without any copy: separates the
+        # copies' cost from the launch order of csa2_decode_group.
+        g = sets[0]["graph"]
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        for _ in range(steps):
+            g.replay()
+        e1.record(main)
+        torch.cuda.synchronize()
+        ms_calls_only = e0.elapsed_time(e1) / steps
     ms = timed(step_pipelined)
     st = csa2.csa2_check_device_status()
     if st != csa2.OK:
@@ -527,7 +597,8 @@ def run_e2e(args, wl, S, R, dev):
             "ms_per_step": ms, "steps": steps,
             "launch": launch + "; copies of steps k-1 and k+1 overlap the compute of step k "
                       "(two staging sets, copy streams)",
-            "ms_per_step_serial": ms_serial, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step_serial": ms_serial, "ms_per_step_calls_only": ms_calls_only,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
 # ---- the CPU oracle (baseline and reference arm) ------------------------------------------------
@@ -538,7 +609,7 @@ def oracle_query(wl, b=0, j=0, n_scan=None):
     sample (positions 0..n_scan-1); its time is scaled to the full context."""
     import oracle
     import synth
-    from tests.harness import n_blocks
+    from sparse_attention_fp4_mxfp4_gb300.workload import n_blocks
     seed, N, n_q = wl.seed, wl.N, wl.n_q
     t = N - n_q + j
     li = 0
@@ -661,6 +732,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-modes", action="store_true", help="skip the Reuse / Reindex / group modes of the default line")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--B", type=int, default=None, help="override the batch (profiling captures only)")
     ap.add_argument("--N", type=int, default=None, help="override the context (profiling captures only)")
