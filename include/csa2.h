@@ -90,6 +90,7 @@ extern "C" {
 #define CSA2_ERR_CUDA 4            /* a CUDA runtime call or launch failed */
 #define CSA2_ERR_DEVICE_TIMEOUT 5  /* a bounded wait inside a kernel gave up */
 #define CSA2_ERR_DEVICE_BOUNDS 6   /* a device-side index check failed */
+#define CSA2_ERR_DEVICE_RANGE 7    /* an input value outside the supported range (read on the device) */
 
 /* ---- fixed geometry of the decoder CSA2 layer ([RN] 1, [AB] 3.1) ----------- */
 #define CSA2_LATENT_DIM 512    /* main KV latent channels (K = V) */
@@ -250,17 +251,23 @@ int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const 
                          const int32_t* pool, int32_t* topk, void* ws, size_t ws_bytes, int m,
                          void* stream);
 
-/* Same computation and outputs as csa2_indexer_reindex, for callers that cannot
- * allocate device memory (inside CUDA-graph capture, under a host framework
- * that owns every allocation, or on a decode path where allocating could
- * synchronise or fail): the per-slot scores live in a fixed 4 MiB device
- * array inside the library instead of a caller workspace. The pages have no
- * counterpart of this entry point; it only changes where scratch lives.
+/* Same computation and outputs as csa2_indexer_reindex (same arguments,
+ * including the ratio m, and the same host checks and status codes), for
+ * callers that cannot allocate device memory: plug-ins whose host framework
+ * owns every device allocation, and decode loops that must not allocate
+ * because an allocation there can synchronise the device or fail under
+ * memory pressure in the middle of a step. The per-slot scores live in a
+ * fixed 4 MiB device array inside the library instead of a caller workspace.
+ * The pages have no counterpart of this entry point; it only changes where
+ * scratch lives.
  *   - At most 64 query tokens per call (B * n_q <= 64); larger calls return
- *     CSA2_ERR_UNSUPPORTED and allocate nothing.
+ *     CSA2_ERR_UNSUPPORTED and launch nothing.
  *   - Every GPU that loads the library holds the array until the process
  *     exits. The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress) and keeps it for the process; make that first
+ *     call before any stream capture. A device reset (cudaDeviceReset)
+ *     invalidates the kept address: do not call this entry point on a device
+ *     after resetting it.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other threads) race and must be serialised by the caller. No
  *     content has to start at zero: each call writes every slot it reads.
@@ -268,7 +275,7 @@ int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const 
 int csa2_indexer_reindex_noalloc(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
                                  const int64_t* seq_len, int B, int n_q,
                                  const int32_t* block_table, int max_pages, int64_t n_pages,
-                                 const uint8_t* idx_pages, const int32_t* pool, int32_t* topk,
+                                 const uint8_t* idx_pages, const int32_t* pool, int32_t* topk, int m,
                                  void* stream);
 
 /* Full-mode indexer = scan + block top-2048 + rescore of the pool + top-512.
@@ -284,7 +291,12 @@ int csa2_indexer_full(const uint8_t* q_codes, const uint8_t* q_scales, const flo
 /* o_h = softmax(scale * q_h K^T) V with K = V = the dequantised keys: the main
  * entries at the query's top-k positions (-1 skipped) followed by its FP8
  * window entries, duplicates kept. 64 heads x 512 dims, fp32 softmax.
- *   q: bf16 [B, n_q, 64, 512]; topk: int32 [B, n_q, 512]; ring_idx: int32 [B]
+ *   q: bf16 [B, n_q, 64, 512], every element finite with |q| < 65520: the
+ *   tensor cores take q in f16 (exact for such values, whose f16 rounding
+ *   stays finite); a larger or non-finite element records
+ *   CSA2_ERR_DEVICE_RANGE and makes that token's output undefined (the other
+ *   tokens are unaffected).
+ *   topk: int32 [B, n_q, 512]; ring_idx: int32 [B]
  *   out: [B, n_q, 64, 512] fp32 (out_dtype CSA2_OUT_F32) or bf16
  *   (CSA2_OUT_BF16), optionally | CSA2_OUT_DEROTATE (see its definition;
  *   lse is unchanged by it); lse: fp32 [B, n_q, 64] natural-log sum of exp of the
@@ -359,8 +371,19 @@ int csa2_decode_group(const csa2_layer_args* layers, int n_layers, void* stream)
 
 /* ---- device status ---------------------------------------------------------- */
 /* Waits for the stream, then reads (and clears) the device status words:
- * *status = CSA2_OK, CSA2_ERR_DEVICE_TIMEOUT or CSA2_ERR_DEVICE_BOUNDS. */
+ * *status = CSA2_OK, CSA2_ERR_DEVICE_TIMEOUT, CSA2_ERR_DEVICE_BOUNDS or
+ * CSA2_ERR_DEVICE_RANGE (the first one recorded since the last read). */
 int csa2_check_device_status(void* stream, int* status);
+
+/* Test utility (fault injection without a fault): from this call on, every
+ * bounded wait inside this library's kernels whose internal site number equals
+ * `site` gives up at once, exactly as if its time limit had run out: it
+ * records CSA2_ERR_DEVICE_TIMEOUT (read by csa2_check_device_status), and the
+ * kernel stops its work, waits for its own copies and tensor-core operations
+ * in flight, releases its tensor memory and returns. site = 0 turns it off.
+ * Site 210 is the indexer's tensor-core issuer waiting for a tile's copy (the
+ * Full scan and the pool rescore). Synchronises `stream`. */
+int csa2_debug_force_wait_timeout(int site, void* stream);
 
 #ifdef __cplusplus
 }

@@ -19,7 +19,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 
 # Constants of include/csa2.h.
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE_BOUNDS = range(7)
+(OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE_BOUNDS,
+ ERR_DEVICE_RANGE) = range(8)
 LATENT_DIM, Q_HEADS, IDX_HEADS, IDX_DIM = 512, 64, 32, 128
 TOPK, POOL_BLOCKS, BLOCK, WINDOW, PAGE_TOKENS = 512, 2048, 8, 128, 128
 MAIN_ENTRY_BYTES, IDX_ENTRY_BYTES, MAX_NQ = 288, 72, 8
@@ -37,7 +38,7 @@ EXPORTS = (
     "csa2_ring_refill", "csa2_quant_mxfp4",
     "csa2_dequant_mxfp4", "csa2_quant_fp8", "csa2_indexer_scan", "csa2_block_topk",
     "csa2_indexer_reindex", "csa2_indexer_reindex_noalloc", "csa2_indexer_full", "csa2_sparse_attn", "csa2_sparse_attn_prefill", "csa2_decode_layer",
-    "csa2_decode_group", "csa2_check_device_status",
+    "csa2_decode_group", "csa2_check_device_status", "csa2_debug_force_wait_timeout",
 )
 
 
@@ -86,7 +87,7 @@ def _load():
         "csa2_indexer_scan": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, i64, i32, p], i32),
         "csa2_block_topk": ([p, p, i32, i32, i64, p, i32, p], i32),
         "csa2_indexer_reindex": ([p, p, p, p, i32, i32, p, i32, i64, p, p, p, p, sz, i32, p], i32),
-        "csa2_indexer_reindex_noalloc": ([p, p, p, p, i32, i32, p, i32, i64, p, p, p, p], i32),
+        "csa2_indexer_reindex_noalloc": ([p, p, p, p, i32, i32, p, i32, i64, p, p, p, i32, p], i32),
         "csa2_indexer_full": ([p, p, p, p, i32, i32, i64, p, i32, i64, p, p, p, p, sz, i32, p], i32),
         "csa2_sparse_attn": ([p, p, p, i32, i32, p, i32, i64, p, p, p, i64, f32, i32, p, p, p, sz, i32, p], i32),
         "csa2_sparse_attn_prefill": ([p, p, p, i32, i32, p, i32, i64, p, p, p, i64, p, f32, i32, p, p, p, sz, i32,
@@ -94,6 +95,7 @@ def _load():
         "csa2_decode_layer": ([ctypes.POINTER(LayerArgs), p], i32),
         "csa2_decode_group": ([ctypes.POINTER(LayerArgs), i32, p], i32),
         "csa2_check_device_status": ([p, ctypes.POINTER(ctypes.c_int)], i32),
+        "csa2_debug_force_wait_timeout": ([i32, p], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -272,13 +274,13 @@ def csa2_indexer_reindex(q_codes, q_scales, w, seq_len, block_table, n_pages, id
 
 
 def csa2_indexer_reindex_noalloc(q_codes, q_scales, w, seq_len, block_table, n_pages, idx_pages, pool, topk,
-                                 stream=None):
+                                 stream=None, m=1):
     """csa2_indexer_reindex without a workspace (scores kept in the library's
     fixed device array; at most 64 query tokens per call)."""
     B, n_q = w.shape[0], w.shape[1]
     _check(lib.csa2_indexer_reindex_noalloc(_ptr(q_codes), _ptr(q_scales), _ptr(w), _ptr(seq_len), B, n_q,
                                             _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx_pages),
-                                            _ptr(pool), _ptr(topk), _stream(stream)))
+                                            _ptr(pool), _ptr(topk), m, _stream(stream)))
 
 
 def csa2_indexer_full(q_codes, q_scales, w, seq_len, max_ctx, block_table, n_pages, idx_pages, pool, topk,
@@ -357,6 +359,12 @@ def csa2_check_device_status(stream=None) -> int:
     st = ctypes.c_int(0)
     _check(lib.csa2_check_device_status(_stream(stream), ctypes.byref(st)))
     return st.value
+
+
+def csa2_debug_force_wait_timeout(site: int, stream=None):
+    """Test utility: bounded waits at the given internal site give up at once
+    (CSA2_ERR_DEVICE_TIMEOUT); 0 turns it off."""
+    _check(lib.csa2_debug_force_wait_timeout(site, _stream(stream)))
 
 
 def device_status_message() -> str:

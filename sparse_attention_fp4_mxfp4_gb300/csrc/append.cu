@@ -350,6 +350,8 @@ __global__ void quant_fp8_kernel(const float* __restrict__ x, int64_t n, uint8_t
 
 }  // namespace
 
+cudaError_t force_timeout_append(int site, cudaStream_t stream) { return set_force_timeout_site(site, stream); }
+
 cudaError_t status_append(cudaStream_t stream, int* code, int* where, bool clear) {
   int h[2] = {0, 0};
   cudaError_t e = cudaMemcpyFromSymbolAsync(h, g_status, sizeof(h), 0, cudaMemcpyDeviceToHost, stream);

@@ -291,11 +291,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
       float f[8];
       bf16x8_to_f32(qv[it], f);
       uint32_t o[4];
+      bool bad = false;  // f16 holds |q| < 65520 (65504 after rounding); larger or non-finite q is out of range
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
+        bad |= !(fabsf(f[2 * k]) < 65520.f) || !(fabsf(f[2 * k + 1]) < 65520.f);
         __half2 hv = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
         o[k] = *reinterpret_cast<uint32_t*>(&hv);
       }
+      if (bad) report(CSA2_ERR_DEVICE_RANGE, 405);
       *reinterpret_cast<uint4*>(Qs + (c >> 3) * 8192 + sw128_offset(h, c & 7)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     named_bar_sync(kBarGd, kGdThreads);  // slots of the first chunk are known
@@ -579,6 +582,8 @@ int attn_num_sms() {
 }
 
 }  // namespace
+
+cudaError_t force_timeout_attn(int site, cudaStream_t stream) { return set_force_timeout_site(site, stream); }
 
 cudaError_t status_attn(cudaStream_t stream, int* code, int* where, bool clear) {
   int h[2] = {0, 0};

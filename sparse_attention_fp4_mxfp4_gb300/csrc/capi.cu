@@ -88,6 +88,7 @@ const char* csa2_status_string(int status) {
     case CSA2_ERR_CUDA: return "CUDA error";
     case CSA2_ERR_DEVICE_TIMEOUT: return "a bounded device wait timed out";
     case CSA2_ERR_DEVICE_BOUNDS: return "a device-side index check failed";
+    case CSA2_ERR_DEVICE_RANGE: return "an input value outside the supported range";
     default: return "unknown status";
   }
 }
@@ -281,11 +282,15 @@ int csa2_block_topk(const float* block_max, const int64_t* seq_len, int B, int n
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "block_topk launch");
 }
 
-int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
-                         const int64_t* seq_len, int B, int n_q, const int32_t* block_table,
-                         int max_pages, int64_t n_pages, const uint8_t* idx_pages,
-                         const int32_t* pool, int32_t* topk, void* ws, size_t ws_bytes, int m,
-                         void* stream) {
+}  // extern "C"
+
+namespace csa2 {
+// Host checks of a Reindex call (shared by csa2_indexer_reindex and
+// csa2_indexer_reindex_noalloc, so both accept and reject the same shapes
+// with the same status codes). Pointers are checked only when B > 0.
+int check_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const float* w, const int64_t* seq_len, int B,
+                  int n_q, const int32_t* block_table, int max_pages, int64_t n_pages, const uint8_t* idx_pages,
+                  const int32_t* pool, const int32_t* topk, int m) {
   if (int st = check_batch(B, n_q)) return st;
   if (int st = check_ratio(m)) return st;
   if (B == 0) return CSA2_OK;
@@ -293,6 +298,21 @@ int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const 
   if (int st = check_pages(block_table, max_pages, n_pages)) return st;
   CHECK_PTR(pool, "pool");
   CHECK_PTR(topk, "topk");
+  return CSA2_OK;
+}
+}  // namespace csa2
+
+extern "C" {
+
+int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                         const int64_t* seq_len, int B, int n_q, const int32_t* block_table,
+                         int max_pages, int64_t n_pages, const uint8_t* idx_pages,
+                         const int32_t* pool, int32_t* topk, void* ws, size_t ws_bytes, int m,
+                         void* stream) {
+  if (int st = csa2::check_reindex(q_codes, q_scales, w, seq_len, B, n_q, block_table, max_pages, n_pages,
+                                   idx_pages, pool, topk, m))
+    return st;
+  if (B == 0) return CSA2_OK;
   const int64_t Q = static_cast<int64_t>(B) * n_q;
   if (!ws || ws_bytes < reindex_ws(Q)) return fail(CSA2_ERR_WORKSPACE, "reindex needs %zu workspace bytes", reindex_ws(Q));
   if (!aligned16(ws)) return fail(CSA2_ERR_INVALID_ARG, "ws is not 16-byte aligned");
@@ -436,6 +456,17 @@ int csa2_decode_group(const csa2_layer_args* layers, int n_layers, void* stream)
     }
     if (a->mode == CSA2_MODE_FULL) latest_pool = pool;
     if (a->mode != CSA2_MODE_REUSE) latest_topk = topk;
+  }
+  return CSA2_OK;
+}
+
+int csa2_debug_force_wait_timeout(int site, void* stream) {
+  if (site < 0) return fail(CSA2_ERR_INVALID_ARG, "site = %d < 0", site);
+  cudaError_t (*setters[4])(int, cudaStream_t) = {csa2::force_timeout_append, csa2::force_timeout_indexer,
+                                                   csa2::force_timeout_topk, csa2::force_timeout_attn};
+  for (auto set : setters) {
+    const cudaError_t e = set(site, S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "setting the forced-timeout site");
   }
   return CSA2_OK;
 }

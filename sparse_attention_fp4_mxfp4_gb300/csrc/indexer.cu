@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
     int32_t next_pages = -1;  // scan: page id of tile (i & ~31) + lane
     bool met = false;         // pool: named barrier 2 passed
     const int nt = static_cast<int>(n_tiles);
+    int issued = 0;    // tiles whose copies (or empty arrival) this warp has issued
     int s = 0, u = 0;  // stage of tile i and the round of the ring it is in (i = u * kStages + s)
     for (int i = 0; i < nt; ++i, s = (s + 1 == kStages) ? 0 : s + 1, u += (s == 0) ? 1 : 0) {
       int go = 1;
@@ -319,8 +320,19 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
           bulk_g2s(dst + lane * 576, P.idx_pages + static_cast<int64_t>(src >> 4) * kIdxPageBytes + (src & 15) * 576,
                    576, full0 + 8 * s);
       }
+      issued = i + 1;
     }
     if (pool_split && !met) named_bar_sync(2, 160);  // stopped early: still meet warps 0-3
+    // Every copy issued must have landed before the CTA's shared memory is
+    // released. On the normal path the consumers already waited for all of
+    // them; after an abort, wait here for the last round issued on each stage
+    // (earlier rounds of a stage completed before its next round was issued).
+    if (lane == 0) {
+      for (int st = 0; st < kStages && st < issued; ++st) {
+        const int last = st + kStages * ((issued - 1 - st) / kStages);
+        mbar_wait(full0 + 8 * st, (last / kStages) & 1, 205);
+      }
+    }
   } else if (warp == kEpi + 1) {
     // ---- MMA issuer ----
     if (lane == 0) {
@@ -503,6 +515,8 @@ int ctas_per_sm(int n_q, int pool_tiles, int sub = 1) {
 }
 
 }  // namespace
+
+cudaError_t force_timeout_indexer(int site, cudaStream_t stream) { return set_force_timeout_site(site, stream); }
 
 cudaError_t status_indexer(cudaStream_t stream, int* code, int* where, bool clear) {
   int h[2] = {0, 0};

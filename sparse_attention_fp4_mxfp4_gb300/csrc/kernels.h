@@ -11,12 +11,23 @@ namespace csa2 {
 // Sets the thread-local text returned by csa2_last_error(); returns `code`.
 int record_error(int code, const char* msg);
 
+// Host checks of a Reindex call (batch, ratio m, pointers, alignment, page
+// table); CSA2_OK or the failing status with its error text set.
+int check_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const float* w, const int64_t* seq_len, int B,
+                  int n_q, const int32_t* block_table, int max_pages, int64_t n_pages, const uint8_t* idx_pages,
+                  const int32_t* pool, const int32_t* topk, int m);
+
 // Each kernel translation unit keeps its own device status word; these read
 // (and optionally clear) it. Synchronous with respect to `stream`.
 cudaError_t status_append(cudaStream_t stream, int* code, int* where, bool clear);
 cudaError_t status_indexer(cudaStream_t stream, int* code, int* where, bool clear);
 cudaError_t status_topk(cudaStream_t stream, int* code, int* where, bool clear);
 cudaError_t status_attn(cudaStream_t stream, int* code, int* where, bool clear);
+// Sets the forced-timeout site of each translation unit's bounded waits (0 = off).
+cudaError_t force_timeout_append(int site, cudaStream_t stream);
+cudaError_t force_timeout_indexer(int site, cudaStream_t stream);
+cudaError_t force_timeout_topk(int site, cudaStream_t stream);
+cudaError_t force_timeout_attn(int site, cudaStream_t stream);
 
 cudaError_t launch_append_kv(const void* latent, const void* idx_key, const int32_t* seq_idx,
                              const int64_t* pos, int T, const int32_t* block_table, int B,

@@ -1,17 +1,17 @@
 // Reindex-mode indexer for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc at all: code running inside a CUDA
-// graph that is being captured, plug-ins whose host framework owns every
-// device allocation, and allocators that forbid allocation on the decode path
-// (an allocation there can synchronise the device or fail under memory
-// pressure in the middle of a step). csa2_indexer_reindex needs a caller
-// workspace for its per-slot scores; csa2_indexer_reindex_noalloc keeps those
-// scores in a fixed array of device memory inside this library instead.
+// Some callers cannot call cudaMalloc at all: plug-ins whose host framework
+// owns every device allocation, and decode loops that forbid allocation on
+// the decode path (an allocation there can synchronise the device or fail
+// under memory pressure in the middle of a step). csa2_indexer_reindex needs
+// a caller workspace for its per-slot scores; csa2_indexer_reindex_noalloc
+// keeps those scores in a fixed array of device memory inside this library
+// instead.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it until the process exits. In host code its name is only a
 // host-side stand-in, so the device address is looked up once per device with
-// cudaGetSymbolAddress and passed to the kernels.
+// cudaGetSymbolAddress (with that device current) and passed to the kernels.
 #include <cstdio>
 #include <mutex>
 
@@ -40,12 +40,15 @@ extern "C" {
 int csa2_indexer_reindex_noalloc(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
                                  const int64_t* seq_len, int B, int n_q,
                                  const int32_t* block_table, int max_pages, int64_t n_pages,
-                                 const uint8_t* idx_pages, const int32_t* pool, int32_t* topk,
+                                 const uint8_t* idx_pages, const int32_t* pool, int32_t* topk, int m,
                                  void* stream) {
-  char msg[256];
-  if (B < 0 || n_q < 1 || n_q > CSA2_MAX_NQ)
-    return csa2::record_error(CSA2_ERR_INVALID_ARG, "reindex_noalloc: need B >= 0 and 1 <= n_q <= 8");
+  // The same checks (and status codes) as csa2_indexer_reindex, then the
+  // limit of the fixed scratch array.
+  if (int st = csa2::check_reindex(q_codes, q_scales, w, seq_len, B, n_q, block_table, max_pages, n_pages,
+                                   idx_pages, pool, topk, m))
+    return st;
   if (B == 0) return CSA2_OK;
+  char msg[256];
   if (static_cast<int64_t>(B) * n_q > kMaxQueries) {
     snprintf(msg, sizeof(msg),
              "reindex_noalloc: B * n_q = %lld exceeds the fixed scratch of %d query tokens (4 MiB); "
@@ -53,14 +56,6 @@ int csa2_indexer_reindex_noalloc(const uint8_t* q_codes, const uint8_t* q_scales
              static_cast<long long>(B) * n_q, kMaxQueries);
     return csa2::record_error(CSA2_ERR_UNSUPPORTED, msg);
   }
-  if (!q_codes || !q_scales || !w || !seq_len || !block_table || !idx_pages || !pool || !topk)
-    return csa2::record_error(CSA2_ERR_INVALID_ARG, "reindex_noalloc: a required pointer is NULL");
-  if ((reinterpret_cast<uintptr_t>(q_codes) & 15u) || (reinterpret_cast<uintptr_t>(idx_pages) & 15u) ||
-      (reinterpret_cast<uintptr_t>(q_scales) & 1u))
-    return csa2::record_error(CSA2_ERR_INVALID_ARG, "reindex_noalloc: q_codes / idx_pages must be 16-byte "
-                              "aligned and q_scales 2-byte aligned");
-  if (max_pages < 1 || n_pages < 1)
-    return csa2::record_error(CSA2_ERR_INVALID_ARG, "reindex_noalloc: max_pages and n_pages must be >= 1");
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -82,7 +77,7 @@ int csa2_indexer_reindex_noalloc(const uint8_t* q_codes, const uint8_t* q_scales
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = csa2::launch_pool_scores(q_codes, q_scales, w, seq_len, B, n_q, block_table, max_pages,
-                                           n_pages, idx_pages, pool, scores, s);
+                                           n_pages, idx_pages, pool, scores, s, m);
   if (e == cudaSuccess) e = csa2::launch_pool_topk(scores, seq_len, B, n_q, pool, topk, s);
   if (e != cudaSuccess) {
     snprintf(msg, sizeof(msg), "reindex_noalloc launch: %s", cudaGetErrorString(e));

@@ -19,6 +19,20 @@ __device__ __forceinline__ void report(int code, int where) {
   if (atomicCAS(&g_status[0], 0, code) == 0) g_status[1] = where;
 }
 
+// Test hook (one per translation unit): every bounded wait whose site tag
+// equals this value gives up at once, as if its time limit had run out, so a
+// test can exercise the timeout path without waiting. 0 = off (site tags are
+// positive).
+static __constant__ int g_force_timeout_site;
+
+// Sets this translation unit's forced-timeout site; synchronous on `stream`.
+static inline cudaError_t set_force_timeout_site(int site, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyToSymbolAsync(g_force_timeout_site, &site, sizeof(site), 0, cudaMemcpyHostToDevice,
+                                          stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return e;
+}
+
 // ---- small helpers -----------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -78,11 +92,16 @@ __device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity, 
 }
 
 // Waits for the phase with the given parity to complete. Gives up after about
-// 2 s (or 2^30 polls), records CSA2_ERR_DEVICE_TIMEOUT and returns false. When
+// 2 s (or 2^30 polls; at once when `where` is the forced-timeout site),
+// records CSA2_ERR_DEVICE_TIMEOUT and returns false. When
 // `abort_flag` is given and another role of the CTA has set it, returns false
 // without recording anything.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int where,
                                           volatile int* abort_flag = nullptr) {
+  if (where == g_force_timeout_site) {
+    report(CSA2_ERR_DEVICE_TIMEOUT, where);
+    return false;
+  }
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0; i < (1u << 30); ++i) {
@@ -94,6 +113,71 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int whe
   }
   report(CSA2_ERR_DEVICE_TIMEOUT, where);
   return false;
+}
+
+// As mbar_wait, with cluster-scope acquire: for barriers that CTAs of the
+// cluster arrive on remotely (their stores before the arrival are visible
+// after the wait).
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int where,
+                                                  volatile int* abort_flag = nullptr) {
+  if (where == g_force_timeout_site) {
+    report(CSA2_ERR_DEVICE_TIMEOUT, where);
+    return false;
+  }
+  if (mbar_try_cluster(bar, parity, 0u)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < (1u << 30); ++i) {
+    if (mbar_try_cluster(bar, parity, 100000u)) return true;
+    if ((i & 15u) == 15u) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) break;
+    }
+  }
+  report(CSA2_ERR_DEVICE_TIMEOUT, where);
+  return false;
+}
+
+// ---- thread-block clusters: distributed shared memory -----------------------
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t cl_map(uint32_t smem_addr, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr), "r"(rank));
+  return ra;
+}
+
+__device__ __forceinline__ void cl_st_v4(uint32_t cluster_addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Arrives on an mbarrier of another CTA of the cluster, releasing this
+// thread's earlier memory operations at cluster scope.
+__device__ __forceinline__ void cl_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Every thread of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cl_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ---- bulk copy global -> shared (no tensor map) ------------------------------

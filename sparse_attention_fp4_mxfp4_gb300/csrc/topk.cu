@@ -928,6 +928,8 @@ __global__ void __launch_bounds__(kPoolThreads, 1) pool_topk_kernel(const float*
 
 }  // namespace
 
+cudaError_t force_timeout_topk(int site, cudaStream_t stream) { return set_force_timeout_site(site, stream); }
+
 cudaError_t status_topk(cudaStream_t stream, int* code, int* where, bool clear) {
   int h[2] = {0, 0};
   cudaError_t e = cudaMemcpyFromSymbolAsync(h, g_status, sizeof(h), 0, cudaMemcpyDeviceToHost, stream);

@@ -12,6 +12,10 @@ times (tests.harness.Runner), on outputs the oracle can compute one by one:
   6  Encoder group at 2 tokens per entry (Full + 5 Reuse), 8 x 1M tokens:
      pool and top-512 of 2 sequences and the attention of all six layers
 
+and one context past the block top-k's cluster path: a Full step at
+2,200,000 entries (275,000 block maxima, more than a 16-CTA cluster holds),
+which takes the single-CTA radix select that re-reads the row from memory.
+
 Selections: equal up to ties within 1e-5 relative of the oracle's k-th score.
 Attention: within 2e-3 + 2^-8 (1 + 2e-3) ~ 5.9e-3 max-relative per head row (bf16
 output, as timed: the fp32 bound plus bf16 rounding).
@@ -149,5 +153,20 @@ def test_workload6_encoder_m2_b8_n1m():
         tk = _check_full(S, R, b, 0)
         for li in range(len(S.layers)):
             _check_attn(S, R, b, 0, li, tk)
+    del S, R
+    torch.cuda.empty_cache()
+
+
+def test_full_b1_n2m_block_topk_beyond_the_cluster():
+    from synth.workloads import Workload
+    N = 2_200_000  # > 16 CTAs x 16384 block maxima x 8 positions = 2,097,152
+    wl = Workload(7, "full_b1_n2m", "full", B=1, N=N, n_q=1)
+    S = H.build(wl, DEV)
+    R = H.Runner(S)
+    R.step()
+    torch.cuda.synchronize()
+    assert csa2.csa2_check_device_status() == csa2.OK, csa2.device_status_message()
+    tk = _check_full(S, R, 0, 0)
+    _check_attn(S, R, 0, 0, 0, tk)
     del S, R
     torch.cuda.empty_cache()

@@ -255,6 +255,34 @@ def test_sparse_attention_with_padded_topk():
         H.check_attention(o[b, 0].cpu().numpy(), ro, H.TOL_ATTN_F32)
 
 
+@pytest.mark.parametrize("B", [3, 300])
+def test_sparse_attention_query_out_of_f16_range_sets_the_range_status(B):
+    """A query element at 7e4 does not fit f16 (the tensor cores' operand
+    type): the call records CSA2_ERR_DEVICE_RANGE; the other tokens' outputs
+    stay right. B = 3 takes the split-and-merge path, 300 one CTA per token."""
+    N = 3000
+    wl = Workload(92, "t", "reuse", B=B, N=N, n_q=1, layers=("reuse",))
+    S = H.build(wl, DEV, shuffle_seed=13, prefill_step=True)
+    L = S.layers[0]
+    q = L.q.clone()
+    q[1, 0, 5, 17] = 7e4
+    o = torch.empty(B, 1, 64, 512, device=DEV)
+    ws = torch.empty(csa2.csa2_workspace_bytes(csa2.OP_SPARSE_ATTN, B, 1, N), dtype=torch.uint8, device=DEV)
+    csa2.csa2_sparse_attn(q, S.topk, S.seq_len, S.cache.block_table, S.cache.n_pages, S.cache.main_pages,
+                          S.cache.rings, L.ring_idx, o, None, ws)
+    assert csa2.csa2_check_device_status() == csa2.ERR_DEVICE_RANGE
+    tk = S.topk.cpu().numpy()
+    go = o.cpu().numpy()
+    for b in (0, 2, B - 1):
+        ro, _ = H.oracle_attention(S, b, 0, 0, tk[b, 0])
+        H.check_attention(go[b, 0], ro, H.TOL_ATTN_F32)
+    # The largest finite f16-representable bf16 below the limit is accepted.
+    q[1, 0, 5, 17] = 65280.0
+    csa2.csa2_sparse_attn(q, S.topk, S.seq_len, S.cache.block_table, S.cache.n_pages, S.cache.main_pages,
+                          S.cache.rings, L.ring_idx, o, None, ws)
+    _status_ok()
+
+
 # ---- dispatcher ------------------------------------------------------------------------------
 
 def test_decode_group_full_then_reuse_and_reindex_inheritance():
