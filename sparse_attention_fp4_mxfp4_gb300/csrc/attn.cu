@@ -7,21 +7,37 @@
 // sliding-window entries.
 //
 // A query's 640 key slots form five chunks of 128 (four of top-k entries, one
-// of window entries). A CTA takes a run of consecutive chunks of one query
-// (all five when there are enough queries to fill the GPU, otherwise the
-// chunks are split over up to five CTAs whose partial results a second kernel
-// merges) and walks them with an online softmax:
-//   S^T[128 keys x 64 heads] = K Q^T    (tcgen05, M = 128, N = 64, K = 512)
-//   softmax of the chunk against a running per-head stabiliser, P^T in f16
-//   O^T[512 dims x 64 heads] += V^T P^T (tcgen05, 4 x M = 128, N = 64, K = 128)
-// V^T is the key tile itself read as an MN-major operand; O^T stays in TMEM
-// across chunks. Roles: warps 8-15 gather the next chunk's stored keys into
-// registers while the current chunk is on the tensor cores, then dequantise
-// them (exactly) to f16 into the 128-byte-swizzled key tile, one half of the
-// dimensions at a time, so that the next chunk's first half is written while
-// the tensor cores still read the second half for the current one; warps 0-7
-// own the softmax (S^T row = key, 32 heads per warp) and the output, and their
-// thread 0 issues the MMAs.
+// of window entries). A work item is a run of consecutive chunks of one query
+// (all five when there are enough queries to fill the GPU; otherwise the
+// chunks are split over up to five items whose partial results a second
+// kernel merges), and it runs on a cluster of two CTAs that split the 512
+// latent dimensions: CTA r holds dimensions 256 r .. 256 r + 255 of the query
+// and of every key. Per chunk, with an online softmax:
+//   S_r^T[128 keys x 64 heads] = K_r Q_r^T   (tcgen05, M = 128, N = 64, K = 256)
+//   S^T = S_0^T + S_1^T                       (each CTA sends its partial to the
+//                                              other through distributed shared
+//                                              memory; both add them in the same
+//                                              order, so both hold the same S^T)
+//   softmax against a running per-head stabiliser (computed identically in
+//   both CTAs), P^T in f16
+//   O_r^T[256 dims x 64 heads] += V_r^T P^T  (tcgen05, 2 x M = 128, N = 64, K = 128)
+// V_r^T is the CTA's key half-tile itself read as an MN-major operand; O_r^T
+// stays in TMEM across chunks.
+//
+// An M = 128, K = 16 MMA takes the same time for any N <= 128, so the N = 64
+// (heads) MMAs run well below the tensor pipe's peak whatever the layout;
+// what this design buys is overlap. Half the dimensions per CTA halve the key
+// tile (64 KB of f16 per 128 keys), so each CTA double-buffers it, and the
+// tensor pipe runs S^T of chunk j + 1 and O^T of chunk j - 1 while the
+// softmax warps work on chunk j: pipe order S(0) S(1) O(0) S(2) O(1) ...
+// Roles per CTA: warps 8-11 gather the stored bytes of the CTA's half of each
+// key (one thread per key) into registers ahead of time and dequantise them
+// (exactly) to f16 into the 128-byte-swizzled key tile, a quarter of the
+// dimensions (two K-blocks) at a time, so that a tile's first half is filled
+// while the tensor pipe still reads its second half for the chunk before, and
+// their thread 0 issues the MMAs (each S^T quarter right after the warps wrote
+// it, O^T once the softmax is done); warps 0-7 exchange partial scores, run
+// the softmax (thread = key row x 32 heads) and write the output.
 //
 // The stabiliser is only raised when a chunk's logit exceeds it by more than
 // 8 (log2 units), as in lazy-rescaling flash attention: p = 2^(l - m) <= 256
@@ -37,22 +53,31 @@ namespace csa2 {
 namespace {
 
 constexpr int kChunks = 5;  // four top-k chunks of 128 entries, one window chunk
-constexpr int kSxWarps = 8;
-constexpr int kGdWarps = 8;
-constexpr int kGdThreads = kGdWarps * 32;
-constexpr int kSxThreads = kSxWarps * 32;
-constexpr int kThreads = kSxThreads + kGdThreads;
-constexpr int kKtOff = 0;                // 128 keys x 512 f16: 8 K-blocks of 16 KB
-constexpr int kQsOff = 131072;           // 64 heads x 512 f16: 8 K-blocks of 8 KB
-constexpr int kPtOff = 196608;           // P^T, MN-major: 128 keys x 64 heads f16
-constexpr int kMiscOff = kPtOff + 16384;  // barriers, key offsets, per-head state
-constexpr int kSmemBytes = 1024 + kMiscOff + 4096;
+constexpr int kXWarps = 8;  // scores exchange, softmax, output
+constexpr int kGWarps = 4;  // gather + dequantise; their thread 0 issues the MMAs
+constexpr int kXThreads = kXWarps * 32;
+constexpr int kGThreads = kGWarps * 32;
+constexpr int kTmemWarp = kXWarps;  // the first gather warp allocates and frees TMEM
+constexpr int kThreads = kXThreads + kGThreads;
+constexpr int kTmemCols = 256;           // S^T x 2 buffers (64 columns each), O^T (2 M tiles x 64)
+constexpr int kQsOff = 0;                // Q half: 64 heads x 256 dims f16, 4 K-blocks of 8 KB
+constexpr int kKtOff = 32768;            // 2 key half-tiles: 128 keys x 256 dims f16, 4 K-blocks of 16 KB each
+constexpr int kKtBytes = 65536;
+constexpr int kPtOff = kKtOff + 2 * kKtBytes;  // P^T, MN-major: 128 keys x 64 heads f16
+constexpr int kSxOff = kPtOff + 16384;         // the other CTA's partial S^T: 128 keys x 64 heads fp32
+constexpr int kSxBytes = 32768;
+constexpr int kMiscOff = kSxOff + kSxBytes;    // barriers, key offsets, per-head state
+constexpr int kMiscBytes = 7680;
+constexpr int kSmemBytes = 1024 + kMiscOff + kMiscBytes;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.f;  // headroom (log2 units) before the stabiliser is raised
-constexpr int kBarGd = 1, kBarSxOr = 2, kBarSx = 3;  // named barriers
-constexpr int64_t kChunkSrc = int64_t(1) << 62;     // key offset tag: the call's own window entries
-// Tokens from which a query's chunks are never split over several CTAs (so no
-// partial-output workspace is needed), whatever the SM count.
+// Initial stabiliser: below every finite logit, so the first valid key raises
+// it, and finite, so 2^(l - m) needs no special case (-inf logits give 0).
+constexpr float kNoMax = -1e30f;
+constexpr int kBarG = 1, kBarXOr = 2, kBarX = 3;  // named barriers
+constexpr int64_t kChunkSrc = int64_t(1) << 62;   // key offset tag: the call's own window entries
+// Tokens from which a query's chunks are never split over several work items
+// (so no partial-output workspace is needed), whatever the SM count.
 constexpr int64_t kNoSplitQueries = 256;
 
 struct AttnParams {
@@ -73,7 +98,7 @@ struct AttnParams {
   const uint8_t* swa_chunk;
   int m_shift;        // log2 of the tokens per entry: top-k entries of token t are < (t + 1) >> m_shift
   float scale_log2;   // softmax_scale * log2(e)
-  int nsplit;         // CTAs per query (1..5)
+  int nsplit;         // work items per query (1..5)
   int out_dtype;
   void* out;          // final output (nsplit == 1)
   float* lse;
@@ -114,45 +139,69 @@ __device__ __forceinline__ float derotate_value(float x, float y, int d, float c
   return (d & 1) ? (y * s + x * c) : (x * c - y * s);
 }
 
+// Byte offset, in the partial-score exchange buffer (128 keys x 64 heads
+// fp32), of the 16 bytes that softmax thread (lane quarter qt, head half hh,
+// lane) sends as its c-th group of 4 heads (c = 0..7): the 32 lanes of a warp
+// cover 512 contiguous bytes for each c, so a warp's asynchronous remote
+// stores, and the receiving warp's loads, are contiguous.
+__device__ __forceinline__ uint32_t sx_offset(int qt, int hh, int lane, int c) {
+  return static_cast<uint32_t>((((c * 2 + hh) * 4 + qt) * 32 + lane) * 16);
+}
+
+// 2^x on the special-function unit (x <= 8 here; -inf gives +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* Kt = smem + kKtOff;
   uint8_t* Qs = smem + kQsOff;
+  uint8_t* Kt = smem + kKtOff;
   uint8_t* Pt = smem + kPtOff;
+  uint8_t* Sx = smem + kSxOff;
   uint8_t* misc = smem + kMiscOff;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 64);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 68);
-  int64_t* key_off = reinterpret_cast<int64_t*>(misc + 128);  // [2][128] byte offsets, -1 = none
-  float* mst = reinterpret_cast<float*>(misc + 2176);         // [64] running stabiliser (log2)
-  float* fac = reinterpret_cast<float*>(misc + 2432);         // [64] rescale factors
-  float* lsum = reinterpret_cast<float*>(misc + 2688);        // [64] sums, then their inverses
-  float* red = reinterpret_cast<float*>(misc + 2944);         // [4][64] per-lane-quarter partials
-  // Key tile halves: "lo" = dimensions 0-255 (K-blocks 0-3), "hi" = 256-511.
-  const uint32_t kfull_lo = smem_u32(&bars[0]), kfull_hi = smem_u32(&bars[1]);
-  const uint32_t kfree_lo = smem_u32(&bars[2]), kfree_hi = smem_u32(&bars[3]);
-  const uint32_t sfull = smem_u32(&bars[4]), drain = smem_u32(&bars[5]);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);          // barriers 2..16
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
+  int64_t* key_off = reinterpret_cast<int64_t*>(misc + 512);   // [5][128] byte offsets, -1 = none
+  float* mst = reinterpret_cast<float*>(misc + 5632);          // [64] running stabiliser (log2)
+  float* fac = reinterpret_cast<float*>(misc + 5888);          // [64] rescale factors
+  float* lsum = reinterpret_cast<float*>(misc + 6144);         // [64] inverse sums
+  float* red = reinterpret_cast<float*>(misc + 6400);          // [4][64] per-lane-quarter partials
+  // Key tile quarters: "lo" = dimensions 0-127 of the CTA's half (K-blocks 0-1), "hi" = 128-255.
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t kfull_hi0 = bar(2), kfree_lo0 = bar(4), kfree_hi0 = bar(6);
+  const uint32_t sfull0 = bar(8), sfree0 = bar(10);
+  const uint32_t odone = bar(12), pfull = bar(13), sxfull = bar(14), sxfree = bar(15), drain = bar(16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    mbar_init(kfull_lo, kGdThreads);
-    mbar_init(kfull_hi, kGdThreads);
-    mbar_init(kfree_lo, 1);
-    mbar_init(kfree_hi, 1);
-    mbar_init(sfull, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(kfull_hi0 + 8 * i, kGThreads);
+      mbar_init(kfree_lo0 + 8 * i, 1);
+      mbar_init(kfree_hi0 + 8 * i, 1);
+      mbar_init(sfull0 + 8 * i, 1);
+      mbar_init(sfree0 + 8 * i, kXThreads);
+    }
+    mbar_init(odone, 1);
+    mbar_init(pfull, kXThreads);
+    mbar_init(sxfull, 1);  // armed here with the bytes expected from the other CTA (st.async)
+    mbar_init(sxfree, 1);  // one remote arrival per chunk: the other CTA has read its partials
     mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_init_fence();
+    mbar_arrive_expect_tx(sxfull, kSxBytes);  // chunk 0's partials
   }
-  if (tid < 64) {
-    mst[tid] = -INFINITY;
-    lsum[tid] = 0.f;
-  }
-  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (tid < 64) mst[tid] = kNoMax;
+  if (warp == kTmemWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  cl_sync();       // both CTAs' barriers exist before either arrives remotely
   griddep_wait();  // everything below may read what earlier kernels wrote
   griddep_launch();
-  const int split = blockIdx.x;
+  const int rk = static_cast<int>(cl_rank());  // this CTA's dimension half
+  const int split = blockIdx.x >> 1;
   const int q = blockIdx.y;
   const int b = q / P.n_q, jq = q % P.n_q;
   const int64_t N = P.seq_len[b];
@@ -166,97 +215,109 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= kSxWarps) {
-    // ============ gather + dequantise (256 threads, two per key) ============
-    // Thread (key r, sub) owns dimensions sub*128 .. +127 of each tile half:
-    // lo = sub*128 + [0,128), hi = 256 + sub*128 + [0,128).
-    const int gt = tid - kSxThreads;
-    const int r = gt >> 1, sub = gt & 1;
-    auto resolve = [&](int c, int64_t* dst) {  // threads gt < 128: byte offset of key slot gt
-      if (gt >= 128) return;
-      int64_t off = -1;
-      if (c < 4) {
-        const int32_t p = P.topk[static_cast<int64_t>(q) * 512 + c * 128 + gt];
+  if (warp >= kXWarps) {
+    // ============ gather + dequantise (128 threads, one per key row), MMAs ============
+    const int gt = tid - kXThreads;
+    const int r = gt;
+    // Byte offsets of key slot gt of every chunk of the work item, into
+    // key_off (-1 = no key). The top-k reads of all chunks are issued
+    // together, then their block-table reads, so the whole lookup costs two
+    // dependent round trips once instead of two per chunk.
+    auto resolve_all = [&]() {
+      int32_t pos[kChunks], page[kChunks];
+#pragma unroll
+      for (int k = 0; k < kChunks; ++k) {
+        const int c = c0 + k;
+        pos[k] = (k < nc && c < 4) ? P.topk[static_cast<int64_t>(q) * 512 + c * 128 + gt] : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < kChunks; ++k) {
+        page[k] = -1;
+        const int32_t p = pos[k];
         if (p >= 0) {
           if (p > ((t + 1) >> P.m_shift) - 1 || (p >> 7) >= P.max_pages) {
             report(CSA2_ERR_DEVICE_BOUNDS, 401);
+            pos[k] = -1;
           } else {
-            const int32_t page = P.block_table[static_cast<int64_t>(b) * P.max_pages + (p >> 7)];
-            if (page < 0 || page >= P.n_pages) report(CSA2_ERR_DEVICE_BOUNDS, 402);
-            else off = static_cast<int64_t>(page) * (128 * 288) + (p & 127) * 288;
-          }
-        }
-      } else if (!P.swa_chunk) {
-        const int32_t ri = P.ring_idx[b];
-        const int64_t base = N - 128;  // the ring holds positions N-128 .. N-1
-        int64_t d = (static_cast<int64_t>(gt) - base) % 128;
-        if (d < 0) d += 128;
-        const int64_t p = base + d;  // the position stored in slot gt
-        int64_t lo = t - 127;
-        if (lo < base) lo = base;
-        if (lo < 0) lo = 0;
-        if (ri < 0 || ri >= P.n_rings) {
-          if (gt == 0) report(CSA2_ERR_DEVICE_BOUNDS, 403);
-        } else if (p >= lo && p <= t) {
-          off = (static_cast<int64_t>(ri) * 128 + gt) * 512;
-        }
-      } else {
-        // Prefill: key slot gt holds position t - 127 + gt, from the call's
-        // own entries when it is one of the new positions, else from the ring
-        // (which still holds the 128 positions before them).
-        const int64_t p = t - 127 + gt, first_new = N - P.n_q;
-        if (p >= 0) {
-          if (p >= first_new) {
-            off = kChunkSrc | ((static_cast<int64_t>(b) * P.n_q + (p - first_new)) * 512);
-          } else {
-            const int32_t ri = P.ring_idx[b];
-            if (ri < 0 || ri >= P.n_rings) report(CSA2_ERR_DEVICE_BOUNDS, 404);
-            else off = (static_cast<int64_t>(ri) * 128 + (p & 127)) * 512;
+            page[k] = P.block_table[static_cast<int64_t>(b) * P.max_pages + (p >> 7)];
           }
         }
       }
-      dst[gt] = off;
+#pragma unroll
+      for (int k = 0; k < kChunks; ++k) {
+        const int c = c0 + k;
+        if (k >= nc) continue;
+        int64_t off = -1;
+        if (c < 4) {
+          if (pos[k] >= 0) {
+            if (page[k] < 0 || page[k] >= P.n_pages) report(CSA2_ERR_DEVICE_BOUNDS, 402);
+            else off = static_cast<int64_t>(page[k]) * (128 * 288) + (pos[k] & 127) * 288;
+          }
+        } else if (!P.swa_chunk) {
+          const int32_t ri = P.ring_idx[b];
+          const int64_t base = N - 128;  // the ring holds positions N-128 .. N-1
+          int64_t d = (static_cast<int64_t>(gt) - base) % 128;
+          if (d < 0) d += 128;
+          const int64_t p = base + d;  // the position stored in slot gt
+          int64_t lo = t - 127;
+          if (lo < base) lo = base;
+          if (lo < 0) lo = 0;
+          if (ri < 0 || ri >= P.n_rings) {
+            if (gt == 0) report(CSA2_ERR_DEVICE_BOUNDS, 403);
+          } else if (p >= lo && p <= t) {
+            off = (static_cast<int64_t>(ri) * 128 + gt) * 512;
+          }
+        } else {
+          // Prefill: key slot gt holds position t - 127 + gt, from the call's
+          // own entries when it is one of the new positions, else from the
+          // ring (which still holds the 128 positions before them).
+          const int64_t p = t - 127 + gt, first_new = N - P.n_q;
+          if (p >= 0) {
+            if (p >= first_new) {
+              off = kChunkSrc | ((static_cast<int64_t>(b) * P.n_q + (p - first_new)) * 512);
+            } else {
+              const int32_t ri = P.ring_idx[b];
+              if (ri < 0 || ri >= P.n_rings) report(CSA2_ERR_DEVICE_BOUNDS, 404);
+              else off = (static_cast<int64_t>(ri) * 128 + (p & 127)) * 512;
+            }
+          }
+        }
+        key_off[c * 128 + gt] = off;
+      }
     };
-    // Stored bytes of this thread's share of key r. FP4: code bytes
-    // [sub*64, +64) and [128 + sub*64, +64), scale bytes [256 + sub*8, +8) and
-    // [272 + sub*8, +8). FP8: bytes [sub*128, +128) and [256 + sub*128, +128).
+    // Stored bytes of this CTA's half of key r. FP4: code bytes
+    // [128 rk, +128) and scale bytes [256 + 16 rk, +16). FP8: bytes
+    // [256 rk, +256).
     uint4 raw[16];
-    uint2 scl[2];
-    auto load = [&](int c, const int64_t* offs) {
-      const int64_t off = offs[r];
+    uint4 scl;
+    auto load = [&](int c, int64_t off) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) raw[i] = make_uint4(0, 0, 0, 0);
-      scl[0] = scl[1] = make_uint2(0, 0);
+      scl = make_uint4(0, 0, 0, 0);
       if (off < 0) return;
       if (c < 4) {
         const uint8_t* e = P.main_pages + off;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) raw[4 * hf + i] = reinterpret_cast<const uint4*>(e + hf * 128 + sub * 64)[i];
-          scl[hf] = *reinterpret_cast<const uint2*>(e + 256 + hf * 16 + sub * 8);
-        }
+        for (int i = 0; i < 8; ++i) raw[i] = reinterpret_cast<const uint4*>(e + 128 * rk)[i];
+        scl = *reinterpret_cast<const uint4*>(e + 256 + 16 * rk);
       } else {
         const uint8_t* e = (off & kChunkSrc) ? P.swa_chunk + (off & ~kChunkSrc) : P.rings + off;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) raw[8 * hf + i] = reinterpret_cast<const uint4*>(e + hf * 256 + sub * 128)[i];
-        }
+        for (int i = 0; i < 16; ++i) raw[i] = reinterpret_cast<const uint4*>(e + 256 * rk)[i];
       }
     };
-    auto dequant = [&](int c, int hf) {  // one tile half of this thread's share
-      const int d0 = hf * 256 + sub * 128;
+    auto dequant = [&](int c, uint8_t* kt, int hf) {  // dimensions 128 hf .. +127 of the half
       if (c < 4) {
-        const uint32_t sw[2] = {scl[hf].x, scl[hf].y};
+        const uint32_t sw[4] = {scl.x, scl.y, scl.z, scl.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint4 o[4];
-          dequant32_f16(raw[4 * hf + i], static_cast<uint16_t>(sw[i >> 1] >> (16 * (i & 1))), o);
+          const int ib = 4 * hf + i;  // 32-dim group: 16 code bytes, 2 scale bytes
+          dequant32_f16(raw[ib], static_cast<uint16_t>(sw[ib >> 1] >> (16 * (ib & 1))), o);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const int d = d0 + 32 * i + 8 * k;
-            *reinterpret_cast<uint4*>(Kt + (d >> 6) * 16384 + sw128_offset(r, (d & 63) >> 3)) = o[k];
+            const int d = 32 * ib + 8 * k;
+            *reinterpret_cast<uint4*>(kt + (d >> 6) * 16384 + sw128_offset(r, (d & 63) >> 3)) = o[k];
           }
         }
       } else {
@@ -270,220 +331,310 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
             h[2 * k] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xFFFFu));
             h[2 * k + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
           }
-          const int d = d0 + 16 * i;
-          uint8_t* kb = Kt + (d >> 6) * 16384;
+          const int d = 128 * hf + 16 * i;
+          uint8_t* kb = kt + (d >> 6) * 16384;
           *reinterpret_cast<uint4*>(kb + sw128_offset(r, (d & 63) >> 3)) = make_uint4(h[0], h[1], h[2], h[3]);
           *reinterpret_cast<uint4*>(kb + sw128_offset(r, ((d & 63) >> 3) + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
         }
       }
     };
 
-    // Q loads first: they depend on nothing and overlap the slot lookups.
+    // The CTA's half of Q: 64 heads x 256 dims, 16 x 16 bytes per thread, in
+    // two batches of loads; the first chunk's slot lookups overlap them.
     const uint4* qg = reinterpret_cast<const uint4*>(P.q + static_cast<int64_t>(q) * 64 * 512);
-    uint4 qv[16];
+    bool bad = false;  // f16 holds |q| < 65520 (65504 after rounding); larger or non-finite q is out of range
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      uint4 qv[8];
 #pragma unroll
-    for (int it = 0; it < 16; ++it) qv[it] = qg[gt + it * kGdThreads];
-    resolve(c0, key_off);
-#pragma unroll
-    for (int it = 0; it < 16; ++it) {  // Q (bf16 -> f16) into the swizzled B operand
-      const int i = gt + it * kGdThreads;
-      const int h = i >> 6, c = i & 63;
-      float f[8];
-      bf16x8_to_f32(qv[it], f);
-      uint32_t o[4];
-      bool bad = false;  // f16 holds |q| < 65520 (65504 after rounding); larger or non-finite q is out of range
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        bad |= !(fabsf(f[2 * k]) < 65520.f) || !(fabsf(f[2 * k + 1]) < 65520.f);
-        __half2 hv = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
-        o[k] = *reinterpret_cast<uint32_t*>(&hv);
+      for (int it = 0; it < 8; ++it) {
+        const int i = gt + (8 * half + it) * kGThreads;  // (head, 8-dim group) = (i >> 5, i & 31)
+        qv[it] = qg[(i >> 5) * 64 + 32 * rk + (i & 31)];
       }
-      if (bad) report(CSA2_ERR_DEVICE_RANGE, 405);
-      *reinterpret_cast<uint4*>(Qs + (c >> 3) * 8192 + sw128_offset(h, c & 7)) = make_uint4(o[0], o[1], o[2], o[3]);
+      if (half == 0) {
+        resolve_all();
+        load(c0, key_off[c0 * 128 + r]);  // each thread reads only its own key slots
+      }
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {  // Q (bf16 -> f16) into the swizzled B operand
+        const int i = gt + (8 * half + it) * kGThreads;
+        const int h = i >> 5, g = i & 31;
+        float f[8];
+        bf16x8_to_f32(qv[it], f);
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          bad |= !(fabsf(f[2 * k]) < 65520.f) || !(fabsf(f[2 * k + 1]) < 65520.f);
+          __half2 hv = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
+          o[k] = *reinterpret_cast<uint32_t*>(&hv);
+        }
+        *reinterpret_cast<uint4*>(Qs + (g >> 3) * 8192 + sw128_offset(h, g & 7)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
     }
-    named_bar_sync(kBarGd, kGdThreads);  // slots of the first chunk are known
-    load(c0, key_off);
+    if (bad) report(CSA2_ERR_DEVICE_RANGE, 405);
+    fence_proxy_async();
+    named_bar_sync(kBarG, kGThreads);  // the Q tile is complete
+
+    // MMAs, issued by thread gt == 0 right after a named barrier of the
+    // gather warps (their shared-memory writes, each followed by a proxy
+    // fence, are then visible to the tensor cores).
+    const uint32_t id_s = idesc_f16(128, 64, false, false);
+    const uint32_t id_o = idesc_f16(128, 64, true, true);
+    const uint32_t qs = smem_u32(Qs), pt = smem_u32(Pt);
+    bool mma_ok = true;  // gt == 0: every MMA wait so far succeeded
+    // S_r^T = K_r Q_r^T, one key tile quarter (8 K-steps) of chunk jj.
+    auto issue_s = [&](int jj, int hf) {
+      const int bf = jj & 1;
+      const uint32_t kt = smem_u32(Kt + bf * kKtBytes);
+      tc_fence_after();
+#pragma unroll
+      for (int k = 8 * hf; k < 8 * hf + 8; ++k) {
+        const uint64_t ad = sdesc(kt + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, kSwizzle128B);
+        const uint64_t bd = sdesc(qs + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024, kSwizzle128B);
+        umma_f16(tmem + 64 * bf, ad, bd, id_s, k > 0 ? 1u : 0u);
+      }
+      if (hf == 1) umma_commit(sfull0 + 8 * bf);
+    };
+    // O_r^T += V_r^T P^T of chunk j, once its P^T is written; frees the key
+    // tile quarter by quarter.
+    auto issue_o = [&](int j) -> bool {
+      if (!mbar_wait(pfull, j & 1, 452, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t kt = smem_u32(Kt + (j & 1) * kKtBytes);
+#pragma unroll 1
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ad = sdesc(kt + mt * 32768 + ks * 2048, 16384, 1024, kSwizzle128B);
+          const uint64_t bd = sdesc(pt + ks * 2048, 16384, 1024, kSwizzle128B);
+          umma_f16(tmem + 128 + 64 * mt, ad, bd, id_o, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit((mt == 0 ? kfree_lo0 : kfree_hi0) + 8 * (j & 1));
+      }
+      umma_commit(odone);
+      return true;
+    };
+
+    bool done = true;  // every chunk's tile was written
     for (int jj = 0; jj < nc; ++jj) {
-      // A tile half is free once the previous chunk's O^T MMAs that read it are done.
-      const bool ok = jj == 0 || mbar_wait(kfree_lo, (jj - 1) & 1, 421, abort_flag);
-      if (named_bar_or(kBarGd, kGdThreads, !ok || *abort_flag)) {
+      const int c = c0 + jj, bf = jj & 1;
+      uint8_t* kt = Kt + bf * kKtBytes;
+      // A tile quarter is free once the O^T MMAs of the chunk two back that read it are done.
+      const uint32_t ph = ((jj >> 1) - 1) & 1;
+      bool ok = jj < 2 || mbar_wait(kfree_lo0 + 8 * bf, ph, 421, abort_flag);
+      if (named_bar_or(kBarG, kGThreads, !ok || *abort_flag)) {
         *abort_flag = 1;
+        done = false;
         break;
       }
-      dequant(c0 + jj, 0);
+      dequant(c, kt, 0);
       fence_proxy_async();
-      mbar_arrive(kfull_lo);
-      if (jj == 0 || mbar_wait(kfree_hi, (jj - 1) & 1, 422, abort_flag)) {
-        dequant(c0 + jj, 1);
-        fence_proxy_async();
-        mbar_arrive(kfull_hi);
-      } else {
-        *abort_flag = 1;  // the next check (or the waiting roles) stops everyone
+      named_bar_sync(kBarG, kGThreads);
+      if (gt == 0 && mma_ok) {
+        // The S^T buffer is free once the softmax has read chunk jj - 2 from it.
+        if (jj >= 2 && !mbar_wait(sfree0 + 8 * bf, ph, 451, abort_flag)) {
+          mma_ok = false;
+          *abort_flag = 1;
+        } else {
+          issue_s(jj, 0);
+        }
       }
-      if (jj + 1 < nc) {
-        int64_t* nxt = key_off + ((jj + 1) & 1) * 128;
-        resolve(c0 + jj + 1, nxt);
-        named_bar_sync(kBarGd, kGdThreads);
-        load(c0 + jj + 1, nxt);
+      ok = jj < 2 || mbar_wait(kfree_hi0 + 8 * bf, ph, 422, abort_flag);
+      if (named_bar_or(kBarG, kGThreads, !ok || *abort_flag)) {
+        *abort_flag = 1;
+        done = false;
+        break;
+      }
+      dequant(c, kt, 1);
+      fence_proxy_async();
+      mbar_arrive(kfull_hi0 + 8 * bf);  // the softmax reads the rows' validity after this
+      named_bar_sync(kBarG, kGThreads);
+      if (gt == 0 && mma_ok) issue_s(jj, 1);
+      // The next chunk's bytes are on their way while the MMAs run (each
+      // thread loads its own key row).
+      if (jj + 1 < nc) load(c + 1, key_off[(c + 1) * 128 + r]);
+      if (gt == 0 && mma_ok && jj >= 1 && !issue_o(jj - 1)) {
+        mma_ok = false;
+        *abort_flag = 1;
       }
     }
-  } else {
-    // ============ softmax + output (256 threads) ============
-    // Warp w: TMEM lane quarter qt = w % 4, heads 32*hh .. +31 with hh = w / 4.
+    if (gt == 0) {
+      if (done && mma_ok && nc > 0 && !issue_o(nc - 1)) *abort_flag = 1;
+      // Every MMA issued has completed before TMEM is released.
+      umma_commit(drain);
+      mbar_wait(drain, 0, 433);
+    }
+  } else if (warp < kXWarps) {
+    // ============ score exchange, softmax, output (256 threads) ============
+    // Warp w: TMEM lane quarter qt = w % 4, heads 32 hh .. +31 with hh = w / 4.
     // In S^T a thread owns key row qt*32 + lane; in O^T dimension row
-    // qt*32 + lane of every M tile.
+    // qt*32 + lane of both M tiles.
     const int qt = warp & 3, hh = warp >> 2;
     const int row = qt * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(qt * 32) << 16;
+    const uint32_t peer = static_cast<uint32_t>(rk ^ 1);
+    const uint32_t sx_peer = cl_map(smem_u32(Sx), peer);
+    const uint32_t sxfull_peer = cl_map(sxfull, peer), sxfree_peer = cl_map(sxfree, peer);
     float l[32], acc[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-    auto load_logits = [&](bool kvalid) {
-      uint32_t v[32];
-      tmem_ld32(tmem + lane_base + 32 * hh, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) l[i] = kvalid ? __uint_as_float(v[i]) * P.scale_log2 : -INFINITY;
-    };
-    const uint32_t id_s = idesc_f16(128, 64, false, false);
-    const uint32_t id_o = idesc_f16(128, 64, true, true);
-    const uint32_t kt = smem_u32(Kt), qs = smem_u32(Qs), pt = smem_u32(Pt);
     bool ok = true;
     for (int jj = 0; jj < nc; ++jj) {
-      bool got = mbar_wait(kfull_lo, jj & 1, 441, abort_flag);
-      if (tid == 0 && got) {  // S^T = K Q^T, a tile half at a time
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          if (hf == 1 && !(got = mbar_wait(kfull_hi, jj & 1, 444, abort_flag))) break;
-          tc_fence_after();
-#pragma unroll 4
-          for (int k = 16 * hf; k < 16 * hf + 16; ++k) {
-            const uint64_t ad = sdesc(kt + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bd = sdesc(qs + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024, kSwizzle128B);
-            umma_f16(tmem, ad, bd, id_s, k > 0 ? 1u : 0u);
-          }
-        }
-        if (got) umma_commit(sfull);
+      const int bf = jj & 1;
+      bool got = mbar_wait(sfull0 + 8 * bf, (jj >> 1) & 1, 441, abort_flag);
+      tc_fence_after();
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_base + 64 * bf + 32 * hh, v);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(sfree0 + 8 * bf);
+      // Partial scores to the other CTA (asynchronous stores counted on its
+      // barrier), once it has read the previous ones.
+      got = got && (jj == 0 || mbar_wait_cluster(sxfree, (jj - 1) & 1, 445, abort_flag));
+      if (got) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          cl_st_async_v4(sx_peer + sx_offset(qt, hh, lane, c),
+                         make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]), sxfull_peer);
       }
-      if (!got) *abort_flag = 1;
-      got = got && mbar_wait(sfull, jj & 1, 442, abort_flag);
-      if (named_bar_or(kBarSxOr, kSxThreads, !got)) {
+      got = got && mbar_wait_cluster(sxfull, jj & 1, 446, abort_flag);
+      // The key rows' validity (written by the gather warps before this chunk's tile).
+      got = got && mbar_wait(kfull_hi0 + 8 * bf, (jj >> 1) & 1, 447, abort_flag);
+      if (named_bar_or(kBarXOr, kXThreads, !got)) {
         ok = false;
         *abort_flag = 1;
         break;
       }
-      tc_fence_after();
-      const bool kvalid = key_off[(jj & 1) * 128 + row] >= 0;
-      load_logits(kvalid);
+      const bool kvalid = key_off[(c0 + jj) * 128 + row] >= 0;
       bool over = false;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) over |= l[i] > mst[32 * hh + i] + kLazy;
-      if (named_bar_or(kBarSxOr, kSxThreads, over)) {
+      for (int c = 0; c < 8; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(Sx + sx_offset(qt, hh, lane, c));
+        const float4 m4 = *reinterpret_cast<const float4*>(mst + 32 * hh + 4 * c);
+        // Own partial + the other CTA's (IEEE addition is commutative: both
+        // CTAs get the same logit).
+        l[4 * c] = kvalid ? (__uint_as_float(v[4 * c]) + __uint_as_float(w.x)) * P.scale_log2 : -INFINITY;
+        l[4 * c + 1] = kvalid ? (__uint_as_float(v[4 * c + 1]) + __uint_as_float(w.y)) * P.scale_log2 : -INFINITY;
+        l[4 * c + 2] = kvalid ? (__uint_as_float(v[4 * c + 2]) + __uint_as_float(w.z)) * P.scale_log2 : -INFINITY;
+        l[4 * c + 3] = kvalid ? (__uint_as_float(v[4 * c + 3]) + __uint_as_float(w.w)) * P.scale_log2 : -INFINITY;
+        over |= (l[4 * c] > m4.x + kLazy) || (l[4 * c + 1] > m4.y + kLazy) || (l[4 * c + 2] > m4.z + kLazy) ||
+                (l[4 * c + 3] > m4.w + kLazy);
+      }
+      // Every X thread has read its partials once past this barrier.
+      const bool raise = named_bar_or(kBarXOr, kXThreads, over);
+      if (tid == 0) {
+        if (jj + 1 < nc) mbar_arrive_expect_tx(sxfull, kSxBytes);  // the next chunk's partials
+        // This CTA's exchange buffer may take them: every read of it has
+        // completed (its values were used before the barrier above).
+        cl_arrive_remote_relaxed(sxfree_peer);
+      }
+      if (raise) {
         // Raise the stabiliser to this chunk's per-head maximum where it is larger.
-        warp_reduce_scatter32(l, lane, [](float a, float c) { return fmaxf(a, c); });
-        red[qt * 64 + 32 * hh + lane] = l[0];
-        named_bar_sync(kBarSx, kSxThreads);
+        float mx[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx[i] = l[i];
+        warp_reduce_scatter32(mx, lane, [](float a, float c) { return fmaxf(a, c); });
+        red[qt * 64 + 32 * hh + lane] = mx[0];
+        named_bar_sync(kBarX, kXThreads);
         if (tid < 64) {
           const float cm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
           const float m_old = mst[tid];
           const float m_new = fmaxf(m_old, cm);
-          fac[tid] = m_old == -INFINITY ? 0.f : (m_new == m_old ? 1.f : exp2f(m_old - m_new));
+          fac[tid] = m_new == m_old ? 1.f : ex2(m_old - m_new);  // 0 on the first raise
           mst[tid] = m_new;
         }
-        named_bar_sync(kBarSx, kSxThreads);
+        named_bar_sync(kBarX, kXThreads);
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[i] *= fac[32 * hh + i];
-        if (jj > 0) {  // O^T columns of this warp's heads, every M tile
-          uint32_t v[32];
+      }
+      // P^T row of this key: heads 32*hh .. +31 as f16 (into registers first).
+      uint32_t pw[16];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 m4 = *reinterpret_cast<const float4*>(mst + 32 * hh + 4 * c);
+        __half2 h01 = __floats2half2_rn(ex2(l[4 * c] - m4.x), ex2(l[4 * c + 1] - m4.y));
+        __half2 h23 = __floats2half2_rn(ex2(l[4 * c + 2] - m4.z), ex2(l[4 * c + 3] - m4.w));
+        pw[2 * c] = *reinterpret_cast<uint32_t*>(&h01);
+        pw[2 * c + 1] = *reinterpret_cast<uint32_t*>(&h23);
+        const float2 b01 = __half22float2(h01), b23 = __half22float2(h23);  // the sums use exactly what the MMA sees
+        acc[4 * c] += b01.x;
+        acc[4 * c + 1] += b01.y;
+        acc[4 * c + 2] += b23.x;
+        acc[4 * c + 3] += b23.y;
+      }
+      // O^T and P^T are free once the previous chunk's O^T MMAs are done.
+      got = jj == 0 || mbar_wait(odone, (jj - 1) & 1, 443, abort_flag);
+      if (named_bar_or(kBarXOr, kXThreads, !got)) {
+        ok = false;
+        *abort_flag = 1;
+        break;
+      }
+      if (raise && jj > 0) {  // O^T columns of this warp's heads, both M tiles
+        tc_fence_after();
+        uint32_t o[32];
 #pragma unroll 1
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint32_t a = tmem + lane_base + 64 + 64 * mt + 32 * hh;
-            tmem_ld32(a, v);
-            tmem_wait_ld();
+        for (int mt = 0; mt < 2; ++mt) {
+          const uint32_t a = tmem + lane_base + 128 + 64 * mt + 32 * hh;
+          tmem_ld32(a, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * fac[32 * hh + i]);
-            tmem_st32(a, v);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac[32 * hh + i]);
+          tmem_st32(a, o);
         }
-        load_logits(kvalid);  // the reduction consumed l
+        tmem_wait_st();
       }
-      // P^T row of this key: heads 32*hh .. +31 as f16, MN-major (heads contiguous).
+      // MN-major (heads contiguous).
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = 8 * c + 2 * k;
-          const float m0 = mst[32 * hh + i], m1 = mst[32 * hh + i + 1];
-          const float p0 = m0 == -INFINITY ? 0.f : exp2f(l[i] - m0);
-          const float p1 = m1 == -INFINITY ? 0.f : exp2f(l[i + 1] - m1);
-          __half2 hv = __floats2half2_rn(p0, p1);
-          w[k] = *reinterpret_cast<uint32_t*>(&hv);
-          const float2 back = __half22float2(hv);  // the sums use exactly what the MMA sees
-          acc[i] += back.x;
-          acc[i + 1] += back.y;
-        }
-        *reinterpret_cast<uint4*>(Pt + sw128_offset(row, 4 * hh + c)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(Pt + sw128_offset(row, 4 * hh + c)) =
+            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
       fence_proxy_async();
       tc_fence_before();
-      named_bar_sync(kBarSx, kSxThreads);  // P^T complete (and O^T rescaled)
-      if (tid == 0) {  // O^T += V^T P^T, one commit per tile half
-        tc_fence_after();
-#pragma unroll 1
-        for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t ad = sdesc(kt + mt * 32768 + ks * 2048, 16384, 1024, kSwizzle128B);
-            const uint64_t bd = sdesc(pt + ks * 2048, 16384, 1024, kSwizzle128B);
-            umma_f16(tmem + 64 + 64 * mt, ad, bd, id_o, (jj > 0 || ks > 0) ? 1u : 0u);
-          }
-          if (mt == 1) umma_commit(kfree_lo);
-        }
-        umma_commit(kfree_hi);
-      }
+      mbar_arrive(pfull);
     }
     if (ok && nc > 0) {
-      ok = mbar_wait(kfree_hi, (nc - 1) & 1, 443, abort_flag);
-      ok = !named_bar_or(kBarSxOr, kSxThreads, !ok);
+      ok = mbar_wait(odone, (nc - 1) & 1, 448, abort_flag);
+      ok = !named_bar_or(kBarXOr, kXThreads, !ok);
     }
-    if (ok) {
+    if (ok && nc > 0) {
       tc_fence_after();
-      // Per-head sums over the keys of all chunks.
+      // Per-head sums over the keys of all chunks (the same in both CTAs).
       warp_reduce_scatter32(acc, lane, [](float a, float c) { return a + c; });
       red[qt * 64 + 32 * hh + lane] = acc[0];
-      named_bar_sync(kBarSx, kSxThreads);
+      named_bar_sync(kBarX, kXThreads);
       const bool final_out = P.nsplit == 1;
       if (tid < 64) {
         const float s = (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]);
-        if (final_out) {
-          lsum[tid] = s > 0.f ? 1.f / s : 0.f;
-          if (P.lse)
-            P.lse[static_cast<int64_t>(q) * 64 + tid] = s > 0.f ? (mst[tid] + log2f(s)) * 0.6931471805599453f : -INFINITY;
-        } else {
-          P.stats[(static_cast<int64_t>(q) * kChunks + split) * 64 + tid] = make_float2(mst[tid], s);
+        lsum[tid] = final_out ? (s > 0.f ? 1.f / s : 0.f) : 1.f;
+        if (rk == 0) {
+          if (final_out) {
+            if (P.lse)
+              P.lse[static_cast<int64_t>(q) * 64 + tid] =
+                  s > 0.f ? (mst[tid] + log2f(s)) * 0.6931471805599453f : -INFINITY;
+          } else {
+            P.stats[(static_cast<int64_t>(q) * kChunks + split) * 64 + tid] = make_float2(mst[tid], s);
+          }
         }
       }
-      named_bar_sync(kBarSx, kSxThreads);
+      named_bar_sync(kBarX, kXThreads);
       float* part = P.part + (static_cast<int64_t>(q) * kChunks + split) * (64 * 512);
 #pragma unroll 1
-      for (int mt = 0; mt < 4; ++mt) {
-        const int d = mt * 128 + row;
+      for (int mt = 0; mt < 2; ++mt) {
+        const int d = 256 * rk + 128 * mt + row;
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + 64 + 64 * mt + 32 * hh, v);
+        tmem_ld32(tmem + lane_base + 128 + 64 * mt + 32 * hh, v);
         tmem_wait_ld();
         if (final_out) {
           float y[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(v[i]) * lsum[32 * hh + i];
           if ((P.out_dtype & CSA2_OUT_DEROTATE) && d >= 448) {  // whole warps: rows 64..127 of the last M tile
-            float c, sn;
-            derotate_cs(t, (d - 448) >> 1, c, sn);
+            float cs, sn;
+            derotate_cs(t, (d - 448) >> 1, cs, sn);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float other = __shfl_xor_sync(0xffffffffu, y[i], 1);
-              y[i] = derotate_value(y[i], other, d, c, sn);
+              y[i] = derotate_value(y[i], other, d, cs, sn);
             }
           }
           if ((P.out_dtype & ~CSA2_OUT_DEROTATE) == CSA2_OUT_F32) {
@@ -504,15 +655,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
     }
   }
 
-  if (tid == 0) {  // every MMA issued has completed before TMEM is released
-    umma_commit(drain);
-    mbar_wait(drain, 0, 433);
-  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  cl_sync();  // the other CTA no longer touches this CTA's shared memory
+  if (warp == kTmemWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -638,17 +786,18 @@ cudaError_t launch_sparse_attn(const void* q, const int32_t* topk, const int64_t
   p.swa_chunk = swa_chunk;
   p.m_shift = m == 2 ? 1 : 0;
   p.scale_log2 = softmax_scale * kLog2e;
-  // Split a query's chunks over several CTAs only while that is what fills the GPU.
+  // Split a query's chunks over several work items (two CTAs each) only while
+  // that is what fills the GPU.
   p.nsplit = Q >= kNoSplitQueries
-                 ? 1 : static_cast<int>(std::min<int64_t>(kChunks, std::max<int64_t>(1, attn_num_sms() / Q)));
+                 ? 1 : static_cast<int>(std::min<int64_t>(kChunks, std::max<int64_t>(1, attn_num_sms() / (2 * Q))));
   p.out_dtype = out_dtype;
   p.out = out;
   p.lse = lse;
   const size_t part_bytes = static_cast<size_t>(Q) * kChunks * 64 * 512 * sizeof(float);
   p.part = static_cast<float*>(ws);
   p.stats = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + ((part_bytes + 255) & ~size_t(255)));
-  cudaError_t e = launch_pdl(attn_kernel, dim3(static_cast<unsigned>(p.nsplit), static_cast<unsigned>(Q)),
-                             dim3(kThreads), kSmemBytes, stream, 0, p);
+  cudaError_t e = launch_pdl(attn_kernel, dim3(static_cast<unsigned>(2 * p.nsplit), static_cast<unsigned>(Q)),
+                             dim3(kThreads), kSmemBytes, stream, 2, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
   return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(Q), 64), dim3(256), 0, stream, 0,
                     static_cast<const float*>(p.part), static_cast<const float2*>(p.stats), p.nsplit, out_dtype,

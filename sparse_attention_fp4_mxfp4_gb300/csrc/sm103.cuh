@@ -169,10 +169,27 @@ __device__ __forceinline__ void cl_st_v4(uint32_t cluster_addr, uint4 v) {
                : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory; its
+// completion counts 16 transaction bytes on that CTA's mbarrier `cluster_bar`
+// (both addresses in the shared::cluster window of the same CTA). The storing
+// thread does not wait for it.
+__device__ __forceinline__ void cl_st_async_v4(uint32_t cluster_addr, uint4 v, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   cluster_addr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_bar)
+               : "memory");
+}
+
 // Arrives on an mbarrier of another CTA of the cluster, releasing this
 // thread's earlier memory operations at cluster scope.
 __device__ __forceinline__ void cl_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Arrives on an mbarrier of another CTA of the cluster without ordering this
+// thread's memory operations (for signals whose reads have already completed).
+__device__ __forceinline__ void cl_arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 // Every thread of every CTA of the cluster (release / acquire).

@@ -39,42 +39,34 @@ class Runner:
         self.out = [torch.empty(B, n_q, 64, 512, dtype=out_dtype, device=dev) for _ in S.layers]
         self.lse = [torch.empty(B, n_q, 64, dtype=torch.float32, device=dev) for _ in S.layers]
         self.launches = 0
-        # The attention launch splits a token's five key chunks over several
-        # CTAs (plus a merge kernel) only while there are fewer tokens than SMs.
+        # The attention splits a token's five key chunks over several work
+        # items of two CTAs each (plus a merge kernel) only while there are
+        # fewer than half as many tokens as SMs.
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        self.attn_launches = 1 if Q >= 256 or min(5, max(1, sms // Q)) == 1 else 2
-        self.side = None
+        self.attn_launches = 1 if Q >= 256 or min(5, max(1, sms // (2 * Q))) == 1 else 2
         self.prefill = prefill
         self.chunk = [torch.empty(B, n_q, 512, dtype=torch.uint8, device=dev) for _ in S.layers] if prefill else None
 
     def step(self, mark=None):
-        """The window-ring appends and the indexer-query quantisations do not
-        depend on the main append, so they run on two side streams forked from
-        the current one and joined before their first consumer."""
+        """All launches on the current stream, in the order of the public-call
+        path (csa2_decode_group after the appends and quantisations), so that
+        every kernel overlaps its predecessor's tail through programmatic
+        dependent launch; side streams would join through events, which
+        this overlap does not cross."""
         csa2, S, c = self.csa2, self.S, self.S.cache
         mark = mark or (lambda name: None)
         n = 0
-        main = torch.cuda.current_stream()
-        if self.side is None:
-            self.side = (torch.cuda.Stream(device=main.device), torch.cuda.Stream(device=main.device))
-        s_swa, s_q = self.side
-        s_swa.wait_stream(main)
-        s_q.wait_stream(main)
-        with torch.cuda.stream(s_swa):
-            for li in range(len(S.layers)):
-                if self.prefill:
-                    csa2.csa2_quant_fp8_entries(S.step_swa[li], self.chunk[li])
-                else:
-                    csa2.csa2_append_swa(S.step_swa[li], S.step_ring_idx[li], S.step_pos, c.rings)
-        with torch.cuda.stream(s_q):
-            for L in S.layers:
-                if L.kind in ("full", "reindex"):
-                    csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
-                    n += 1
         append_main(S)
-        n += (1 if S.m == 1 else 2) + len(S.layers)
-        main.wait_stream(s_q)
-        swa_joined = False
+        n += 1 if S.m == 1 else 2
+        for li, L in enumerate(S.layers):
+            if self.prefill:
+                csa2.csa2_quant_fp8_entries(S.step_swa[li], self.chunk[li])
+            else:
+                csa2.csa2_append_swa(S.step_swa[li], S.step_ring_idx[li], S.step_pos, c.rings)
+            n += 1
+            if L.kind in ("full", "reindex"):
+                csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
+                n += 1
         for li, L in enumerate(S.layers):
             if L.kind == "full":
                 mark("scan0")
@@ -92,9 +84,6 @@ class Runner:
                                           c.idx_pages, pool, self.topk, self.rws, m=S.m)
                 mark("rescore1")
                 n += 2
-            if not swa_joined:
-                main.wait_stream(s_swa)
-                swa_joined = True
             mark("attn0")
             if self.prefill:
                 csa2.csa2_sparse_attn_prefill(L.q, self.topk, S.seq_len, c.block_table, c.n_pages, c.main_pages,
