@@ -67,7 +67,7 @@ constexpr int kPtOff = kKtOff + 2 * kKtBytes;  // P^T, MN-major: 128 keys x 64 h
 constexpr int kSxOff = kPtOff + 16384;         // the other CTA's partial S^T: 128 keys x 64 heads fp32
 constexpr int kSxBytes = 32768;
 constexpr int kMiscOff = kSxOff + kSxBytes;    // barriers, key offsets, per-head state
-constexpr int kMiscBytes = 7680;
+constexpr int kMiscBytes = 3072;
 constexpr int kSmemBytes = 1024 + kMiscOff + kMiscBytes;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.f;  // headroom (log2 units) before the stabiliser is raised
@@ -99,6 +99,7 @@ struct AttnParams {
   int m_shift;        // log2 of the tokens per entry: top-k entries of token t are < (t + 1) >> m_shift
   float scale_log2;   // softmax_scale * log2(e)
   int nsplit;         // work items per query (1..5)
+  int n_items;        // Q * nsplit; each CTA pair walks items pair, pair + pairs, ...
   int out_dtype;
   void* out;          // final output (nsplit == 1)
   float* lse;
@@ -155,6 +156,26 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// One work item: a run of consecutive chunks of one query token.
+struct Item {
+  int q, split, b;
+  int64_t N, t;
+  int c0, nc;
+};
+
+__device__ __forceinline__ Item item_of(const AttnParams& P, int w) {
+  Item it;
+  it.q = w / P.nsplit;
+  it.split = w % P.nsplit;
+  it.b = it.q / P.n_q;
+  it.N = P.seq_len[it.b];
+  it.t = it.N - P.n_q + it.q % P.n_q;
+  const int per = kChunks / P.nsplit, rem = kChunks % P.nsplit;
+  it.c0 = it.split * per + (it.split < rem ? it.split : rem);
+  it.nc = per + (it.split < rem ? 1 : 0);
+  return it;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -166,16 +187,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);          // barriers 2..16
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
-  int64_t* key_off = reinterpret_cast<int64_t*>(misc + 512);   // [5][128] byte offsets, -1 = none
-  float* mst = reinterpret_cast<float*>(misc + 5632);          // [64] running stabiliser (log2)
-  float* fac = reinterpret_cast<float*>(misc + 5888);          // [64] rescale factors
-  float* lsum = reinterpret_cast<float*>(misc + 6144);         // [64] inverse sums
-  float* red = reinterpret_cast<float*>(misc + 6400);          // [4][64] per-lane-quarter partials
+  uint32_t* vbits = reinterpret_cast<uint32_t*>(misc + 512);   // [8 chunk slots][4 words]: key row holds a key
+  float* mst = reinterpret_cast<float*>(misc + 1024);          // [64] running stabiliser (log2)
+  float* fac = reinterpret_cast<float*>(misc + 1280);          // [64] rescale factors
+  float* lsum = reinterpret_cast<float*>(misc + 1536);         // [64] inverse sums
+  float* red = reinterpret_cast<float*>(misc + 1792);          // [4][64] per-lane-quarter partials
   // Key tile quarters: "lo" = dimensions 0-127 of the CTA's half (K-blocks 0-1), "hi" = 128-255.
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t kfull_hi0 = bar(2), kfree_lo0 = bar(4), kfree_hi0 = bar(6);
   const uint32_t sfull0 = bar(8), sfree0 = bar(10);
-  const uint32_t odone = bar(12), pfull = bar(13), sxfull = bar(14), sxfree = bar(15), drain = bar(16);
+  const uint32_t odone = bar(12), drain_o = bar(13), sxfull = bar(14), sxfree = bar(15), drain = bar(16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -187,28 +208,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
       mbar_init(sfree0 + 8 * i, kXThreads);
     }
     mbar_init(odone, 1);
-    mbar_init(pfull, kXThreads);
+    mbar_init(drain_o, 1);
     mbar_init(sxfull, 1);  // armed here with the bytes expected from the other CTA (st.async)
     mbar_init(sxfree, 1);  // one remote arrival per chunk: the other CTA has read its partials
     mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_init_fence();
-    mbar_arrive_expect_tx(sxfull, kSxBytes);  // chunk 0's partials
+    mbar_arrive_expect_tx(sxfull, kSxBytes);  // the first chunk's partials
   }
-  if (tid < 64) mst[tid] = kNoMax;
   if (warp == kTmemWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   cl_sync();       // both CTAs' barriers exist before either arrives remotely
   griddep_wait();  // everything below may read what earlier kernels wrote
   griddep_launch();
   const int rk = static_cast<int>(cl_rank());  // this CTA's dimension half
-  const int split = blockIdx.x >> 1;
-  const int q = blockIdx.y;
-  const int b = q / P.n_q, jq = q % P.n_q;
-  const int64_t N = P.seq_len[b];
-  const int64_t t = N - P.n_q + jq;
-  const int per = kChunks / P.nsplit, rem = kChunks % P.nsplit;
-  const int c0 = split * per + (split < rem ? split : rem);
-  const int nc = per + (split < rem ? 1 : 0);
+  // Work items w = pair, pair + pairs, ...; both CTAs of the pair walk the same ones.
+  const int pair = blockIdx.x >> 1, pairs = gridDim.x >> 1;
 
   tc_fence_before();
   __syncthreads();
@@ -219,70 +233,70 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
     // ============ gather + dequantise (128 threads, one per key row), MMAs ============
     const int gt = tid - kXThreads;
     const int r = gt;
-    // Byte offsets of key slot gt of every chunk of the work item, into
-    // key_off (-1 = no key). The top-k reads of all chunks are issued
-    // together, then their block-table reads, so the whole lookup costs two
-    // dependent round trips once instead of two per chunk.
-    auto resolve_all = [&]() {
+    int64_t offs[kChunks];  // byte offsets of key slot gt of the current item's chunks (-1 = no key)
+    // Resolves this thread's slot of every chunk of item `it`: the top-k
+    // reads of all chunks are issued together, then their block-table reads,
+    // so an item's lookups cost two dependent round trips.
+    auto resolve_item = [&](const Item& it) {
       int32_t pos[kChunks], page[kChunks];
 #pragma unroll
       for (int k = 0; k < kChunks; ++k) {
-        const int c = c0 + k;
-        pos[k] = (k < nc && c < 4) ? P.topk[static_cast<int64_t>(q) * 512 + c * 128 + gt] : -1;
+        const int c = it.c0 + k;
+        pos[k] = (k < it.nc && c < 4) ? P.topk[static_cast<int64_t>(it.q) * 512 + c * 128 + gt] : -1;
       }
 #pragma unroll
       for (int k = 0; k < kChunks; ++k) {
         page[k] = -1;
         const int32_t p = pos[k];
         if (p >= 0) {
-          if (p > ((t + 1) >> P.m_shift) - 1 || (p >> 7) >= P.max_pages) {
+          if (p > ((it.t + 1) >> P.m_shift) - 1 || (p >> 7) >= P.max_pages) {
             report(CSA2_ERR_DEVICE_BOUNDS, 401);
             pos[k] = -1;
           } else {
-            page[k] = P.block_table[static_cast<int64_t>(b) * P.max_pages + (p >> 7)];
+            page[k] = P.block_table[static_cast<int64_t>(it.b) * P.max_pages + (p >> 7)];
           }
         }
       }
 #pragma unroll
       for (int k = 0; k < kChunks; ++k) {
-        const int c = c0 + k;
-        if (k >= nc) continue;
+        const int c = it.c0 + k;
         int64_t off = -1;
-        if (c < 4) {
+        if (k >= it.nc) {
+        } else if (c < 4) {
           if (pos[k] >= 0) {
             if (page[k] < 0 || page[k] >= P.n_pages) report(CSA2_ERR_DEVICE_BOUNDS, 402);
             else off = static_cast<int64_t>(page[k]) * (128 * 288) + (pos[k] & 127) * 288;
           }
         } else if (!P.swa_chunk) {
-          const int32_t ri = P.ring_idx[b];
-          const int64_t base = N - 128;  // the ring holds positions N-128 .. N-1
+          const int32_t ri = P.ring_idx[it.b];
+          const int64_t base = it.N - 128;  // the ring holds positions N-128 .. N-1
           int64_t d = (static_cast<int64_t>(gt) - base) % 128;
           if (d < 0) d += 128;
           const int64_t p = base + d;  // the position stored in slot gt
-          int64_t lo = t - 127;
+          int64_t lo = it.t - 127;
           if (lo < base) lo = base;
           if (lo < 0) lo = 0;
           if (ri < 0 || ri >= P.n_rings) {
             if (gt == 0) report(CSA2_ERR_DEVICE_BOUNDS, 403);
-          } else if (p >= lo && p <= t) {
+          } else if (p >= lo && p <= it.t) {
             off = (static_cast<int64_t>(ri) * 128 + gt) * 512;
           }
         } else {
           // Prefill: key slot gt holds position t - 127 + gt, from the call's
           // own entries when it is one of the new positions, else from the
           // ring (which still holds the 128 positions before them).
-          const int64_t p = t - 127 + gt, first_new = N - P.n_q;
+          const int64_t p = it.t - 127 + gt, first_new = it.N - P.n_q;
           if (p >= 0) {
             if (p >= first_new) {
-              off = kChunkSrc | ((static_cast<int64_t>(b) * P.n_q + (p - first_new)) * 512);
+              off = kChunkSrc | ((static_cast<int64_t>(it.b) * P.n_q + (p - first_new)) * 512);
             } else {
-              const int32_t ri = P.ring_idx[b];
+              const int32_t ri = P.ring_idx[it.b];
               if (ri < 0 || ri >= P.n_rings) report(CSA2_ERR_DEVICE_BOUNDS, 404);
               else off = (static_cast<int64_t>(ri) * 128 + (p & 127)) * 512;
             }
           }
         }
-        key_off[c * 128 + gt] = off;
+        offs[k] = off;
       }
     };
     // Stored bytes of this CTA's half of key r. FP4: code bytes
@@ -290,10 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
     // [256 rk, +256).
     uint4 raw[16];
     uint4 scl;
+    bool raw_valid = false;
     auto load = [&](int c, int64_t off) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) raw[i] = make_uint4(0, 0, 0, 0);
       scl = make_uint4(0, 0, 0, 0);
+      raw_valid = off >= 0;
       if (off < 0) return;
       if (c < 4) {
         const uint8_t* e = P.main_pages + off;
@@ -338,53 +354,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
         }
       }
     };
-
-    // The CTA's half of Q: 64 heads x 256 dims, 16 x 16 bytes per thread, in
-    // two batches of loads; the first chunk's slot lookups overlap them.
-    const uint4* qg = reinterpret_cast<const uint4*>(P.q + static_cast<int64_t>(q) * 64 * 512);
+    // The CTA's half of an item's Q: 64 heads x 256 dims, 16 x 16 bytes per
+    // thread, in two batches of loads, bf16 -> f16 into the swizzled B operand.
     bool bad = false;  // f16 holds |q| < 65520 (65504 after rounding); larger or non-finite q is out of range
+    auto load_q = [&](const Item& it) {
+      const uint4* qg = reinterpret_cast<const uint4*>(P.q + static_cast<int64_t>(it.q) * 64 * 512);
 #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      uint4 qv[8];
+      for (int half = 0; half < 2; ++half) {
+        uint4 qv[8];
 #pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int i = gt + (8 * half + it) * kGThreads;  // (head, 8-dim group) = (i >> 5, i & 31)
-        qv[it] = qg[(i >> 5) * 64 + 32 * rk + (i & 31)];
-      }
-      if (half == 0) {
-        resolve_all();
-        load(c0, key_off[c0 * 128 + r]);  // each thread reads only its own key slots
-      }
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {  // Q (bf16 -> f16) into the swizzled B operand
-        const int i = gt + (8 * half + it) * kGThreads;
-        const int h = i >> 5, g = i & 31;
-        float f[8];
-        bf16x8_to_f32(qv[it], f);
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          bad |= !(fabsf(f[2 * k]) < 65520.f) || !(fabsf(f[2 * k + 1]) < 65520.f);
-          __half2 hv = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
-          o[k] = *reinterpret_cast<uint32_t*>(&hv);
+        for (int k = 0; k < 8; ++k) {
+          const int i = gt + (8 * half + k) * kGThreads;  // (head, 8-dim group) = (i >> 5, i & 31)
+          qv[k] = qg[(i >> 5) * 64 + 32 * rk + (i & 31)];
         }
-        *reinterpret_cast<uint4*>(Qs + (g >> 3) * 8192 + sw128_offset(h, g & 7)) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int i = gt + (8 * half + k) * kGThreads;
+          const int h = i >> 5, g = i & 31;
+          float f[8];
+          bf16x8_to_f32(qv[k], f);
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            bad |= !(fabsf(f[2 * e]) < 65520.f) || !(fabsf(f[2 * e + 1]) < 65520.f);
+            __half2 hv = __floats2half2_rn(f[2 * e], f[2 * e + 1]);
+            o[e] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+          *reinterpret_cast<uint4*>(Qs + (g >> 3) * 8192 + sw128_offset(h, g & 7)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
       }
-    }
-    if (bad) report(CSA2_ERR_DEVICE_RANGE, 405);
-    fence_proxy_async();
-    named_bar_sync(kBarG, kGThreads);  // the Q tile is complete
+      fence_proxy_async();
+    };
 
-    // MMAs, issued by thread gt == 0 right after a named barrier of the
+    // S^T MMAs, issued by thread gt == 0 right after a named barrier of the
     // gather warps (their shared-memory writes, each followed by a proxy
     // fence, are then visible to the tensor cores).
     const uint32_t id_s = idesc_f16(128, 64, false, false);
-    const uint32_t id_o = idesc_f16(128, 64, true, true);
-    const uint32_t qs = smem_u32(Qs), pt = smem_u32(Pt);
+    const uint32_t qs = smem_u32(Qs);
     bool mma_ok = true;  // gt == 0: every MMA wait so far succeeded
-    // S_r^T = K_r Q_r^T, one key tile quarter (8 K-steps) of chunk jj.
-    auto issue_s = [&](int jj, int hf) {
-      const int bf = jj & 1;
+    // S_r^T = K_r Q_r^T, one key tile quarter (8 K-steps) of chunk g.
+    auto issue_s = [&](int g, int hf) {
+      const int bf = g & 1;
       const uint32_t kt = smem_u32(Kt + bf * kKtBytes);
       tc_fence_after();
 #pragma unroll
@@ -395,76 +406,78 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
       }
       if (hf == 1) umma_commit(sfull0 + 8 * bf);
     };
-    // O_r^T += V_r^T P^T of chunk j, once its P^T is written; frees the key
-    // tile quarter by quarter.
-    auto issue_o = [&](int j) -> bool {
-      if (!mbar_wait(pfull, j & 1, 452, abort_flag)) return false;
-      tc_fence_after();
-      const uint32_t kt = smem_u32(Kt + (j & 1) * kKtBytes);
-#pragma unroll 1
-      for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t ad = sdesc(kt + mt * 32768 + ks * 2048, 16384, 1024, kSwizzle128B);
-          const uint64_t bd = sdesc(pt + ks * 2048, 16384, 1024, kSwizzle128B);
-          umma_f16(tmem + 128 + 64 * mt, ad, bd, id_o, (j > 0 || ks > 0) ? 1u : 0u);
-        }
-        umma_commit((mt == 0 ? kfree_lo0 : kfree_hi0) + 8 * (j & 1));
-      }
-      umma_commit(odone);
-      return true;
-    };
 
-    bool done = true;  // every chunk's tile was written
-    for (int jj = 0; jj < nc; ++jj) {
-      const int c = c0 + jj, bf = jj & 1;
-      uint8_t* kt = Kt + bf * kKtBytes;
-      // A tile quarter is free once the O^T MMAs of the chunk two back that read it are done.
-      const uint32_t ph = ((jj >> 1) - 1) & 1;
-      bool ok = jj < 2 || mbar_wait(kfree_lo0 + 8 * bf, ph, 421, abort_flag);
+    int g = 0;          // global chunk counter of this CTA
+    bool live = true;   // no abort seen
+    if (pair < P.n_items) {
+      const Item it0 = item_of(P, pair);
+      resolve_item(it0);
+      load(it0.c0, offs[0]);
+    }
+    for (int w = pair; w < P.n_items && live; w += pairs) {
+      const Item it = item_of(P, w);
+      // Q of this item: the previous item's last S^T MMAs must have read Qs.
+      bool ok = g == 0 || mbar_wait(sfull0 + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1, 456, abort_flag);
+      if (ok) load_q(it);
       if (named_bar_or(kBarG, kGThreads, !ok || *abort_flag)) {
         *abort_flag = 1;
-        done = false;
+        live = false;
         break;
       }
-      dequant(c, kt, 0);
-      fence_proxy_async();
-      named_bar_sync(kBarG, kGThreads);
-      if (gt == 0 && mma_ok) {
-        // The S^T buffer is free once the softmax has read chunk jj - 2 from it.
-        if (jj >= 2 && !mbar_wait(sfree0 + 8 * bf, ph, 451, abort_flag)) {
-          mma_ok = false;
+      for (int jj = 0; jj < it.nc; ++jj, ++g) {
+        const int c = it.c0 + jj, bf = g & 1;
+        uint8_t* kt = Kt + bf * kKtBytes;
+        // A tile quarter is free once the O^T MMAs of the chunk two back that read it are done.
+        const uint32_t ph = ((g >> 1) - 1) & 1;
+        ok = g < 2 || mbar_wait(kfree_lo0 + 8 * bf, ph, 421, abort_flag);
+        if (named_bar_or(kBarG, kGThreads, !ok || *abort_flag)) {
           *abort_flag = 1;
-        } else {
-          issue_s(jj, 0);
+          live = false;
+          break;
         }
-      }
-      ok = jj < 2 || mbar_wait(kfree_hi0 + 8 * bf, ph, 422, abort_flag);
-      if (named_bar_or(kBarG, kGThreads, !ok || *abort_flag)) {
-        *abort_flag = 1;
-        done = false;
-        break;
-      }
-      dequant(c, kt, 1);
-      fence_proxy_async();
-      mbar_arrive(kfull_hi0 + 8 * bf);  // the softmax reads the rows' validity after this
-      named_bar_sync(kBarG, kGThreads);
-      if (gt == 0 && mma_ok) issue_s(jj, 1);
-      // The next chunk's bytes are on their way while the MMAs run (each
-      // thread loads its own key row).
-      if (jj + 1 < nc) load(c + 1, key_off[(c + 1) * 128 + r]);
-      if (gt == 0 && mma_ok && jj >= 1 && !issue_o(jj - 1)) {
-        mma_ok = false;
-        *abort_flag = 1;
+        dequant(c, kt, 0);
+        fence_proxy_async();
+        named_bar_sync(kBarG, kGThreads);
+        if (gt == 0 && mma_ok) {
+          // The S^T buffer is free once the softmax has read chunk g - 2 from it.
+          if (g >= 2 && !mbar_wait(sfree0 + 8 * bf, ph, 451, abort_flag)) {
+            mma_ok = false;
+            *abort_flag = 1;
+          } else {
+            issue_s(g, 0);
+          }
+        }
+        ok = g < 2 || mbar_wait(kfree_hi0 + 8 * bf, ph, 422, abort_flag);
+        if (named_bar_or(kBarG, kGThreads, !ok || *abort_flag)) {
+          *abort_flag = 1;
+          live = false;
+          break;
+        }
+        dequant(c, kt, 1);
+        fence_proxy_async();
+        // Which key rows hold a key (read by the softmax after this chunk's tile is complete).
+        const uint32_t vb = __ballot_sync(0xffffffffu, raw_valid);
+        if (lane == 0) vbits[(g & 7) * 4 + (warp - kXWarps)] = vb;
+        mbar_arrive(kfull_hi0 + 8 * bf);
+        named_bar_sync(kBarG, kGThreads);
+        if (gt == 0 && mma_ok) issue_s(g, 1);
+        // The next chunk's bytes (of this item, or the next item's first) are
+        // on their way while the MMAs run; each thread loads its own key row.
+        if (jj + 1 < it.nc) {
+          load(c + 1, offs[jj + 1]);
+        } else if (w + pairs < P.n_items) {
+          const Item nx = item_of(P, w + pairs);
+          resolve_item(nx);
+          load(nx.c0, offs[0]);
+        }
       }
     }
-    if (gt == 0) {
-      if (done && mma_ok && nc > 0 && !issue_o(nc - 1)) *abort_flag = 1;
-      // Every MMA issued has completed before TMEM is released.
+    if (bad) report(CSA2_ERR_DEVICE_RANGE, 405);
+    if (gt == 0) {  // every S^T MMA issued has completed before TMEM is released
       umma_commit(drain);
       mbar_wait(drain, 0, 433);
     }
-  } else if (warp < kXWarps) {
+  } else {
     // ============ score exchange, softmax, output (256 threads) ============
     // Warp w: TMEM lane quarter qt = w % 4, heads 32 hh .. +31 with hh = w / 4.
     // In S^T a thread owns key row qt*32 + lane; in O^T dimension row
@@ -475,128 +488,157 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
     const uint32_t peer = static_cast<uint32_t>(rk ^ 1);
     const uint32_t sx_peer = cl_map(smem_u32(Sx), peer);
     const uint32_t sxfull_peer = cl_map(sxfull, peer), sxfree_peer = cl_map(sxfree, peer);
+    const uint32_t id_o = idesc_f16(128, 64, true, true);
     float l[32], acc[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
     bool ok = true;
-    for (int jj = 0; jj < nc; ++jj) {
-      const int bf = jj & 1;
-      bool got = mbar_wait(sfull0 + 8 * bf, (jj >> 1) & 1, 441, abort_flag);
-      tc_fence_after();
-      uint32_t v[32];
-      tmem_ld32(tmem + lane_base + 64 * bf + 32 * hh, v);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(sfree0 + 8 * bf);
-      // Partial scores to the other CTA (asynchronous stores counted on its
-      // barrier), once it has read the previous ones.
-      got = got && (jj == 0 || mbar_wait_cluster(sxfree, (jj - 1) & 1, 445, abort_flag));
-      if (got) {
+    int g = 0;
+    for (int w = pair; w < P.n_items && ok; w += pairs) {
+      const Item it = item_of(P, w);
+      const bool more_after = w + pairs < P.n_items;  // another item follows this one
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          cl_st_async_v4(sx_peer + sx_offset(qt, hh, lane, c),
-                         make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]), sxfull_peer);
-      }
-      got = got && mbar_wait_cluster(sxfull, jj & 1, 446, abort_flag);
-      // The key rows' validity (written by the gather warps before this chunk's tile).
-      got = got && mbar_wait(kfull_hi0 + 8 * bf, (jj >> 1) & 1, 447, abort_flag);
-      if (named_bar_or(kBarXOr, kXThreads, !got)) {
-        ok = false;
-        *abort_flag = 1;
-        break;
-      }
-      const bool kvalid = key_off[(c0 + jj) * 128 + row] >= 0;
-      bool over = false;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 w = *reinterpret_cast<const uint4*>(Sx + sx_offset(qt, hh, lane, c));
-        const float4 m4 = *reinterpret_cast<const float4*>(mst + 32 * hh + 4 * c);
-        // Own partial + the other CTA's (IEEE addition is commutative: both
-        // CTAs get the same logit).
-        l[4 * c] = kvalid ? (__uint_as_float(v[4 * c]) + __uint_as_float(w.x)) * P.scale_log2 : -INFINITY;
-        l[4 * c + 1] = kvalid ? (__uint_as_float(v[4 * c + 1]) + __uint_as_float(w.y)) * P.scale_log2 : -INFINITY;
-        l[4 * c + 2] = kvalid ? (__uint_as_float(v[4 * c + 2]) + __uint_as_float(w.z)) * P.scale_log2 : -INFINITY;
-        l[4 * c + 3] = kvalid ? (__uint_as_float(v[4 * c + 3]) + __uint_as_float(w.w)) * P.scale_log2 : -INFINITY;
-        over |= (l[4 * c] > m4.x + kLazy) || (l[4 * c + 1] > m4.y + kLazy) || (l[4 * c + 2] > m4.z + kLazy) ||
-                (l[4 * c + 3] > m4.w + kLazy);
-      }
-      // Every X thread has read its partials once past this barrier.
-      const bool raise = named_bar_or(kBarXOr, kXThreads, over);
-      if (tid == 0) {
-        if (jj + 1 < nc) mbar_arrive_expect_tx(sxfull, kSxBytes);  // the next chunk's partials
-        // This CTA's exchange buffer may take them: every read of it has
-        // completed (its values were used before the barrier above).
-        cl_arrive_remote_relaxed(sxfree_peer);
-      }
-      if (raise) {
-        // Raise the stabiliser to this chunk's per-head maximum where it is larger.
-        float mx[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mx[i] = l[i];
-        warp_reduce_scatter32(mx, lane, [](float a, float c) { return fmaxf(a, c); });
-        red[qt * 64 + 32 * hh + lane] = mx[0];
-        named_bar_sync(kBarX, kXThreads);
-        if (tid < 64) {
-          const float cm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
-          const float m_old = mst[tid];
-          const float m_new = fmaxf(m_old, cm);
-          fac[tid] = m_new == m_old ? 1.f : ex2(m_old - m_new);  // 0 on the first raise
-          mst[tid] = m_new;
-        }
-        named_bar_sync(kBarX, kXThreads);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] *= fac[32 * hh + i];
-      }
-      // P^T row of this key: heads 32*hh .. +31 as f16 (into registers first).
-      uint32_t pw[16];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 m4 = *reinterpret_cast<const float4*>(mst + 32 * hh + 4 * c);
-        __half2 h01 = __floats2half2_rn(ex2(l[4 * c] - m4.x), ex2(l[4 * c + 1] - m4.y));
-        __half2 h23 = __floats2half2_rn(ex2(l[4 * c + 2] - m4.z), ex2(l[4 * c + 3] - m4.w));
-        pw[2 * c] = *reinterpret_cast<uint32_t*>(&h01);
-        pw[2 * c + 1] = *reinterpret_cast<uint32_t*>(&h23);
-        const float2 b01 = __half22float2(h01), b23 = __half22float2(h23);  // the sums use exactly what the MMA sees
-        acc[4 * c] += b01.x;
-        acc[4 * c + 1] += b01.y;
-        acc[4 * c + 2] += b23.x;
-        acc[4 * c + 3] += b23.y;
-      }
-      // O^T and P^T are free once the previous chunk's O^T MMAs are done.
-      got = jj == 0 || mbar_wait(odone, (jj - 1) & 1, 443, abort_flag);
-      if (named_bar_or(kBarXOr, kXThreads, !got)) {
-        ok = false;
-        *abort_flag = 1;
-        break;
-      }
-      if (raise && jj > 0) {  // O^T columns of this warp's heads, both M tiles
+      for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+      if (tid < 64) mst[tid] = kNoMax;
+      named_bar_sync(kBarX, kXThreads);  // the previous item's epilogue is done with the per-head state
+      for (int jj = 0; jj < it.nc; ++jj, ++g) {
+        const int bf = g & 1;
+        bool got = mbar_wait(sfull0 + 8 * bf, (g >> 1) & 1, 441, abort_flag);
         tc_fence_after();
-        uint32_t o[32];
-#pragma unroll 1
-        for (int mt = 0; mt < 2; ++mt) {
-          const uint32_t a = tmem + lane_base + 128 + 64 * mt + 32 * hh;
-          tmem_ld32(a, o);
-          tmem_wait_ld();
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + 64 * bf + 32 * hh, v);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(sfree0 + 8 * bf);
+        // Partial scores to the other CTA (asynchronous stores counted on its
+        // barrier), once it has read the previous ones.
+        got = got && (g == 0 || mbar_wait_cluster(sxfree, (g - 1) & 1, 445, abort_flag));
+        if (got) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac[32 * hh + i]);
-          tmem_st32(a, o);
+          for (int c = 0; c < 8; ++c)
+            cl_st_async_v4(sx_peer + sx_offset(qt, hh, lane, c),
+                           make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]), sxfull_peer);
         }
-        tmem_wait_st();
-      }
-      // MN-major (heads contiguous).
+        got = got && mbar_wait_cluster(sxfull, g & 1, 446, abort_flag);
+        // The key rows' validity (written by the gather warps before this chunk's tile).
+        got = got && mbar_wait(kfull_hi0 + 8 * bf, (g >> 1) & 1, 447, abort_flag);
+        if (named_bar_or(kBarXOr, kXThreads, !got)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        const bool kvalid = (vbits[(g & 7) * 4 + qt] >> lane) & 1u;
+        bool over = false;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(Pt + sw128_offset(row, 4 * hh + c)) =
-            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-      fence_proxy_async();
-      tc_fence_before();
-      mbar_arrive(pfull);
-    }
-    if (ok && nc > 0) {
-      ok = mbar_wait(odone, (nc - 1) & 1, 448, abort_flag);
-      ok = !named_bar_or(kBarXOr, kXThreads, !ok);
-    }
-    if (ok && nc > 0) {
+        for (int c = 0; c < 8; ++c) {
+          const uint4 wv = *reinterpret_cast<const uint4*>(Sx + sx_offset(qt, hh, lane, c));
+          const float4 m4 = *reinterpret_cast<const float4*>(mst + 32 * hh + 4 * c);
+          // Own partial + the other CTA's (IEEE addition is commutative: both
+          // CTAs get the same logit).
+          l[4 * c] = kvalid ? (__uint_as_float(v[4 * c]) + __uint_as_float(wv.x)) * P.scale_log2 : -INFINITY;
+          l[4 * c + 1] = kvalid ? (__uint_as_float(v[4 * c + 1]) + __uint_as_float(wv.y)) * P.scale_log2 : -INFINITY;
+          l[4 * c + 2] = kvalid ? (__uint_as_float(v[4 * c + 2]) + __uint_as_float(wv.z)) * P.scale_log2 : -INFINITY;
+          l[4 * c + 3] = kvalid ? (__uint_as_float(v[4 * c + 3]) + __uint_as_float(wv.w)) * P.scale_log2 : -INFINITY;
+          over |= (l[4 * c] > m4.x + kLazy) || (l[4 * c + 1] > m4.y + kLazy) || (l[4 * c + 2] > m4.z + kLazy) ||
+                  (l[4 * c + 3] > m4.w + kLazy);
+        }
+        // Every X thread has read its partials once past this barrier.
+        const bool raise = named_bar_or(kBarXOr, kXThreads, over);
+        if (tid == 0) {
+          if (jj + 1 < it.nc || more_after) mbar_arrive_expect_tx(sxfull, kSxBytes);  // the next chunk's partials
+          // This CTA's exchange buffer may take them: every read of it has
+          // completed (its values were used before the barrier above).
+          cl_arrive_remote_relaxed(sxfree_peer);
+        }
+        if (raise) {
+          // Raise the stabiliser to this chunk's per-head maximum where it is larger.
+          float mx[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx[i] = l[i];
+          warp_reduce_scatter32(mx, lane, [](float a, float c) { return fmaxf(a, c); });
+          red[qt * 64 + 32 * hh + lane] = mx[0];
+          named_bar_sync(kBarX, kXThreads);
+          if (tid < 64) {
+            const float cm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+            const float m_old = mst[tid];
+            const float m_new = fmaxf(m_old, cm);
+            fac[tid] = m_new == m_old ? 1.f : ex2(m_old - m_new);  // 0 on the first raise
+            mst[tid] = m_new;
+          }
+          named_bar_sync(kBarX, kXThreads);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] *= fac[32 * hh + i];
+        }
+        // P^T row of this key: heads 32*hh .. +31 as f16 (into registers first).
+        uint32_t pw[16];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 m4 = *reinterpret_cast<const float4*>(mst + 32 * hh + 4 * c);
+          __half2 h01 = __floats2half2_rn(ex2(l[4 * c] - m4.x), ex2(l[4 * c + 1] - m4.y));
+          __half2 h23 = __floats2half2_rn(ex2(l[4 * c + 2] - m4.z), ex2(l[4 * c + 3] - m4.w));
+          pw[2 * c] = *reinterpret_cast<uint32_t*>(&h01);
+          pw[2 * c + 1] = *reinterpret_cast<uint32_t*>(&h23);
+          const float2 b01 = __half22float2(h01), b23 = __half22float2(h23);  // the sums use exactly what the MMA sees
+          acc[4 * c] += b01.x;
+          acc[4 * c + 1] += b01.y;
+          acc[4 * c + 2] += b23.x;
+          acc[4 * c + 3] += b23.y;
+        }
+        // O^T and P^T are free once the previous chunk's O^T MMAs are done
+        // (for an item's first chunk, the previous item's last, which its
+        // epilogue already waited for).
+        got = jj == 0 || mbar_wait(odone, (g - 1) & 1, 443, abort_flag);
+        if (named_bar_or(kBarXOr, kXThreads, !got)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        if (raise && jj > 0) {  // O^T columns of this warp's heads, both M tiles
+          tc_fence_after();
+          uint32_t o[32];
+#pragma unroll 1
+          for (int mt = 0; mt < 2; ++mt) {
+            const uint32_t a = tmem + lane_base + 128 + 64 * mt + 32 * hh;
+            tmem_ld32(a, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac[32 * hh + i]);
+            tmem_st32(a, o);
+          }
+          tmem_wait_st();
+        }
+        // MN-major (heads contiguous).
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(Pt + sw128_offset(row, 4 * hh + c)) =
+              make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+        fence_proxy_async();
+        tc_fence_before();
+        named_bar_sync(kBarX, kXThreads);  // P^T complete (and O^T rescaled)
+        if (tid == 0) {
+          // O_r^T (+)= V_r^T P^T; an item's first chunk overwrites O^T. Frees
+          // the key tile quarter by quarter.
+          tc_fence_after();
+          const uint32_t kt = smem_u32(Kt + bf * kKtBytes), pt = smem_u32(Pt);
+#pragma unroll 1
+          for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t ad = sdesc(kt + mt * 32768 + ks * 2048, 16384, 1024, kSwizzle128B);
+              const uint64_t bd = sdesc(pt + ks * 2048, 16384, 1024, kSwizzle128B);
+              umma_f16(tmem + 128 + 64 * mt, ad, bd, id_o, (jj > 0 || ks > 0) ? 1u : 0u);
+            }
+            umma_commit((mt == 0 ? kfree_lo0 : kfree_hi0) + 8 * bf);
+          }
+          umma_commit(odone);
+        }
+      }
+      if (!ok) break;
+      // ---- this item's output ----
+      ok = mbar_wait(odone, (g - 1) & 1, 448, abort_flag);
+      if (named_bar_or(kBarXOr, kXThreads, !ok)) {
+        ok = false;
+        *abort_flag = 1;
+        break;
+      }
       tc_fence_after();
       // Per-head sums over the keys of all chunks (the same in both CTAs).
       warp_reduce_scatter32(acc, lane, [](float a, float c) { return a + c; });
@@ -609,15 +651,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
         if (rk == 0) {
           if (final_out) {
             if (P.lse)
-              P.lse[static_cast<int64_t>(q) * 64 + tid] =
+              P.lse[static_cast<int64_t>(it.q) * 64 + tid] =
                   s > 0.f ? (mst[tid] + log2f(s)) * 0.6931471805599453f : -INFINITY;
           } else {
-            P.stats[(static_cast<int64_t>(q) * kChunks + split) * 64 + tid] = make_float2(mst[tid], s);
+            P.stats[(static_cast<int64_t>(it.q) * kChunks + it.split) * 64 + tid] = make_float2(mst[tid], s);
           }
         }
       }
       named_bar_sync(kBarX, kXThreads);
-      float* part = P.part + (static_cast<int64_t>(q) * kChunks + split) * (64 * 512);
+      float* part = P.part + (static_cast<int64_t>(it.q) * kChunks + it.split) * (64 * 512);
 #pragma unroll 1
       for (int mt = 0; mt < 2; ++mt) {
         const int d = 256 * rk + 128 * mt + row;
@@ -630,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
           for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(v[i]) * lsum[32 * hh + i];
           if ((P.out_dtype & CSA2_OUT_DEROTATE) && d >= 448) {  // whole warps: rows 64..127 of the last M tile
             float cs, sn;
-            derotate_cs(t, (d - 448) >> 1, cs, sn);
+            derotate_cs(it.t, (d - 448) >> 1, cs, sn);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float other = __shfl_xor_sync(0xffffffffu, y[i], 1);
@@ -638,11 +680,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
             }
           }
           if ((P.out_dtype & ~CSA2_OUT_DEROTATE) == CSA2_OUT_F32) {
-            float* o = static_cast<float*>(P.out) + (static_cast<int64_t>(q) * 64 + 32 * hh) * 512 + d;
+            float* o = static_cast<float*>(P.out) + (static_cast<int64_t>(it.q) * 64 + 32 * hh) * 512 + d;
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i * 512] = y[i];
           } else {
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(P.out) + (static_cast<int64_t>(q) * 64 + 32 * hh) * 512 + d;
+            __nv_bfloat16* o =
+                static_cast<__nv_bfloat16*>(P.out) + (static_cast<int64_t>(it.q) * 64 + 32 * hh) * 512 + d;
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i * 512] = __float2bfloat16_rn(y[i]);
           }
@@ -652,6 +695,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
           for (int i = 0; i < 32; ++i) o[i * 512] = __uint_as_float(v[i]);
         }
       }
+      tc_fence_before();  // the O^T reads precede the next item's first O^T MMAs
+    }
+    if (tid == 0) {  // every O^T MMA issued has completed before TMEM is released
+      umma_commit(drain_o);
+      mbar_wait(drain_o, 0, 434);
     }
   }
 
@@ -796,8 +844,12 @@ cudaError_t launch_sparse_attn(const void* q, const int32_t* topk, const int64_t
   const size_t part_bytes = static_cast<size_t>(Q) * kChunks * 64 * 512 * sizeof(float);
   p.part = static_cast<float*>(ws);
   p.stats = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + ((part_bytes + 255) & ~size_t(255)));
-  cudaError_t e = launch_pdl(attn_kernel, dim3(static_cast<unsigned>(2 * p.nsplit), static_cast<unsigned>(Q)),
-                             dim3(kThreads), kSmemBytes, stream, 2, p);
+  // One CTA pair per SM pair, each walking its share of the work items (or
+  // one pair per item when there are fewer items than SM pairs).
+  p.n_items = static_cast<int>(Q * p.nsplit);
+  const int pairs = static_cast<int>(std::min<int64_t>(p.n_items, std::max(1, attn_num_sms() / 2)));
+  cudaError_t e = launch_pdl(attn_kernel, dim3(static_cast<unsigned>(2 * pairs)), dim3(kThreads), kSmemBytes, stream,
+                             2, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
   return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(Q), 64), dim3(256), 0, stream, 0,
                     static_cast<const float*>(p.part), static_cast<const float2*>(p.stats), p.nsplit, out_dtype,
