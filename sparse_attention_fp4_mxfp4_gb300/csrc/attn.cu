@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
   float* red = reinterpret_cast<float*>(misc + 1792);          // [4][64] per-lane-quarter partials
   // Key tile quarters: "lo" = dimensions 0-127 of the CTA's half (K-blocks 0-1), "hi" = 128-255.
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const uint32_t kfull_hi0 = bar(2), kfree_lo0 = bar(4), kfree_hi0 = bar(6);
+  const uint32_t qready = bar(0), kfull_hi0 = bar(2), kfree_lo0 = bar(4), kfree_hi0 = bar(6);
   const uint32_t sfull0 = bar(8), sfree0 = bar(10);
   const uint32_t odone = bar(12), drain_o = bar(13), sxfull = bar(14), sxfree = bar(15), drain = bar(16);
 
@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
     }
     mbar_init(odone, 1);
     mbar_init(drain_o, 1);
+    mbar_init(qready, kXThreads);  // the first item's Q, written by the softmax warps
     mbar_init(sxfull, 1);  // armed here with the bytes expected from the other CTA (st.async)
     mbar_init(sxfree, 1);  // one remote arrival per chunk: the other CTA has read its partials
     mbar_init(drain, 1);
@@ -417,8 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
     for (int w = pair; w < P.n_items && live; w += pairs) {
       const Item it = item_of(P, w);
       // Q of this item: the previous item's last S^T MMAs must have read Qs.
+      // The first item's Q is loaded by the softmax warps (idle until its
+      // first S^T), while these warps look up its keys.
       bool ok = g == 0 || mbar_wait(sfull0 + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1, 456, abort_flag);
-      if (ok) load_q(it);
+      if (ok && g > 0) load_q(it);
       if (named_bar_or(kBarG, kGThreads, !ok || *abort_flag)) {
         *abort_flag = 1;
         live = false;
@@ -439,8 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
         fence_proxy_async();
         named_bar_sync(kBarG, kGThreads);
         if (gt == 0 && mma_ok) {
-          // The S^T buffer is free once the softmax has read chunk g - 2 from it.
-          if (g >= 2 && !mbar_wait(sfree0 + 8 * bf, ph, 451, abort_flag)) {
+          // The S^T buffer is free once the softmax has read chunk g - 2 from
+          // it; the first S^T needs the first item's Q.
+          if ((g == 0 && !mbar_wait(qready, 0, 457, abort_flag)) ||
+              (g >= 2 && !mbar_wait(sfree0 + 8 * bf, ph, 451, abort_flag))) {
             mma_ok = false;
             *abort_flag = 1;
           } else {
@@ -492,6 +497,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
     float l[32], acc[32];
     bool ok = true;
     int g = 0;
+    if (pair < P.n_items) {
+      // The first item's half of Q (64 heads x 256 dims): 8 x 16 bytes per
+      // thread in one batch, bf16 -> f16 into the swizzled B operand.
+      const Item it0 = item_of(P, pair);
+      const uint4* qg = reinterpret_cast<const uint4*>(P.q + static_cast<int64_t>(it0.q) * 64 * 512);
+      uint4 qv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = tid + k * kXThreads;  // (head, 8-dim group) = (i >> 5, i & 31)
+        qv[k] = qg[(i >> 5) * 64 + 32 * rk + (i & 31)];
+      }
+      bool qbad = false;  // f16 holds |q| < 65520; larger or non-finite q is out of range
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = tid + k * kXThreads;
+        const int h = i >> 5, g8 = i & 31;
+        float f[8];
+        bf16x8_to_f32(qv[k], f);
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qbad |= !(fabsf(f[2 * e]) < 65520.f) || !(fabsf(f[2 * e + 1]) < 65520.f);
+          __half2 hv = __floats2half2_rn(f[2 * e], f[2 * e + 1]);
+          o[e] = *reinterpret_cast<uint32_t*>(&hv);
+        }
+        *reinterpret_cast<uint4*>(Qs + (g8 >> 3) * 8192 + sw128_offset(h, g8 & 7)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      if (qbad) report(CSA2_ERR_DEVICE_RANGE, 405);
+      fence_proxy_async();
+      mbar_arrive(qready);
+    }
     for (int w = pair; w < P.n_items && ok; w += pairs) {
       const Item it = item_of(P, w);
       const bool more_after = w + pairs < P.n_items;  // another item follows this one
