@@ -369,12 +369,14 @@ def test_host_validation_errors():
     assert e.value.status == csa2.ERR_WORKSPACE
 
 
+@pytest.mark.parametrize("N", [100000, 140000])
 @pytest.mark.parametrize("weights", ["zero", "mixed_sign"])
-def test_indexer_full_ties_and_mixed_sign_scores(weights):
+def test_indexer_full_ties_and_mixed_sign_scores(weights, N):
     """All scores tied (zero head weights: the lowest blocks and positions win)
-    and scores of both signs (negative head weights), at a context whose block
-    selection spans several CTAs of a cluster."""
-    N, B = 140000, 2
+    and scores of both signs (negative head weights), at a context whose
+    12,500 block maxima fit one CTA of the block selection and at one whose
+    17,500 span several CTAs of a cluster."""
+    B = 2
     wl = Workload(99, "t", "full", B=B, N=N, n_q=1)
     S = H.build(wl, DEV, shuffle_seed=17, prefill_step=True)
     L = S.layers[0]
