@@ -579,10 +579,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const AttnParams P) {
         }
         // Every X thread has read its partials once past this barrier.
         const bool raise = named_bar_or(kBarXOr, kXThreads, over);
-        if (tid == 0) {
-          if (jj + 1 < it.nc || more_after) mbar_arrive_expect_tx(sxfull, kSxBytes);  // the next chunk's partials
+        if (tid == 0 && (jj + 1 < it.nc || more_after)) {
+          mbar_arrive_expect_tx(sxfull, kSxBytes);  // the next chunk's partials
           // This CTA's exchange buffer may take them: every read of it has
-          // completed (its values were used before the barrier above).
+          // completed (its values were used before the barrier above). After
+          // the last chunk nobody waits for this.
           cl_arrive_remote_relaxed(sxfree_peer);
         }
         if (raise) {
