@@ -34,10 +34,18 @@
 // key (one thread per key) into registers ahead of time and dequantise them
 // (exactly) to f16 into the 128-byte-swizzled key tile, a quarter of the
 // dimensions (two K-blocks) at a time, so that a tile's first half is filled
-// while the tensor pipe still reads its second half for the chunk before, and
-// their thread 0 issues the MMAs (each S^T quarter right after the warps wrote
-// it, O^T once the softmax is done); warps 0-7 exchange partial scores, run
-// the softmax (thread = key row x 32 heads) and write the output.
+// while the tensor pipe still reads its second half for the chunk before;
+// their thread 0 issues each S^T quarter right after the warps wrote it.
+// Warps 0-7 exchange partial scores, run the softmax (thread = key row x 32
+// heads), write P^T, and their thread 0 issues the chunk's O^T MMAs; they
+// also write the output.
+//
+// The CTA pairs are persistent: pair p walks work items p, p + pairs, ...
+// with one running chunk counter, so barrier phases and buffers continue
+// across items. While an item's last chunk is in flight the gather warps look
+// up the next item's key slots and load its first keys, and they reload Q as
+// soon as the last S^T MMA that reads it has completed; the first item's Q is
+// loaded by the softmax warps, idle until its first S^T.
 //
 // The stabiliser is only raised when a chunk's logit exceeds it by more than
 // 8 (log2 units), as in lazy-rescaling flash attention: p = 2^(l - m) <= 256
