@@ -431,6 +431,7 @@ def run_e2e(args, wl, S, R, dev):
     its new entries and every layer's queries from pinned host memory, runs
     the layers with csa2_decode_group and reads every layer's output back."""
     import sparse_attention_fp4_mxfp4_gb300 as csa2
+    from sparse_attention_fp4_mxfp4_gb300.step import append_layers
     from sparse_attention_fp4_mxfp4_gb300.workload import append_main
     c = S.cache
     host = {"latent": S.step_latent, "key": S.step_idx_key}
@@ -485,7 +486,11 @@ def run_e2e(args, wl, S, R, dev):
                 topk=R.topk if L.kind != "reuse" or li == 0 else None,
                 swa_chunk=R.chunk[li] if wl.prefill else None, m=wl.m))
         ev = {k: torch.cuda.Event() for k in ("in_ready", "computed", "out_sent")}
-        sets.append(dict(din=din, dout=dout, hout=hout, dev_in=dev_in, args=args_list, ev=ev, used=False))
+        app = None
+        if R.fused_appends:
+            app = append_layers(S, swa=[dev_in[f"swa{li}"] for li in range(len(S.layers))],
+                                q_idx=[dev_in.get(f"qi{li}") for li in range(len(S.layers))])
+        sets.append(dict(din=din, dout=dout, hout=hout, dev_in=dev_in, args=args_list, app=app, ev=ev, used=False))
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(o.numel() * o.element_size() for o in R.out) + sum(x.numel() * 4 for x in R.lse)
     main = torch.cuda.current_stream()
@@ -493,14 +498,18 @@ def run_e2e(args, wl, S, R, dev):
 
     def compute(st):
         dev_in = st["dev_in"]
-        append_main(S, dev_in["latent"], dev_in["key"], dev_in.get("kv_gate"), dev_in.get("idx_gate"))
-        for li, L in enumerate(S.layers):
-            if wl.prefill:
-                csa2.csa2_quant_fp8_entries(dev_in[f"swa{li}"], R.chunk[li])
-            else:
-                csa2.csa2_append_swa(dev_in[f"swa{li}"], S.step_ring_idx[li], S.step_pos, c.rings)
-            if L.q_idx is not None:
-                csa2.csa2_quant_mxfp4(dev_in[f"qi{li}"], L.q_codes, L.q_scales)
+        if st["app"] is not None:
+            csa2.csa2_decode_appends(dev_in["latent"], dev_in["key"], S.step_seq, S.step_pos, c.block_table,
+                                     c.main_pages, c.idx_pages, st["app"])
+        else:
+            append_main(S, dev_in["latent"], dev_in["key"], dev_in.get("kv_gate"), dev_in.get("idx_gate"))
+            for li, L in enumerate(S.layers):
+                if wl.prefill:
+                    csa2.csa2_quant_fp8_entries(dev_in[f"swa{li}"], R.chunk[li])
+                else:
+                    csa2.csa2_append_swa(dev_in[f"swa{li}"], S.step_ring_idx[li], S.step_pos, c.rings)
+                if L.q_idx is not None:
+                    csa2.csa2_quant_mxfp4(dev_in[f"qi{li}"], L.q_codes, L.q_scales)
         csa2.csa2_decode_group(st["args"])
         if wl.prefill:
             for li, L in enumerate(S.layers):

@@ -166,6 +166,35 @@ int csa2_append_kv(const void* latent, const void* idx_key, const int32_t* seq_i
 int csa2_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, int T,
                     int64_t n_rings, uint8_t* rings, void* stream);
 
+/* One layer's share of csa2_decode_appends: its window entries and its
+ * indexer query. swa == NULL: no window append for this layer; q_idx == NULL:
+ * no quantisation. */
+typedef struct {
+  const void* swa;          /* bf16 [T, 512] window entries, 16-byte aligned, or NULL */
+  const int32_t* ring_idx;  /* int32 [T]: ring of each entry */
+  int64_t n_rings;
+  uint8_t* rings;           /* [n_rings, 128, 512], 16-byte aligned */
+  const void* q_idx;        /* bf16 [q_n] indexer query, 16-byte aligned, or NULL */
+  int64_t q_n;              /* a multiple of 16 */
+  uint8_t* q_codes;         /* [q_n / 2], 8-byte aligned */
+  uint8_t* q_scales;        /* [q_n / 16] */
+} csa2_append_layer;
+
+/* A decode step's stores and query quantisations in ONE kernel launch: the
+ * same bytes as csa2_append_kv(latent, idx_key, seq_idx, pos, T, ...) (main
+ * KV at one token per entry), then, for each of the n_layers layers,
+ * csa2_append_swa(swa, ring_idx, pos, T, n_rings, rings) and
+ * csa2_quant_mxfp4(q_idx, q_n, q_codes, q_scales). The parts run
+ * concurrently, so no part may write memory another part reads or writes
+ * (distinct rings per layer and distinct code buffers, as a decode step has).
+ * T = 0: only the quantisations run (latent .. idx_pages and every swa may
+ * then be NULL). n_layers <= 16 (else CSA2_ERR_UNSUPPORTED). Errors and
+ * device-side bounds reports are those of the three calls ([RN] 2.3 and
+ * [AB] 3.6 for the stores, [AB] 3.4 for the indexer query). */
+int csa2_decode_appends(const void* latent, const void* idx_key, const int32_t* seq_idx, const int64_t* pos, int T,
+                        const int32_t* block_table, int B, int max_pages, int64_t n_pages, uint8_t* main_pages,
+                        uint8_t* idx_pages, const csa2_append_layer* layers, int n_layers, void* stream);
+
 /* Encoder-side append at m tokens per entry (m = 1 or 2; [RN] 1 / [AB] 3.1
  * give m = 2 for the encoder's CSA2 layers; "DeepSeek-V4 model structure
  * (7)", KV cache of hybrid attention: an unfinished entry's tail tokens and

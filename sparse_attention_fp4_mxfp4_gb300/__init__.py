@@ -34,7 +34,7 @@ OP_INDEXER_FULL, OP_INDEXER_REINDEX, OP_SPARSE_ATTN, OP_DECODE_LAYER = 1, 2, 3, 
 # Exported entry points of include/csa2.h.
 EXPORTS = (
     "csa2_status_string", "csa2_last_error", "csa2_version", "csa2_page_bytes", "csa2_ring_bytes",
-    "csa2_workspace_bytes", "csa2_append_kv", "csa2_compress_append", "csa2_append_swa", "csa2_quant_fp8_entries",
+    "csa2_workspace_bytes", "csa2_append_kv", "csa2_decode_appends", "csa2_compress_append", "csa2_append_swa", "csa2_quant_fp8_entries",
     "csa2_ring_refill", "csa2_quant_mxfp4",
     "csa2_dequant_mxfp4", "csa2_quant_fp8", "csa2_indexer_scan", "csa2_block_topk",
     "csa2_indexer_reindex", "csa2_indexer_reindex_noalloc", "csa2_indexer_full", "csa2_sparse_attn", "csa2_sparse_attn_prefill", "csa2_decode_layer",
@@ -46,6 +46,15 @@ class Csa2Error(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(f"csa2 status {status}: {msg}")
         self.status = status
+
+
+class AppendLayer(ctypes.Structure):
+    """csa2_append_layer of include/csa2.h."""
+    _fields_ = [
+        ("swa", ctypes.c_void_p), ("ring_idx", ctypes.c_void_p), ("n_rings", ctypes.c_int64),
+        ("rings", ctypes.c_void_p), ("q_idx", ctypes.c_void_p), ("q_n", ctypes.c_int64),
+        ("q_codes", ctypes.c_void_p), ("q_scales", ctypes.c_void_p),
+    ]
 
 
 class LayerArgs(ctypes.Structure):
@@ -77,6 +86,7 @@ def _load():
         "csa2_ring_bytes": ([psz], i32),
         "csa2_workspace_bytes": ([i32, i32, i32, i64, psz], i32),
         "csa2_append_kv": ([p, p, p, p, i32, p, i32, i32, i64, p, p, p], i32),
+        "csa2_decode_appends": ([p, p, p, p, i32, p, i32, i32, i64, p, p, p, i32, p], i32),
         "csa2_compress_append": ([p, p, p, p, p, p, i32, i32, p, p, i32, i32, i64, p, p, p], i32),
         "csa2_append_swa": ([p, p, p, i32, i64, p, p], i32),
         "csa2_quant_fp8_entries": ([p, i32, p, p], i32),
@@ -170,6 +180,38 @@ def csa2_append_kv(latent, idx_key, seq_idx, pos, block_table, main_pages, idx_p
     _check(lib.csa2_append_kv(_ptr(latent), _ptr(idx_key), _ptr(seq_idx), _ptr(pos), T, _ptr(block_table),
                               block_table.shape[0], block_table.shape[1], main_pages.shape[0],
                               _ptr(main_pages), _ptr(idx_pages), _stream(stream)))
+
+
+def csa2_decode_appends(latent, idx_key, seq_idx, pos, block_table, main_pages, idx_pages, layers, stream=None):
+    """One launch for a decode step's stores and query quantisations: csa2_append_kv(latent, idx_key, seq_idx,
+    pos, ...) and, per entry of `layers` (dicts with optional keys swa, ring_idx, rings and q_idx, q_codes,
+    q_scales), csa2_append_swa(swa, ring_idx, pos, rings) and csa2_quant_mxfp4(q_idx, q_codes, q_scales)."""
+    _need(latent, "latent", torch.bfloat16, 2)
+    _need(idx_key, "idx_key", torch.bfloat16, 2)
+    _need(seq_idx, "seq_idx", torch.int32, 1)
+    _need(pos, "pos", torch.int64, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    T = latent.shape[0]
+    if latent.shape[1] != LATENT_DIM or idx_key.shape != (T, IDX_DIM) or seq_idx.numel() != T or pos.numel() != T:
+        raise ValueError("decode_appends: inconsistent shapes")
+    arr = (AppendLayer * max(1, len(layers)))()
+    for a, L in zip(arr, layers):
+        swa, q_idx = L.get("swa"), L.get("q_idx")
+        if swa is not None:
+            _need(swa, "swa", torch.bfloat16, 2)
+            _need(L["ring_idx"], "ring_idx", torch.int32, 1)
+            if swa.shape != (T, LATENT_DIM) or L["ring_idx"].numel() != T:
+                raise ValueError("decode_appends: inconsistent window shapes")
+            a.swa, a.ring_idx, a.n_rings, a.rings = _ptr(swa), _ptr(L["ring_idx"]), L["rings"].shape[0], _ptr(L["rings"])
+        if q_idx is not None:
+            _need(q_idx, "q_idx", torch.bfloat16)
+            n = q_idx.numel()
+            if L["q_codes"].numel() != n // 2 or L["q_scales"].numel() != n // 16:
+                raise ValueError("decode_appends: inconsistent query code shapes")
+            a.q_idx, a.q_n, a.q_codes, a.q_scales = _ptr(q_idx), n, _ptr(L["q_codes"]), _ptr(L["q_scales"])
+    _check(lib.csa2_decode_appends(_ptr(latent), _ptr(idx_key), _ptr(seq_idx), _ptr(pos), T, _ptr(block_table),
+                                   block_table.shape[0], block_table.shape[1], main_pages.shape[0], _ptr(main_pages),
+                                   _ptr(idx_pages), ctypes.cast(arr, ctypes.c_void_p), len(layers), _stream(stream)))
 
 
 def csa2_compress_append(kv, kv_gate, idx_key, idx_gate, seq_idx, pos, m, tail, block_table, main_pages, idx_pages,

@@ -189,16 +189,12 @@ __global__ void __launch_bounds__(256) compress_tail_kernel(
 }
 
 
-__global__ void __launch_bounds__(256) append_kv_kernel(
-    const uint16_t* __restrict__ latent, const uint16_t* __restrict__ idx_key,
-    const int32_t* __restrict__ seq_idx, const int64_t* __restrict__ pos, int T,
+// Entry tok of an MXFP4 append, by the 32 lanes of one warp.
+__device__ __forceinline__ void append_kv_entry(
+    int tok, int lane, const uint16_t* __restrict__ latent, const uint16_t* __restrict__ idx_key,
+    const int32_t* __restrict__ seq_idx, const int64_t* __restrict__ pos,
     const int32_t* __restrict__ block_table, int B, int max_pages, int64_t n_pages,
     uint8_t* __restrict__ main_pages, uint8_t* __restrict__ idx_pages) {
-  griddep_wait();
-  griddep_launch();
-  const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (tok >= T) return;
   // The entry's values do not depend on where it goes: load them first, so
   // their latency overlaps the position and page lookups.
   const uint4* lsrc = reinterpret_cast<const uint4*>(latent + static_cast<int64_t>(tok) * 512) + 2 * lane;
@@ -249,16 +245,24 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
   }
 }
 
-__global__ void __launch_bounds__(256) append_swa_kernel(const uint16_t* __restrict__ x,
-                                                         const int32_t* __restrict__ ring_idx,
-                                                         const int64_t* __restrict__ pos, int T,
-                                                         int64_t n_rings,
-                                                         uint8_t* __restrict__ rings) {
+__global__ void __launch_bounds__(256) append_kv_kernel(
+    const uint16_t* __restrict__ latent, const uint16_t* __restrict__ idx_key,
+    const int32_t* __restrict__ seq_idx, const int64_t* __restrict__ pos, int T,
+    const int32_t* __restrict__ block_table, int B, int max_pages, int64_t n_pages,
+    uint8_t* __restrict__ main_pages, uint8_t* __restrict__ idx_pages) {
   griddep_wait();
   griddep_launch();
   const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
   if (tok >= T) return;
+  append_kv_entry(tok, threadIdx.x & 31, latent, idx_key, seq_idx, pos, block_table, B, max_pages, n_pages,
+                  main_pages, idx_pages);
+}
+
+// Window entry tok (E4M3), by the 32 lanes of one warp.
+__device__ __forceinline__ void append_swa_entry(int tok, int lane, const uint16_t* __restrict__ x,
+                                                 const int32_t* __restrict__ ring_idx,
+                                                 const int64_t* __restrict__ pos, int64_t n_rings,
+                                                 uint8_t* __restrict__ rings) {
   // ring_idx == NULL: entry tok goes to row tok of a plain [T, 512] array
   // (a prefill chunk's own window entries).
   int64_t row = tok;
@@ -282,6 +286,18 @@ __global__ void __launch_bounds__(256) append_swa_kernel(const uint16_t* __restr
            (static_cast<uint32_t>(e4m3x2_from_f32(v[4 * i + 2], v[4 * i + 3])) << 16);
   uint8_t* dst = rings + row * 512 + 16 * lane;
   *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__global__ void __launch_bounds__(256) append_swa_kernel(const uint16_t* __restrict__ x,
+                                                         const int32_t* __restrict__ ring_idx,
+                                                         const int64_t* __restrict__ pos, int T,
+                                                         int64_t n_rings,
+                                                         uint8_t* __restrict__ rings) {
+  griddep_wait();
+  griddep_launch();
+  const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (tok >= T) return;
+  append_swa_entry(tok, threadIdx.x & 31, x, ring_idx, pos, n_rings, rings);
 }
 
 // Ring refill: entries [B][n][512] (E4M3) hold positions seq_len[b] - n ..
@@ -309,12 +325,9 @@ __global__ void __launch_bounds__(256) ring_refill_kernel(const uint8_t* __restr
   reinterpret_cast<uint4*>(rings + (static_cast<int64_t>(r) * 128 + (p & 127)) * 512)[lane] = v;
 }
 
-__global__ void quant_mxfp4_kernel(const uint16_t* __restrict__ x, int64_t nblocks,
-                                   uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
-  griddep_wait();
-  griddep_launch();
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= nblocks) return;
+// 16-value block i of an MXFP4 quantisation.
+__device__ __forceinline__ void quant_mxfp4_block(int64_t i, const uint16_t* __restrict__ x,
+                                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   const uint4* src = reinterpret_cast<const uint4*>(x + 16 * i);
   float v[16];
   bf16x8_to_f32(src[0], v);
@@ -324,6 +337,54 @@ __global__ void quant_mxfp4_kernel(const uint16_t* __restrict__ x, int64_t nbloc
   mxfp4_block(v, sc, lo, hi);
   *reinterpret_cast<uint2*>(codes + 8 * i) = make_uint2(lo, hi);
   scales[i] = sc;
+}
+
+__global__ void quant_mxfp4_kernel(const uint16_t* __restrict__ x, int64_t nblocks,
+                                   uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  griddep_wait();
+  griddep_launch();
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= nblocks) return;
+  quant_mxfp4_block(i, x, codes, scales);
+}
+
+// A decode step's appends and indexer-query quantisations in one launch
+// (the same work as append_kv_kernel, then append_swa_kernel per layer, then
+// quant_mxfp4_kernel per indexed layer; they touch disjoint memory). Block
+// ranges: [0, kv_blocks) append entries, 8 per block; then per layer its
+// window entries (8 per block) and its query's 16-value blocks (256 per block).
+__global__ void __launch_bounds__(256) decode_appends_kernel(const DecodeAppends P) {
+  griddep_wait();
+  griddep_launch();
+  const int tid = threadIdx.x, lane = tid & 31;
+  int blk = blockIdx.x;
+  if (blk < P.kv_blocks) {
+    const int tok = blk * 8 + (tid >> 5);
+    if (tok < P.T)
+      append_kv_entry(tok, lane, static_cast<const uint16_t*>(P.latent), static_cast<const uint16_t*>(P.idx_key),
+                      P.seq_idx, P.pos, P.block_table, P.B, P.max_pages, P.n_pages, P.main_pages, P.idx_pages);
+    return;
+  }
+  blk -= P.kv_blocks;
+  for (int l = 0; l < P.n_layers; ++l) {
+    const DecodeAppendsLayer& L = P.layer[l];
+    const int swa_blocks = L.swa ? (P.T + 7) / 8 : 0;
+    if (blk < swa_blocks) {
+      const int tok = blk * 8 + (tid >> 5);
+      if (tok < P.T)
+        append_swa_entry(tok, lane, static_cast<const uint16_t*>(L.swa), L.ring_idx, P.pos, L.n_rings, L.rings);
+      return;
+    }
+    blk -= swa_blocks;
+    const int64_t qb = L.q_idx ? L.q_n / 16 : 0;
+    const int q_blocks = static_cast<int>((qb + 255) / 256);
+    if (blk < q_blocks) {
+      const int64_t i = static_cast<int64_t>(blk) * 256 + tid;
+      if (i < qb) quant_mxfp4_block(i, static_cast<const uint16_t*>(L.q_idx), L.q_codes, L.q_scales);
+      return;
+    }
+    blk -= q_blocks;
+  }
 }
 
 __global__ void dequant_mxfp4_kernel(const uint8_t* __restrict__ codes,
@@ -374,6 +435,18 @@ cudaError_t launch_append_kv(const void* latent, const void* idx_key, const int3
   return launch_pdl(append_kv_kernel, dim3((T + 7) / 8), dim3(256), 0, stream, 0,
                     static_cast<const uint16_t*>(latent), static_cast<const uint16_t*>(idx_key), seq_idx, pos, T,
                     block_table, B, max_pages, n_pages, main_pages, idx_pages);
+}
+
+cudaError_t launch_decode_appends(const DecodeAppends& P, cudaStream_t stream) {
+  DecodeAppends p = P;
+  p.kv_blocks = (p.T + 7) / 8;
+  int64_t blocks = p.kv_blocks;
+  for (int l = 0; l < p.n_layers; ++l) {
+    if (p.layer[l].swa) blocks += (p.T + 7) / 8;
+    if (p.layer[l].q_idx) blocks += (p.layer[l].q_n / 16 + 255) / 256;
+  }
+  if (blocks == 0) return cudaSuccess;
+  return launch_pdl(decode_appends_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 0, p);
 }
 
 cudaError_t launch_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, int T,

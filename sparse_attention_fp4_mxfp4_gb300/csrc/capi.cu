@@ -149,6 +149,70 @@ int csa2_append_kv(const void* latent, const void* idx_key, const int32_t* seq_i
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "append_kv launch");
 }
 
+int csa2_decode_appends(const void* latent, const void* idx_key, const int32_t* seq_idx, const int64_t* pos, int T,
+                        const int32_t* block_table, int B, int max_pages, int64_t n_pages, uint8_t* main_pages,
+                        uint8_t* idx_pages, const csa2_append_layer* layers, int n_layers, void* stream) {
+  if (T < 0) return fail(CSA2_ERR_INVALID_ARG, "T = %d < 0", T);
+  if (n_layers < 0) return fail(CSA2_ERR_INVALID_ARG, "n_layers = %d < 0", n_layers);
+  if (n_layers > csa2::kMaxAppendLayers)
+    return fail(CSA2_ERR_UNSUPPORTED, "n_layers = %d > %d", n_layers, csa2::kMaxAppendLayers);
+  if (n_layers > 0) CHECK_PTR(layers, "layers");
+  csa2::DecodeAppends P{};
+  P.T = T;
+  if (T > 0) {
+    CHECK_A16(latent, "latent");
+    CHECK_A16(idx_key, "idx_key");
+    CHECK_PTR(seq_idx, "seq_idx");
+    CHECK_PTR(pos, "pos");
+    CHECK_A16(main_pages, "main_pages");
+    CHECK_A16(idx_pages, "idx_pages");
+    if (B < 1) return fail(CSA2_ERR_INVALID_ARG, "B = %d < 1", B);
+    if (int st = check_pages(block_table, max_pages, n_pages)) return st;
+  }
+  P.latent = latent;
+  P.idx_key = idx_key;
+  P.seq_idx = seq_idx;
+  P.pos = pos;
+  P.block_table = block_table;
+  P.B = B;
+  P.max_pages = max_pages;
+  P.n_pages = n_pages;
+  P.main_pages = main_pages;
+  P.idx_pages = idx_pages;
+  P.n_layers = n_layers;
+  for (int i = 0; i < n_layers; ++i) {
+    const csa2_append_layer& a = layers[i];
+    csa2::DecodeAppendsLayer& d = P.layer[i];
+    if (a.swa && T > 0) {
+      if (!aligned16(a.swa)) return fail(CSA2_ERR_INVALID_ARG, "layer %d: swa is not 16-byte aligned", i);
+      if (!a.ring_idx) return fail(CSA2_ERR_INVALID_ARG, "layer %d: ring_idx is NULL", i);
+      if (!a.rings || !aligned16(a.rings))
+        return fail(CSA2_ERR_INVALID_ARG, "layer %d: rings is NULL or not 16-byte aligned", i);
+      if (a.n_rings < 1) return fail(CSA2_ERR_INVALID_ARG, "layer %d: n_rings < 1", i);
+      d.swa = a.swa;
+      d.ring_idx = a.ring_idx;
+      d.n_rings = a.n_rings;
+      d.rings = a.rings;
+    }
+    if (a.q_idx) {
+      if (a.q_n < 0 || a.q_n % 16)
+        return fail(CSA2_ERR_INVALID_ARG, "layer %d: q_n = %lld is not a multiple of 16", i,
+                    static_cast<long long>(a.q_n));
+      if (!aligned16(a.q_idx)) return fail(CSA2_ERR_INVALID_ARG, "layer %d: q_idx is not 16-byte aligned", i);
+      if (!a.q_codes || (reinterpret_cast<uintptr_t>(a.q_codes) & 7u))
+        return fail(CSA2_ERR_INVALID_ARG, "layer %d: q_codes is NULL or not 8-byte aligned", i);
+      if (!a.q_scales) return fail(CSA2_ERR_INVALID_ARG, "layer %d: q_scales is NULL", i);
+      if (a.q_n > 0) {
+        d.q_idx = a.q_idx;
+        d.q_n = a.q_n;
+        d.q_codes = a.q_codes;
+        d.q_scales = a.q_scales;
+      }
+    }
+  }
+  cudaError_t e = csa2::launch_decode_appends(P, S(stream));
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "decode_appends launch");
+}
 int csa2_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, int T,
                     int64_t n_rings, uint8_t* rings, void* stream) {
   if (T < 0) return fail(CSA2_ERR_INVALID_ARG, "T = %d < 0", T);

@@ -33,6 +33,37 @@ cudaError_t launch_append_kv(const void* latent, const void* idx_key, const int3
                              const int64_t* pos, int T, const int32_t* block_table, int B,
                              int max_pages, int64_t n_pages, uint8_t* main_pages,
                              uint8_t* idx_pages, cudaStream_t stream);
+// One decode step's appends and indexer-query quantisations in one launch:
+// the main append (as launch_append_kv), then per layer its window entries
+// (as launch_append_swa, with the call's pos and T; swa == NULL: none) and
+// its query (as launch_quant_mxfp4; q_idx == NULL: none). kv_blocks is set
+// by the launcher.
+constexpr int kMaxAppendLayers = 16;
+struct DecodeAppendsLayer {
+  const void* swa;
+  const int32_t* ring_idx;
+  int64_t n_rings;
+  uint8_t* rings;
+  const void* q_idx;
+  int64_t q_n;
+  uint8_t* q_codes;
+  uint8_t* q_scales;
+};
+struct DecodeAppends {
+  const void* latent;
+  const void* idx_key;
+  const int32_t* seq_idx;
+  const int64_t* pos;
+  int T;
+  const int32_t* block_table;
+  int B, max_pages;
+  int64_t n_pages;
+  uint8_t* main_pages;
+  uint8_t* idx_pages;
+  int n_layers, kv_blocks;
+  DecodeAppendsLayer layer[kMaxAppendLayers];
+};
+cudaError_t launch_decode_appends(const DecodeAppends& P, cudaStream_t stream);
 // Encoder-side append at ratio m (1 or 2): entries from groups of m tokens
 // (softmax of their logits per channel), MXFP4 into entry pages; pending
 // tokens into tail [B][m-1][1280] bf16.

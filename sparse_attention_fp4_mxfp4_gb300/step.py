@@ -7,12 +7,27 @@ import torch
 from .workload import Setup, append_main
 
 
+def append_layers(S: Setup, swa=None, q_idx=None):
+    """csa2_decode_appends' per-layer arguments of a decode step: every
+    layer's window entries and, for FULL and REINDEX layers, its indexer
+    query (swa / q_idx: per-layer replacements of the step's own tensors)."""
+    out = []
+    for li, L in enumerate(S.layers):
+        d = {"swa": S.step_swa[li] if swa is None else swa[li], "ring_idx": S.step_ring_idx[li],
+             "rings": S.cache.rings}
+        if L.kind in ("full", "reindex"):
+            d.update(q_idx=L.q_idx if q_idx is None else q_idx[li], q_codes=L.q_codes, q_scales=L.q_scales)
+        out.append(d)
+    return out
+
+
 class Runner:
     """One decode step of a materialised workload, as bench.py times it: the
-    step's appends (A1, A2), then every layer in order. A FULL layer quantises
-    its indexer query, scans, selects the pool and the top-512; a REINDEX
-    layer quantises its query and rescores its pool; every layer then runs
-    sparse attention with the latest top-k, its own query and its own ring.
+    step's appends (A1, A2) and indexer-query quantisations (one launch at
+    one token per entry), then every layer in order. A FULL layer scans,
+    selects the pool and the top-512; a REINDEX layer rescores its pool;
+    every layer then runs sparse attention with the latest top-k, its own
+    query and its own ring.
 
     prefill=True runs the step's n_q tokens as one prefill chunk instead: each
     layer's window entries of the chunk are encoded to E4M3 into a chunk
@@ -45,6 +60,10 @@ class Runner:
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         self.attn_launches = 1 if Q >= 256 or min(5, max(1, sms // (2 * Q))) == 1 else 2
         self.prefill = prefill
+        # One launch for the step's stores and query quantisations (decode at
+        # one token per entry); otherwise one call each.
+        self.fused_appends = S.m == 1 and not prefill and len(S.layers) <= 16
+        self.append_args = append_layers(S) if self.fused_appends else None
         self.chunk = [torch.empty(B, n_q, 512, dtype=torch.uint8, device=dev) for _ in S.layers] if prefill else None
 
     def step(self, mark=None):
@@ -56,17 +75,22 @@ class Runner:
         csa2, S, c = self.csa2, self.S, self.S.cache
         mark = mark or (lambda name: None)
         n = 0
-        append_main(S)
-        n += 1 if S.m == 1 else 2
-        for li, L in enumerate(S.layers):
-            if self.prefill:
-                csa2.csa2_quant_fp8_entries(S.step_swa[li], self.chunk[li])
-            else:
-                csa2.csa2_append_swa(S.step_swa[li], S.step_ring_idx[li], S.step_pos, c.rings)
+        if self.fused_appends:
+            csa2.csa2_decode_appends(S.step_latent, S.step_idx_key, S.step_seq, S.step_pos, c.block_table,
+                                     c.main_pages, c.idx_pages, self.append_args)
             n += 1
-            if L.kind in ("full", "reindex"):
-                csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
+        else:
+            append_main(S)
+            n += 1 if S.m == 1 else 2
+            for li, L in enumerate(S.layers):
+                if self.prefill:
+                    csa2.csa2_quant_fp8_entries(S.step_swa[li], self.chunk[li])
+                else:
+                    csa2.csa2_append_swa(S.step_swa[li], S.step_ring_idx[li], S.step_pos, c.rings)
                 n += 1
+                if L.kind in ("full", "reindex"):
+                    csa2.csa2_quant_mxfp4(L.q_idx, L.q_codes, L.q_scales)
+                    n += 1
         for li, L in enumerate(S.layers):
             if L.kind == "full":
                 mark("scan0")

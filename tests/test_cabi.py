@@ -130,3 +130,27 @@ def test_tokens_per_entry_and_compressor_host_checks(lib):
     assert b"max_blocks" in lib.csa2_last_error()
     lib.csa2_block_topk.argtypes = [p, p, i32, i32, i64, p, i32, p]
     assert lib.csa2_block_topk(x, x, 1, 1, 10, x, 0, None) == 2
+
+
+def test_decode_appends_host_checks(lib):
+    """csa2_decode_appends rejects bad arguments before any device work."""
+    import sparse_attention_fp4_mxfp4_gb300 as m
+    p, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.csa2_decode_appends.argtypes = [p, p, p, p, i32, p, i32, i32, i64, p, p, p, i32, p]
+    x = p(4096)  # an aligned non-null address; no call below reaches the device
+    layers = (m.AppendLayer * 17)()
+    assert lib.csa2_decode_appends(x, x, x, x, -1, x, 1, 1, 1, x, x, layers, 1, None) == 1    # T < 0
+    assert lib.csa2_decode_appends(x, x, x, x, 1, x, 1, 1, 1, x, x, layers, -1, None) == 1    # n_layers < 0
+    assert lib.csa2_decode_appends(x, x, x, x, 1, x, 1, 1, 1, x, x, layers, 17, None) == 2    # > 16 layers
+    assert lib.csa2_decode_appends(x, x, x, x, 1, x, 1, 1, 1, x, x, None, 1, None) == 1       # layers NULL
+    assert lib.csa2_decode_appends(p(4100), x, x, x, 1, x, 1, 1, 1, x, x, layers, 0, None) == 1  # latent unaligned
+    assert lib.csa2_decode_appends(x, x, x, x, 1, x, 0, 1, 1, x, x, layers, 0, None) == 1     # B < 1
+    layers[0].swa, layers[0].ring_idx, layers[0].rings, layers[0].n_rings = 4096, None, 4096, 1
+    assert lib.csa2_decode_appends(x, x, x, x, 1, x, 1, 1, 1, x, x, layers, 1, None) == 1     # ring_idx NULL
+    layers[0].swa = None
+    layers[0].q_idx, layers[0].q_n, layers[0].q_codes, layers[0].q_scales = 4096, 24, 4096, 4096
+    assert lib.csa2_decode_appends(x, x, x, x, 1, x, 1, 1, 1, x, x, layers, 1, None) == 1     # q_n % 16
+    layers[0].q_n, layers[0].q_codes = 32, 4100
+    assert lib.csa2_decode_appends(x, x, x, x, 1, x, 1, 1, 1, x, x, layers, 1, None) == 1     # codes unaligned
+    # Nothing to do: no launch at all.
+    assert lib.csa2_decode_appends(None, None, None, None, 0, None, 0, 0, 0, None, None, None, 0, None) == 0

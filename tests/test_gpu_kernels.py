@@ -115,6 +115,39 @@ def test_append_pages_and_rings_bit_exact(N, n_q):
             assert np.array_equal(ring[np.arange(lo, N) % 128], want)
 
 
+@pytest.mark.parametrize("N,n_q,layers", [(1, 1, ("full",)), (1000, 3, ("reindex", "reuse", "full")),
+                                         (3000, 6, ("full", "reuse"))])
+def test_decode_appends_one_launch_bit_exact(N, n_q, layers):
+    """csa2_decode_appends (the step's stores and query quantisations in one
+    launch) writes the oracle's bytes: pages, every layer's ring, every
+    indexed layer's query codes."""
+    from sparse_attention_fp4_mxfp4_gb300.step import append_layers
+    wl = Workload(91, "t", "group", B=3, N=N, n_q=n_q, layers=layers)
+    S = H.build(wl, DEV, shuffle_seed=7, prefill_step=False)
+    c = S.cache
+    csa2.csa2_decode_appends(S.step_latent, S.step_idx_key, S.step_seq, S.step_pos, c.block_table, c.main_pages,
+                             c.idx_pages, append_layers(S))
+    torch.cuda.synchronize()
+    _status_ok()
+    for b in range(3):
+        pos = np.arange(N)
+        mc, ms = H.unpack_main(c, b, pos)
+        rc, rs = oracle.mxfp4_quant(synth.bf16_to_f32(synth.latent(wl.seed, b, 0, N)))
+        assert np.array_equal(mc, rc) and np.array_equal(ms, rs)
+        ic, is_ = H.unpack_idx(c, b, pos)
+        kc, ks = oracle.mxfp4_quant(synth.bf16_to_f32(synth.normal(wl.seed, synth.IDXKEY, b, 0, N, 128)))
+        assert np.array_equal(ic, kc) and np.array_equal(is_, ks)
+        for li in range(len(layers)):
+            lo = max(0, N - 128)
+            ring = c.rings[li * 3 + b].cpu().numpy()
+            want = oracle.fp8_quant(synth.bf16_to_f32(synth.latent(wl.seed, b, lo, N - lo, tensor=synth.SWA + li)))
+            assert np.array_equal(ring[np.arange(lo, N) % 128], want)
+    for L in S.layers:
+        if L.kind in ("full", "reindex"):
+            qc, qs = oracle.mxfp4_quant(synth.bf16_to_f32(L.q_idx_u16))
+            assert np.array_equal(L.q_codes.cpu().numpy(), qc) and np.array_equal(L.q_scales.cpu().numpy(), qs)
+
+
 # ---- indexer ---------------------------------------------------------------------------
 
 def _quant_q(S, L):
