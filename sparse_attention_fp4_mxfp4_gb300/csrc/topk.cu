@@ -271,8 +271,10 @@ __device__ __forceinline__ void radix_threshold(const Visit& visit, uint32_t k, 
 // ---- cluster version: the row lives in registers -----------------------------
 //
 // A cluster of C CTAs (C <= 16) selects from one row; CTA r keeps elements
-// [r * chunk, (r + 1) * chunk) of the row in registers as ordered keys (thread
-// t holds elements t + 1024 i), so the row is read from global memory once.
+// [r * chunk, (r + 1) * chunk) of the row buffer in registers as ordered keys
+// (thread t holds the 16 consecutive elements from 16 t), so the row is read
+// from global memory once. chunk follows from the buffer's row stride, not
+// from the token's length, so the loads are issued before the length is known.
 //
 // The threshold search first narrows the row to a candidate set with samples:
 // each warp sorts one sample per lane and takes the j-th largest, j chosen so
@@ -283,11 +285,11 @@ __device__ __forceinline__ void radix_threshold(const Visit& visit, uint32_t k, 
 // rows, heavy ties) every pass runs over the whole row: each CTA builds a local
 // histogram, every CTA sums all C histograms through distributed shared memory
 // and derives the same threshold digit. Either way the result is the same.
-// The ordered compaction counts, per (register slot i, warp), the keys above
-// and equal to the threshold with ballots; one prefix sum over those counts in
-// (i, warp) order, plus the counts of lower CTAs, gives every selected key its
-// output position in index order. Control flow is uniform across the cluster:
-// every CTA executes every cluster barrier.
+// The ordered compaction is one block prefix sum of each thread's packed
+// counts of keys above and equal to the threshold; with the counts of lower
+// CTAs it gives every selected key its output position in index order.
+// Control flow is uniform across the cluster: every CTA executes every cluster
+// barrier (a block barrier when the cluster is one CTA).
 constexpr int kChunk = 16384;  // elements per CTA at most
 constexpr int kMaxC = 16;
 constexpr int kSlots = kChunk / kThreads;  // register slots per thread
@@ -299,10 +301,7 @@ struct ClusterShared {
   uint32_t cand[kBlkCandMax];   // CTA 0: the candidates of the whole row
   uint32_t wred[4][32];         // per warp: min, max, valid count, sample statistic
   uint32_t woff[32];            // per warp: offset of its candidates within the CTA
-  // Rows padded to 33 words: warp 0's prefix pass reads 16 consecutive entries
-  // per lane, which with 32-word rows would put every second lane in one bank.
-  uint32_t cgt[kSlots][33];     // per (slot, warp): keys above T, then their prefix
-  uint32_t ceq[kSlots][33];     // per (slot, warp): keys equal to T, then their prefix
+  uint32_t wsel[2][32];         // per warp: packed (above, equal) counts, then their exclusive prefix
   uint32_t warp_sums[32];
   uint32_t xchg[16];            // read by other CTAs: 0-3 min/max/valid/sample median,
                                 // 4 candidate count, 5 slice total, 6-7 gt/eq counts,
@@ -370,17 +369,39 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
   const int q = blockIdx.y;
   const int b = q / n_q, j = q % n_q;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // CTA r's slice of the row buffer (the launcher makes C * kChunk >= row_stride).
+  const int chunk = static_cast<int>(((row_stride + C - 1) / C + 15) & ~int64_t(15));
+  const int lo = static_cast<int>(r) * chunk;
+  const int avail = static_cast<int>(max(int64_t(0), min(static_cast<int64_t>(chunk), row_stride - lo)));
+  const float* row = keys + static_cast<int64_t>(q) * row_stride + lo;
+  const int base = tid * kSlots;  // this thread's first element of the slice
+  float f[kSlots];
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && base + kSlots <= avail) {
+#pragma unroll
+    for (int i = 0; i < kSlots / 4; ++i) {
+      const float4 v = reinterpret_cast<const float4*>(row + base)[i];
+      f[4 * i] = v.x;
+      f[4 * i + 1] = v.y;
+      f[4 * i + 2] = v.z;
+      f[4 * i + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) f[i] = base + i < avail ? row[base + i] : -INFINITY;
+  }
   const int64_t t = ((seq_len[b] - n_q + j + 1) >> m_shift) - 1;  // the token's last visible entry
   int64_t n64 = t >= 0 ? (t + 8) / 8 : 0;
-  if (n64 > row_stride || n64 > static_cast<int64_t>(C) * kChunk) {
+  if (n64 > row_stride) {
     if (tid == 0 && r == 0) report(CSA2_ERR_DEVICE_BOUNDS, 311);
-    n64 = min(row_stride, static_cast<int64_t>(C) * kChunk);
+    n64 = row_stride;
   }
   const int n = static_cast<int>(n64);  // at most 16 * 16384
-  const int chunk = (n + C - 1) / C;
-  const int lo = static_cast<int>(r) * chunk;
-  const int m = max(0, min(n - lo, chunk));
-  const float* row = keys + static_cast<int64_t>(q) * row_stride + lo;
+  const int m = max(0, min(n - lo, chunk));  // valid elements of the slice
+  // One cluster-wide barrier; a block barrier when the cluster is one CTA.
+  auto csync = [&]() {
+    if (C > 1) cluster_sync_all();
+    else __syncthreads();
+  };
 
   // Sample statistic: the j-th largest of a warp's 32 samples sits near the
   // (j - 1/3) / (32 + 1/3) quantile; aim at 2k/n, j = floor((2k/n) 97/3 + 5/6),
@@ -390,16 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
   jrank = jrank < 1 ? 1 : (jrank > 32 ? 32 : jrank);
 
   uint32_t u[kSlots];
-  {
-    float f[kSlots];
 #pragma unroll
-    for (int it = 0; it < kSlots; ++it) {
-      const int i = tid + it * kThreads;
-      f[it] = i < m ? row[i] : -INFINITY;
-    }
-#pragma unroll
-    for (int it = 0; it < kSlots; ++it) u[it] = ordered_key(f[it]);
-  }
+  for (int it = 0; it < kSlots; ++it) u[it] = base + it < m ? ordered_key(f[it]) : 0u;
   const uint32_t smp = (lane & 1) ? u[kSlots / 2] : u[0];
   uint32_t vmin = 0xFFFFFFFFu, vmax = 0u, nvalid = 0u;
 #pragma unroll
@@ -432,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
       xchg[3] = med;
     }
   }
-  cluster_sync_all();
+  csync();
   if (warp == 0) {
     const bool in = lane < C;
     const uint32_t mn = __reduce_min_sync(0xffffffffu, in ? dsmem_ld(&xchg[0], lane) : 0xFFFFFFFFu);
@@ -479,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
         cs.woff[lane] = incl - wv;
         if (lane == 31) xchg[4] = incl;
       }
-      cluster_sync_all();
+      csync();
       if (warp == 0) {
         const uint32_t cr = lane < C ? dsmem_ld(&xchg[4], lane) : 0u;
         uint32_t incl = cr;
@@ -515,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
             ++pos;
           }
         }
-        cluster_sync_all();  // every candidate is in CTA 0
+        csync();  // every candidate is in CTA 0
         if (r == 0) {
           radix_threshold([&](auto&& fn) {
             for (int i = tid; i < static_cast<int>(n_cand); i += kThreads) fn(cs.cand[i]);
@@ -525,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
             xchg[9] = need_eq;
           }
         }
-        cluster_sync_all();  // CTA 0's threshold is published
+        csync();  // CTA 0's threshold is published
         if (tid == 0) {
           bc[6] = dsmem_ld(&xchg[8], 0);
           bc[7] = dsmem_ld(&xchg[9], 0);
@@ -549,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
           const uint32_t d = uu - umin;
           if (uu != 0u && (d & hmask) == pref) atomicAdd(&hist[(d >> shift) & (kBins - 1)], 1u);
         }
-        cluster_sync_all();  // every local histogram is complete
+        csync();  // every local histogram is complete
         // CTA r sums the bins of its slice [r * Sn, (r + 1) * Sn) over the cluster
         // (the last slice may be short); a single CTA uses its own histogram as is.
         const int Sn = (kBins + C - 1) / C;
@@ -569,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
           if (tid == 0) xchg[5] = slice_total;
           totals = tot;
         }
-        cluster_sync_all();  // slice sums complete; nobody reads a remote histogram any more
+        csync();  // slice sums complete; nobody reads a remote histogram any more
         // The slice that holds the remaining-th largest key (slices of higher ranks
         // hold higher digits), and the keys above it.
         if (warp == 0) {
@@ -632,51 +645,38 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
 
   // Ordered compaction. Keys equal to T are all valid when T > 0; when T = 0
   // every valid key is taken and need_eq = 0 takes no "equal" (invalid) key.
-  const uint32_t lt_mask = (1u << lane) - 1u;
+  // Index order is (CTA, thread, slot): one block prefix sum of the packed
+  // (above, equal) counts (16 bits each; a slice has at most 16384 of either).
+  uint32_t gm = 0, em = 0;  // per-slot masks: above T, equal to T
 #pragma unroll
   for (int it = 0; it < kSlots; ++it) {
-    const uint32_t gb = __ballot_sync(0xffffffffu, u[it] > T);
-    const uint32_t eb = __ballot_sync(0xffffffffu, u[it] == T);
-    if (lane == 0) {
-      cs.cgt[it][warp] = __popc(gb);
-      cs.ceq[it][warp] = __popc(eb);
-    }
+    gm |= (u[it] > T ? 1u : 0u) << it;
+    em |= (u[it] == T && u[it] != 0u ? 1u : 0u) << it;
   }
-  __syncthreads();
-  if (warp == 0) {  // exclusive prefixes over (slot, warp) order; lane l takes slot l / 2's half
-    constexpr int kPer = kSlots * 32 / 32;  // entries per lane
-    uint32_t gs = 0, es = 0;
+  const uint32_t v = (static_cast<uint32_t>(__popc(gm)) << 16) | static_cast<uint32_t>(__popc(em));
+  uint32_t incl = v;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int idx = lane * kPer + i;
-      gs += cs.cgt[idx / 32][idx % 32];
-      es += cs.ceq[idx / 32][idx % 32];
-    }
-    uint32_t gi = gs, ei = es;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) cs.wsel[0][warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t wt = cs.wsel[0][lane];
+    uint32_t wi = wt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t yg = __shfl_up_sync(0xffffffffu, gi, o), ye = __shfl_up_sync(0xffffffffu, ei, o);
-      if (lane >= o) {
-        gi += yg;
-        ei += ye;
-      }
+      const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
     }
-    uint32_t gr = gi - gs, er = ei - es;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int idx = lane * kPer + i;
-      const uint32_t g = cs.cgt[idx / 32][idx % 32], e = cs.ceq[idx / 32][idx % 32];
-      cs.cgt[idx / 32][idx % 32] = gr;
-      cs.ceq[idx / 32][idx % 32] = er;
-      gr += g;
-      er += e;
-    }
+    cs.wsel[1][lane] = wi - wt;
     if (lane == 31) {
-      xchg[6] = gi;
-      xchg[7] = ei;
+      xchg[6] = wi >> 16;      // keys above T in this CTA
+      xchg[7] = wi & 0xFFFFu;  // keys equal to T in this CTA
     }
   }
-  cluster_sync_all();
+  csync();
   if (warp == 0) {  // ties go to the lowest indices: CTA slices are in index order
     const uint32_t g = lane < C ? dsmem_ld(&xchg[6], lane) : 0u;
     const uint32_t e = lane < C ? dsmem_ld(&xchg[7], lane) : 0u;
@@ -698,25 +698,29 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
     if (lane == 0) bc[14] = gt_all + min(eq_all, need_eq);  // keys selected in the whole row
   }
   __syncthreads();
-  const uint32_t gt_cta = bc[12], eq_cta = bc[13], total_sel = bc[14];
+  const uint32_t total_sel = bc[14];
+  const uint32_t before = cs.wsel[1][warp] + incl - v;  // packed counts of lower threads of this CTA
+  const uint32_t gb = bc[12] + (before >> 16), eb = bc[13] + (before & 0xFFFFu);
+  // This thread's equal keys that are taken: the lowest min(popc, need_eq - eb) of them.
+  uint32_t take = need_eq > eb ? need_eq - eb : 0u;
+  uint32_t sel = gm, rest = em;
+  while (take > 0u && rest != 0u) {
+    const uint32_t lowest = rest & (0u - rest);
+    sel |= lowest;
+    rest ^= lowest;
+    --take;
+  }
   int32_t* orow = out + static_cast<int64_t>(q) * k;
-#pragma unroll
-  for (int it = 0; it < kSlots; ++it) {
-    const bool is_gt = u[it] > T;
-    const bool is_eq = u[it] == T;
-    const uint32_t gb = __ballot_sync(0xffffffffu, is_gt);
-    const uint32_t eb = __ballot_sync(0xffffffffu, is_eq);
-    const uint32_t eq_before = eq_cta + cs.ceq[it][warp] + __popc(eb & lt_mask);
-    const bool take = is_gt || (is_eq && eq_before < need_eq);
-    if (take) {
-      const uint32_t gt_before = gt_cta + cs.cgt[it][warp] + __popc(gb & lt_mask);
-      const uint32_t pos = gt_before + min(eq_before, need_eq);
-      if (pos < static_cast<uint32_t>(k)) orow[pos] = lo + tid + it * kThreads;  // never past the row
-    }
+  uint32_t pos = gb + min(eb, need_eq);
+  while (sel != 0u) {
+    const int i = __ffs(sel) - 1;
+    sel &= sel - 1u;
+    if (pos < static_cast<uint32_t>(k)) orow[pos] = lo + base + i;  // never past the row
+    ++pos;
   }
   if (r == 0)
     for (int i = static_cast<int>(min(total_sel, static_cast<uint32_t>(k))) + tid; i < k; i += kThreads) orow[i] = -1;
-  cluster_sync_all();  // keep this CTA's shared memory alive until every remote read is done
+  csync();  // keep this CTA's shared memory alive until every remote read is done
 }
 
 constexpr size_t kClusterSmem = sizeof(ClusterShared);
