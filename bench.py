@@ -42,10 +42,10 @@ METRIC_PREFILL = "chunked-prefill tokens/s of a CSA2 Full layer at context N; % 
 # ncu DRAM traffic of the dominant kernel, per launch, with the hash of the
 # sources it was measured on (reported as null once those sources change).
 NCU_TRAFFIC = {
-    # profiles/indexer_scan_b4_n1m.txt: 303.06 MB read + 4.79 MB written for 4 x 1M
+    # profiles/indexer_scan_b4_n1m.txt: 303.05 MB read + 4.91 MB written for 4 x 1M
     # positions; traffic grows with the positions scanned, so x2 for 8 x 1M.
-    ("indexer_scan", 3): {"bytes_per_launch": 2 * (303.057152e6 + 4.785408e6),
-                          "files": ['indexer.cu', 'sm103.cuh'], "hash": "0ba1c125bab376d0"},
+    ("indexer_scan", 3): {"bytes_per_launch": 2 * (303.047424e6 + 4.906752e6),
+                          "files": ['indexer.cu', 'sm103.cuh'], "hash": "e200950964d05106"},
 }
 
 def source_hash(files):

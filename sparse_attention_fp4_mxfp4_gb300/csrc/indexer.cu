@@ -180,24 +180,32 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
 
   // Pool rescore: the source (page * 16 + block in page, or kNoSlot) and the
   // causal positions of pool slot e of this CTA's tiles.
-  auto resolve_slot = [&](int e) {
-    const int64_t t_q = ((seq_n - P.n_q + jq + 1) >> P.m_shift) - 1;  // the token's last visible entry
-    const int32_t blk = P.pool[(static_cast<int64_t>(b) * P.n_q + jq) * 2048 + first_tile * 16 + e];
+  const int64_t t_slot = ((seq_n - P.n_q + jq + 1) >> P.m_shift) - 1;  // pool mode: the token's last visible entry
+  const int32_t* pool_row = kPool ? P.pool + (static_cast<int64_t>(b) * P.n_q + jq) * 2048 + first_tile * 16 : nullptr;
+  // The page of pool block blk (-1: not causal or not mapped).
+  auto slot_page = [&](int32_t blk) -> int32_t {
+    if (blk < 0 || static_cast<int64_t>(blk) * 8 > t_slot) return -1;
+    const int64_t lp = static_cast<int64_t>(blk) >> 4;
+    return lp < P.max_pages ? P.block_table[static_cast<int64_t>(b) * P.max_pages + lp] : -2;
+  };
+  auto store_slot = [&](int e, int32_t blk, int32_t page) {
     uint32_t src = kNoSlot;
     int nv = 0;
-    if (blk >= 0 && static_cast<int64_t>(blk) * 8 <= t_q) {
-      const int64_t lp = static_cast<int64_t>(blk) >> 4;
-      const int32_t page = lp < P.max_pages ? P.block_table[static_cast<int64_t>(b) * P.max_pages + lp] : -1;
+    if (page != -1) {
       if (page < 0 || page >= P.n_pages) {
         report(CSA2_ERR_DEVICE_BOUNDS, 203);
       } else {
         src = static_cast<uint32_t>(page) * 16u + static_cast<uint32_t>(blk & 15);
-        const int64_t left = t_q - static_cast<int64_t>(blk) * 8 + 1;
+        const int64_t left = t_slot - static_cast<int64_t>(blk) * 8 + 1;
         nv = left < 8 ? static_cast<int>(left) : 8;
       }
     }
     slot_src[e] = src;
     slot_n[e] = static_cast<uint8_t>(nv);
+  };
+  auto resolve_slot = [&](int e) {
+    const int32_t blk = pool_row[e];
+    store_slot(e, blk, slot_page(blk));
   };
   // The pool producer resolves the first two tiles' slots itself and starts;
   // warps 0-3 resolve the rest and meet it at named barrier 2 before tile 2.
@@ -225,7 +233,24 @@ __global__ void __launch_bounds__(threads_for(kSub), kSub == 1 ? 4 : 1) indexer_
       wsm[i] = P.w[(static_cast<int64_t>(b) * P.n_q + jj) * 32 + (i & 31)];
     }
     if (kPool) {
-      for (int e = 32 + tid; e < n_tiles * 16; e += 128) resolve_slot(e);
+      // Slots 32.. in batches of 8 per thread: the batch's pool reads, then
+      // its page-table reads, so each batch costs two dependent round trips.
+      const int n_slots = static_cast<int>(n_tiles) * 16;
+      for (int e0 = 32 + tid; e0 < n_slots; e0 += 8 * 128) {
+        int32_t blk[8], page[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int e = e0 + r * 128;
+          blk[r] = e < n_slots ? pool_row[e] : -1;
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) page[r] = slot_page(blk[r]);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int e = e0 + r * 128;
+          if (e < n_slots) store_slot(e, blk[r], page[r]);
+        }
+      }
       if (pool_split) named_bar_sync(2, 160);
     }
     fence_proxy_async();
