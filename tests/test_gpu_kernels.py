@@ -175,7 +175,9 @@ def test_indexer_scan_block_max(N, n_q, B):
             assert (got[b, j, nb:] == 12345.0).all(), "scan wrote past the causal blocks"
 
 
-@pytest.mark.parametrize("N,n_q,B", [(1, 1, 1), (600, 1, 2), (4097, 2, 2), (20000, 1, 2), (40000, 3, 1)])
+# (6000, 8, 20): 160 tokens, more than the SMs: the selections run in two waves of CTAs.
+@pytest.mark.parametrize("N,n_q,B", [(1, 1, 1), (600, 1, 2), (4097, 2, 2), (20000, 1, 2), (40000, 3, 1),
+                                     (6000, 8, 20)])
 def test_indexer_full_pool_and_topk(N, n_q, B):
     wl = Workload(92, "t", "full", B=B, N=N, n_q=n_q)
     S = H.build(wl, DEV, shuffle_seed=5, prefill_step=True)
@@ -198,7 +200,7 @@ def test_indexer_full_pool_and_topk(N, n_q, B):
             assert set(gt[b, j][gt[b, j] >= 0].tolist()) <= pool_pos
 
 
-@pytest.mark.parametrize("N,n_q,B", [(700, 1, 2), (20000, 1, 3), (50000, 6, 1)])
+@pytest.mark.parametrize("N,n_q,B", [(700, 1, 2), (20000, 1, 3), (50000, 6, 1), (20000, 8, 20)])
 def test_indexer_reindex(N, n_q, B):
     wl = Workload(93, "t", "reindex", B=B, N=N, n_q=n_q, layers=("reindex",))
     S = H.build(wl, DEV, shuffle_seed=9, prefill_step=True)
