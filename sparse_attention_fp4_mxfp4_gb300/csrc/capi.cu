@@ -9,6 +9,7 @@
 
 #include "csa2.h"
 #include "kernels.h"
+#include <nvtx3/nvToolsExt.h>
 
 namespace {
 
@@ -79,6 +80,17 @@ int record_error(int code, const char* msg) { return fail(code, "%s", msg); }
 
 extern "C" {
 
+// Every compute call of the C ABI opens an NVTX range named after it, so that
+// a profiler tracing NVTX shows the library's calls around their kernels
+// (without such a tool attached a push and a pop cost a few nanoseconds).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define CSA2_NVTX_RANGE() NvtxRange csa2_nvtx_range_(__func__)
+
 const char* csa2_status_string(int status) {
   switch (status) {
     case CSA2_OK: return "ok";
@@ -134,6 +146,7 @@ int csa2_workspace_bytes(int op, int B, int n_q, int64_t max_ctx, size_t* bytes)
 int csa2_append_kv(const void* latent, const void* idx_key, const int32_t* seq_idx,
                    const int64_t* pos, int T, const int32_t* block_table, int B, int max_pages,
                    int64_t n_pages, uint8_t* main_pages, uint8_t* idx_pages, void* stream) {
+  CSA2_NVTX_RANGE();
   if (T < 0) return fail(CSA2_ERR_INVALID_ARG, "T = %d < 0", T);
   if (T == 0) return CSA2_OK;
   CHECK_A16(latent, "latent");
@@ -152,6 +165,7 @@ int csa2_append_kv(const void* latent, const void* idx_key, const int32_t* seq_i
 int csa2_decode_appends(const void* latent, const void* idx_key, const int32_t* seq_idx, const int64_t* pos, int T,
                         const int32_t* block_table, int B, int max_pages, int64_t n_pages, uint8_t* main_pages,
                         uint8_t* idx_pages, const csa2_append_layer* layers, int n_layers, void* stream) {
+  CSA2_NVTX_RANGE();
   if (T < 0) return fail(CSA2_ERR_INVALID_ARG, "T = %d < 0", T);
   if (n_layers < 0) return fail(CSA2_ERR_INVALID_ARG, "n_layers = %d < 0", n_layers);
   if (n_layers > csa2::kMaxAppendLayers)
@@ -215,6 +229,7 @@ int csa2_decode_appends(const void* latent, const void* idx_key, const int32_t* 
 }
 int csa2_append_swa(const void* x, const int32_t* ring_idx, const int64_t* pos, int T,
                     int64_t n_rings, uint8_t* rings, void* stream) {
+  CSA2_NVTX_RANGE();
   if (T < 0) return fail(CSA2_ERR_INVALID_ARG, "T = %d < 0", T);
   if (T == 0) return CSA2_OK;
   CHECK_A16(x, "x");
@@ -230,6 +245,7 @@ int csa2_compress_append(const void* kv, const void* kv_gate, const void* idx_ke
                          const int32_t* seq_idx, const int64_t* pos, int T, int m, void* tail,
                          const int32_t* block_table, int B, int max_pages, int64_t n_pages,
                          uint8_t* main_pages, uint8_t* idx_pages, void* stream) {
+  CSA2_NVTX_RANGE();
   if (T < 0) return fail(CSA2_ERR_INVALID_ARG, "T = %d < 0", T);
   if (int st = check_ratio(m)) return st;
   if (T == 0) return CSA2_OK;
@@ -250,6 +266,7 @@ int csa2_compress_append(const void* kv, const void* kv_gate, const void* idx_ke
 }
 
 int csa2_quant_fp8_entries(const void* x, int T, uint8_t* out, void* stream) {
+  CSA2_NVTX_RANGE();
   if (T < 0) return fail(CSA2_ERR_INVALID_ARG, "T = %d < 0", T);
   if (T == 0) return CSA2_OK;
   CHECK_A16(x, "x");
@@ -260,6 +277,7 @@ int csa2_quant_fp8_entries(const void* x, int T, uint8_t* out, void* stream) {
 
 int csa2_ring_refill(const uint8_t* entries, const int64_t* seq_len, int B, int n,
                      const int32_t* ring_idx, int64_t n_rings, uint8_t* rings, void* stream) {
+  CSA2_NVTX_RANGE();
   if (B < 0 || B > CSA2_MAX_TOKENS) return fail(CSA2_ERR_INVALID_ARG, "B = %d out of range", B);
   if (n < 0) return fail(CSA2_ERR_INVALID_ARG, "n = %d < 0", n);
   if (B == 0 || n == 0) return CSA2_OK;
@@ -273,6 +291,7 @@ int csa2_ring_refill(const uint8_t* entries, const int64_t* seq_len, int B, int 
 }
 
 int csa2_quant_mxfp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales, void* stream) {
+  CSA2_NVTX_RANGE();
   if (n < 0 || n % 16) return fail(CSA2_ERR_INVALID_ARG, "n = %lld is not a multiple of 16", static_cast<long long>(n));
   if (n == 0) return CSA2_OK;
   CHECK_A16(x, "x");
@@ -285,6 +304,7 @@ int csa2_quant_mxfp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales, 
 
 int csa2_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t n, float* out,
                        void* stream) {
+  CSA2_NVTX_RANGE();
   if (n < 0 || n % 16) return fail(CSA2_ERR_INVALID_ARG, "n = %lld is not a multiple of 16", static_cast<long long>(n));
   if (n == 0) return CSA2_OK;
   CHECK_PTR(codes, "codes");
@@ -296,6 +316,7 @@ int csa2_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t n, f
 }
 
 int csa2_quant_fp8(const float* x, int64_t n, uint8_t* out, void* stream) {
+  CSA2_NVTX_RANGE();
   if (n < 0) return fail(CSA2_ERR_INVALID_ARG, "n < 0");
   if (n == 0) return CSA2_OK;
   CHECK_PTR(x, "x");
@@ -320,6 +341,7 @@ int csa2_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales, const flo
                       const int32_t* block_table, int max_pages, int64_t n_pages,
                       const uint8_t* idx_pages, float* block_max, int64_t max_blocks, int m,
                       void* stream) {
+  CSA2_NVTX_RANGE();
   if (int st = check_batch(B, n_q)) return st;
   if (int st = check_ratio(m)) return st;
   if (B == 0) return CSA2_OK;
@@ -335,6 +357,7 @@ int csa2_indexer_scan(const uint8_t* q_codes, const uint8_t* q_scales, const flo
 
 int csa2_block_topk(const float* block_max, const int64_t* seq_len, int B, int n_q,
                     int64_t max_blocks, int32_t* pool, int m, void* stream) {
+  CSA2_NVTX_RANGE();
   if (int st = check_batch(B, n_q)) return st;
   if (int st = check_ratio(m)) return st;
   if (B == 0) return CSA2_OK;
@@ -373,6 +396,7 @@ int csa2_indexer_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const 
                          int max_pages, int64_t n_pages, const uint8_t* idx_pages,
                          const int32_t* pool, int32_t* topk, void* ws, size_t ws_bytes, int m,
                          void* stream) {
+  CSA2_NVTX_RANGE();
   if (int st = csa2::check_reindex(q_codes, q_scales, w, seq_len, B, n_q, block_table, max_pages, n_pages,
                                    idx_pages, pool, topk, m))
     return st;
@@ -393,6 +417,7 @@ int csa2_indexer_full(const uint8_t* q_codes, const uint8_t* q_scales, const flo
                       const int32_t* block_table, int max_pages, int64_t n_pages,
                       const uint8_t* idx_pages, int32_t* pool, int32_t* topk, void* ws,
                       size_t ws_bytes, int m, void* stream) {
+  CSA2_NVTX_RANGE();
   if (int st = check_batch(B, n_q)) return st;
   if (int st = check_ratio(m)) return st;
   if (B == 0) return CSA2_OK;
@@ -452,6 +477,7 @@ int csa2_sparse_attn(const void* q, const int32_t* topk, const int64_t* seq_len,
                      const uint8_t* main_pages, const uint8_t* rings, const int32_t* ring_idx,
                      int64_t n_rings, float softmax_scale, int out_dtype, void* out, float* lse,
                      void* ws, size_t ws_bytes, int m, void* stream) {
+  CSA2_NVTX_RANGE();
   return sparse_attn(q, topk, seq_len, B, n_q, block_table, max_pages, n_pages, main_pages, rings, ring_idx,
                      n_rings, nullptr, softmax_scale, out_dtype, out, lse, ws, ws_bytes, m, stream);
 }
@@ -462,6 +488,7 @@ int csa2_sparse_attn_prefill(const void* q, const int32_t* topk, const int64_t* 
                              const int32_t* ring_idx, int64_t n_rings, const uint8_t* swa_chunk,
                              float softmax_scale, int out_dtype, void* out, float* lse, void* ws,
                              size_t ws_bytes, int m, void* stream) {
+  CSA2_NVTX_RANGE();
   CHECK_A16(swa_chunk, "swa_chunk");
   return sparse_attn(q, topk, seq_len, B, n_q, block_table, max_pages, n_pages, main_pages, rings, ring_idx,
                      n_rings, swa_chunk, softmax_scale, out_dtype, out, lse, ws, ws_bytes, m, stream);
@@ -498,11 +525,13 @@ static int run_layer(const csa2_layer_args* a, int32_t* pool, int32_t* topk, voi
 }
 
 int csa2_decode_layer(const csa2_layer_args* layer, void* stream) {
+  CSA2_NVTX_RANGE();
   CHECK_PTR(layer, "layer");
   return run_layer(layer, layer->pool, layer->topk, stream);
 }
 
 int csa2_decode_group(const csa2_layer_args* layers, int n_layers, void* stream) {
+  CSA2_NVTX_RANGE();
   CHECK_PTR(layers, "layers");
   if (n_layers < 1) return fail(CSA2_ERR_INVALID_ARG, "n_layers < 1");
   int32_t* latest_pool = nullptr;

@@ -12,6 +12,7 @@
 // library holds it until the process exits. In host code its name is only a
 // host-side stand-in, so the device address is looked up once per device with
 // cudaGetSymbolAddress (with that device current) and passed to the kernels.
+#include <nvtx3/nvToolsExt.h>
 #include <cstdio>
 #include <mutex>
 
@@ -42,6 +43,10 @@ int csa2_indexer_reindex_noalloc(const uint8_t* q_codes, const uint8_t* q_scales
                                  const int32_t* block_table, int max_pages, int64_t n_pages,
                                  const uint8_t* idx_pages, const int32_t* pool, int32_t* topk, int m,
                                  void* stream) {
+  nvtxRangePushA(__func__);
+  struct Pop {
+    ~Pop() { nvtxRangePop(); }
+  } pop;
   // The same checks (and status codes) as csa2_indexer_reindex, then the
   // limit of the fixed scratch array.
   if (int st = csa2::check_reindex(q_codes, q_scales, w, seq_len, B, n_q, block_table, max_pages, n_pages,
