@@ -148,6 +148,56 @@ def test_decode_appends_one_launch_bit_exact(N, n_q, layers):
             assert np.array_equal(L.q_codes.cpu().numpy(), qc) and np.array_equal(L.q_scales.cpu().numpy(), qs)
 
 
+def test_decode_appends_without_entries_quantises_only():
+    """T = 0: no page or window store, every indexed layer's query codes still written."""
+    wl = Workload(98, "t", "group", B=2, N=700, n_q=2, layers=("full", "reuse", "reindex"))
+    S = H.build(wl, DEV, shuffle_seed=2, prefill_step=True)
+    c = S.cache
+    pages_before = (c.main_pages.clone(), c.idx_pages.clone(), c.rings.clone())
+    layers = [{"q_idx": L.q_idx, "q_codes": L.q_codes, "q_scales": L.q_scales} if L.kind != "reuse" else {}
+              for L in S.layers]
+    empty_bf16 = torch.empty(0, 512, dtype=torch.bfloat16, device=DEV)
+    csa2.csa2_decode_appends(empty_bf16, torch.empty(0, 128, dtype=torch.bfloat16, device=DEV),
+                             torch.empty(0, dtype=torch.int32, device=DEV), torch.empty(0, dtype=torch.int64, device=DEV),
+                             c.block_table, c.main_pages, c.idx_pages, layers)
+    torch.cuda.synchronize()
+    _status_ok()
+    assert torch.equal(c.main_pages, pages_before[0]) and torch.equal(c.idx_pages, pages_before[1])
+    assert torch.equal(c.rings, pages_before[2])
+    for L in S.layers:
+        if L.kind != "reuse":
+            qc, qs = oracle.mxfp4_quant(synth.bf16_to_f32(L.q_idx_u16))
+            assert np.array_equal(L.q_codes.cpu().numpy(), qc) and np.array_equal(L.q_scales.cpu().numpy(), qs)
+
+
+def test_decode_appends_unmapped_page_sets_the_bounds_status():
+    """An entry whose page is unmapped is skipped and reported; the other entries and parts are stored."""
+    from sparse_attention_fp4_mxfp4_gb300.step import append_layers
+    wl = Workload(99, "t", "full", B=2, N=300, n_q=1)
+    S = H.build(wl, DEV, shuffle_seed=2, prefill_step=False)
+    c = S.cache
+    torch.cuda.synchronize()
+    assert csa2.csa2_check_device_status() == csa2.OK
+    bt = c.block_table.clone()
+    bt[0, 299 // 128] = -1  # sequence 0's new entry (position 299) has no page
+    csa2.csa2_decode_appends(S.step_latent, S.step_idx_key, S.step_seq, S.step_pos, bt, c.main_pages, c.idx_pages,
+                             append_layers(S))
+    torch.cuda.synchronize()
+    assert csa2.csa2_check_device_status() == csa2.ERR_DEVICE_BOUNDS
+    assert csa2.csa2_check_device_status() == csa2.OK  # cleared by the read
+    # Sequence 1's entry, both window entries and the query codes are stored.
+    mc, ms = H.unpack_main(c, 1, np.arange(300))
+    rc, rs = oracle.mxfp4_quant(synth.bf16_to_f32(synth.latent(wl.seed, 1, 0, 300)))
+    assert np.array_equal(mc, rc) and np.array_equal(ms, rs)
+    for b in range(2):
+        ring = c.rings[b].cpu().numpy()
+        want = oracle.fp8_quant(synth.bf16_to_f32(synth.latent(wl.seed, b, 299, 1, tensor=synth.SWA)))
+        assert np.array_equal(ring[299 % 128], want[0])
+    L = S.layers[0]
+    qc, qs = oracle.mxfp4_quant(synth.bf16_to_f32(L.q_idx_u16))
+    assert np.array_equal(L.q_codes.cpu().numpy(), qc) and np.array_equal(L.q_scales.cpu().numpy(), qs)
+
+
 # ---- indexer ---------------------------------------------------------------------------
 
 def _quant_q(S, L):
@@ -177,7 +227,7 @@ def test_indexer_scan_block_max(N, n_q, B):
 
 # (6000, 8, 20): 160 tokens, more than the SMs: the selections run in two waves of CTAs.
 @pytest.mark.parametrize("N,n_q,B", [(1, 1, 1), (600, 1, 2), (4097, 2, 2), (20000, 1, 2), (40000, 3, 1),
-                                     (6000, 8, 20)])
+                                     (9000, 8, 2), (6000, 8, 20)])
 def test_indexer_full_pool_and_topk(N, n_q, B):
     wl = Workload(92, "t", "full", B=B, N=N, n_q=n_q)
     S = H.build(wl, DEV, shuffle_seed=5, prefill_step=True)
@@ -224,7 +274,8 @@ def test_indexer_reindex(N, n_q, B):
 # ---- attention ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("N,n_q,B,out", [(1, 1, 1, "f32"), (5, 1, 2, "f32"), (100, 3, 2, "f32"), (600, 1, 2, "f32"),
-                                         (5000, 1, 3, "f32"), (5000, 6, 2, "f32"), (5000, 2, 2, "bf16")])
+                                         (5000, 1, 3, "f32"), (5000, 6, 2, "f32"), (5000, 2, 2, "bf16"),
+                                         (3000, 8, 2, "f32")])
 def test_sparse_attention(N, n_q, B, out):
     wl = Workload(94, "t", "reuse", B=B, N=N, n_q=n_q, layers=("reuse",))
     S = H.build(wl, DEV, shuffle_seed=11, prefill_step=True)
