@@ -181,15 +181,17 @@ constexpr int kBins = 1 << kDigit;
 struct SelectShared {
   uint32_t hist[kBins];
   uint32_t wtot[32];  // per-warp bin totals
-  uint32_t bc[4];     // crossing warp and keys above it; selected bin and keys above it
+  uint32_t bc[5];     // crossing warp and keys above it; selected bin, keys above it and keys in it
 };
 
 // The bin that holds the remaining-th largest counted key, scanning bins from
-// the top, and the number of keys in the bins above it; every thread gets both.
+// the top, the number of keys in the bins above it and in it; every thread
+// gets all three.
 // Warp w owns 128 consecutive bins from the top, lane l four of them; warp 0
 // finds the warp whose range holds the crossing, that warp finds the bin.
 // Three barriers; the block has 32 warps.
-__device__ __forceinline__ void find_bin(SelectShared& S, uint32_t remaining, uint32_t& bin, uint32_t& above) {
+__device__ __forceinline__ void find_bin(SelectShared& S, uint32_t remaining, uint32_t& bin, uint32_t& above,
+                                         uint32_t& in_bin) {
   constexpr int kR = kBins / 32, kL = kR / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t c[kL], own = 0;
@@ -228,6 +230,7 @@ __device__ __forceinline__ void find_bin(SelectShared& S, uint32_t remaining, ui
       if (before < remaining && before + c[i] >= remaining) {
         S.bc[2] = static_cast<uint32_t>(kBins - 1 - (warp * kR + lane * kL + i));
         S.bc[3] = before;
+        S.bc[4] = c[i];
       }
       before += c[i];
     }
@@ -235,12 +238,17 @@ __device__ __forceinline__ void find_bin(SelectShared& S, uint32_t remaining, ui
   __syncthreads();
   bin = S.bc[2];
   above = S.bc[3];
+  in_bin = S.bc[4];
 }
 
 // Radix select over the valid keys >= lo (all of them <= hi) that visit()
-// hands to its callback: T = the k-th largest of them (at least k exist) and
-// need_eq = how many keys equal to T the top k take. Digits of 12 bits from
-// the top of the span hi - lo; at most three passes.
+// hands to its callback: T and need_eq such that the keys > T plus the first
+// need_eq keys equal to T are the top k (at least k exist). Digits of 12 bits
+// from the top of the span hi - lo; at most three passes. It stops early when
+// the bin holding the k-th largest key holds exactly the keys still needed:
+// every key from that bin's lower bound up is then taken, exactly k keys with
+// no tie across the boundary, so T = that bound - 1 and need_eq = 0 select the
+// same set as the exact k-th largest would.
 template <class Visit>
 __device__ __forceinline__ void radix_threshold(const Visit& visit, uint32_t k, uint32_t lo, uint32_t hi,
                                                 SelectShared& S, uint32_t& T, uint32_t& need_eq) {
@@ -256,11 +264,16 @@ __device__ __forceinline__ void radix_threshold(const Visit& visit, uint32_t k, 
       if (u != 0u && u >= lo && (d & hmask) == pref) atomicAdd(&S.hist[(d >> shift) & (kBins - 1)], 1u);
     });
     __syncthreads();
-    uint32_t bin, above;
-    find_bin(S, remaining, bin, above);
+    uint32_t bin, above, in_bin;
+    find_bin(S, remaining, bin, above, in_bin);
     remaining -= above;
     pref |= bin << shift;
     hmask = ~((1u << shift) - 1u);
+    if (in_bin == remaining) {  // the whole bin is taken
+      T = lo + pref - 1u;
+      need_eq = 0u;
+      return;
+    }
     if (shift == 0) break;
     shift = shift > kDigit ? shift - kDigit : 0;
   }
@@ -553,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
       const int bits = span ? 32 - __clz(span) : 0;
       int shift = bits > kDigit ? bits - kDigit : 0;
       uint32_t pref = 0u, hmask = 0u, remaining = static_cast<uint32_t>(k);
+      bool whole_bin = false;  // stopped early: every key from the selected bin up is taken
       for (int pass = 0; pass < 3; ++pass) {
         for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
         __syncthreads();
@@ -627,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
           if (rank < Sn && before < remaining && before + c4[it] >= remaining) {
             bc[10] = static_cast<uint32_t>(static_cast<int>(target) * Sn + (Sn - 1 - rank));
             bc[11] = before;
+            bc[15] = c4[it];
           }
           before += c4[it];
         }
@@ -634,12 +649,15 @@ __global__ void __launch_bounds__(kThreads, 1) cluster_topk_kernel(const float* 
         remaining -= bc[11];
         pref |= bc[10] << shift;
         hmask = ~((1u << shift) - 1u);
+        // The same cluster-wide counts in every CTA: all stop at the same pass.
+        whole_bin = bc[15] == remaining;
         __syncthreads();
-        if (shift == 0) break;
+        if (whole_bin || shift == 0) break;
         shift = shift > kDigit ? shift - kDigit : 0;
       }
-      T = umin + pref;
-      need_eq = remaining;
+      // Stopped early (see radix_threshold): T = the bin's lower bound - 1, no equal keys.
+      T = whole_bin ? umin + pref - 1u : umin + pref;
+      need_eq = whole_bin ? 0u : remaining;
     }
   }
 
